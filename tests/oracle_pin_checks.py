@@ -1,0 +1,262 @@
+"""Pin checks for the CPU oracle: each check compares the oracle with
+something other than itself (a value the pages print, a clause of IEEE 754,
+a closed form, brute force on tiny inputs, a library sort on a special case).
+
+Every check takes the ctypes library to test, so that the mutant test can run
+the same checks against copies of the oracle with planted mistakes.
+"""
+from __future__ import annotations
+
+import json
+import os
+import random
+
+import numpy as np
+
+import oracle
+from tests import _pins
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_bits(name):
+    out = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                out.append(int(line, 16))
+    return out
+
+
+def check_total_order_golden(lib=None):
+    """IEEE 754-2019 5.10 order of hand-listed bit patterns (bf16 and fp32)."""
+    for name, dtype in (("total_order_bf16.txt", oracle.BF16), ("total_order_fp32.txt", oracle.FP32)):
+        seq = _read_bits(name)
+        for i, a in enumerate(seq):
+            for j, b in enumerate(seq):
+                want = (i > j) - (i < j)
+                got = oracle.total_order_cmp(a, b, dtype, lib=lib)
+                assert got == want, f"{name}: cmp({a:#x}, {b:#x}) = {got}, want {want}"
+
+
+def check_total_order_exhaustive_bf16(lib=None):
+    """Every bf16 bit pattern, sorted by an independent Python key (float
+    widening by bit shift); the oracle must agree on each adjacent pair."""
+    pats = sorted(range(1 << 16), key=lambda b: _pins.order_key(b, True))
+    keys = [_pins.order_key(b, True) for b in pats]
+    for a, b, ka, kb in zip(pats, pats[1:], keys, keys[1:]):
+        want = -1 if ka < kb else 0
+        got = oracle.total_order_cmp(a, b, oracle.BF16, lib=lib)
+        assert got == want, f"cmp({a:#06x}, {b:#06x}) = {got}, want {want}"
+
+
+def check_total_order_random_fp32(lib=None, n=20000, seed=5):
+    rng = random.Random(seed)
+    specials = _read_bits("total_order_fp32.txt")
+    for _ in range(n):
+        a = rng.choice(specials) if rng.random() < 0.2 else rng.getrandbits(32)
+        b = rng.choice(specials) if rng.random() < 0.2 else rng.getrandbits(32)
+        ka, kb = _pins.order_key(a, False), _pins.order_key(b, False)
+        want = (ka > kb) - (ka < kb)
+        got = oracle.total_order_cmp(a, b, oracle.FP32, lib=lib)
+        assert got == want, f"cmp({a:#x}, {b:#x}) = {got}, want {want}"
+
+
+def check_causal_pages_golden(lib=None):
+    rows = []
+    with open(os.path.join(GOLDEN, "causal_pages.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                p, n = line.split()
+                rows.append((int(p), int(n)))
+    # decode form, query length 1: position = seq_len - 1
+    for pos, pages in rows:
+        got = oracle.num_valid_pages_decode([pos + 1], 1, lib=lib)[0]
+        assert got == pages, f"decode pos {pos}: {got} != {pages}"
+    # decode form, query length 8: the row of local_q = 7 sits at seq_len - 1
+    for pos, pages in rows:
+        got = oracle.num_valid_pages_decode([pos + 1], 8, lib=lib)[7]
+        assert got == pages, f"decode dql=8 pos {pos}: {got} != {pages}"
+    # varlen form: one-token sequences at position prefix_len
+    ok = [(p, n) for p, n in rows if p >= 0]
+    cu = list(range(len(ok) + 1))
+    got = oracle.num_valid_pages_varlen(cu, [p for p, _ in ok], lib=lib)
+    assert list(got) == [n for _, n in ok], (list(got), ok)
+
+
+def check_varlen_prefill_positions(lib=None):
+    """A 300-token chunk after a 100-token prefix: positions 100..399."""
+    got = oracle.num_valid_pages_varlen([0, 300], [100], lib=lib)
+    want = [(100 + j + 1 + 127) // 128 for j in range(300)]  # closed form of ceil
+    assert list(got) == want
+
+
+def _worked_example():
+    with open(os.path.join(GOLDEN, "spec_decode_sparse_table.json")) as f:
+        return json.load(f)
+
+
+def check_spec_decode_worked_example(lib=None):
+    ex = _worked_example()
+    dql = ex["decode_query_len"]
+    idx = np.array(ex["topk_idx"], dtype=np.int32)[:, None, :]
+    bt, ctx = oracle.build_sparse_block_table(idx, ex["block_table"], ex["seq_lens"], dql, lib=lib)
+    assert list(ctx[:, 0]) == ex["expected_ctx"], list(ctx[:, 0])
+    width = ex["row_width"]
+    assert bt.shape == (12, 1, width)
+    for r, pref in enumerate(ex["expected_bt_nonzero_prefix"]):
+        want = pref + [0] * (width - len(pref))
+        assert list(bt[r, 0]) == want, (r, list(bt[r, 0]))
+    # the page's padded-request rows: empty context, all-zero table
+    assert (bt[8:] == 0).all() and (ctx[8:] == 0).all()
+    nvp = oracle.num_valid_pages_decode(ex["seq_lens"], dql, lib=lib)
+    assert list(nvp) == [3, 3, 3, 3, 2, 2, 2, 2, 0, 0, 0, 0]
+
+
+def check_table_duplicates_ignored(lib=None):
+    """A repeated id counts once (same table and ctx as the deduplicated row)."""
+    seq = [700]
+    table = [[3, 9, 27, 81, 243, 729]]
+    a = np.array([[[4, 1, 4, 1, 5, -1]]], dtype=np.int32)
+    b = np.array([[[4, 1, 5, -1, -1, -1]]], dtype=np.int32)
+    ta, ca = oracle.build_sparse_block_table(a, table, seq, 1, lib=lib)
+    tb, cb = oracle.build_sparse_block_table(b, table, seq, 1, lib=lib)
+    assert (ta == tb).all() and (ca == cb).all()
+    # position 699, causal 700: blocks 1, 4 full (256), block 5 holds 60 tokens
+    assert ca[0, 0] == 128 + 128 + 60
+    row = list(ta[0, 0])
+    assert row[:8] == [9 * 8 + p for p in range(8)]
+    assert row[8:16] == [243 * 8 + p for p in range(8)]
+    assert row[16:20] == [729 * 8 + p for p in range(4)] and row[20:24] == [0] * 4
+
+
+def check_table_full_selection_covers_causal_len(lib=None, seed=3):
+    """When every causal block is selected, ctx equals the causal length and
+    the table is the request's block list expanded page by page."""
+    rng = np.random.default_rng(seed)
+    for _ in range(50):
+        dql = int(rng.integers(1, 5))
+        seq = int(rng.integers(0, 2000))
+        nblk = 20
+        table = rng.integers(0, 1 << 20, size=(1, nblk)).astype(np.int32)
+        K = nblk
+        ids = np.tile(np.arange(K, dtype=np.int32), (dql, 1))[:, None, :]
+        bt, ctx = oracle.build_sparse_block_table(ids, table, [seq], dql, lib=lib)
+        for q in range(dql):
+            causal = max(seq - dql + q + 1, 0)
+            assert ctx[q, 0] == causal
+            npages = -(-causal // 16)
+            flat = [int(table[0, p // 8]) * 8 + p % 8 for p in range(npages)]
+            assert list(bt[q, 0, :npages]) == flat
+            assert (bt[q, 0, npages:] == 0).all()
+
+
+def _rand_row_bits(rng, v, is_bf16, palette_frac=0.5):
+    """Row of bit patterns mixing a small palette (ties, NaN, +-0, +-Inf) and
+    random finite values."""
+    if is_bf16:
+        pal = [0x7FC0, 0xFFC0, 0x7F81, 0xFF81, 0x7F80, 0xFF80, 0x0000, 0x8000, 0x3F80,
+               0xBF80, 0x4000, 0x3F80]
+        rnd = lambda: int(rng.integers(0, 1 << 16))
+    else:
+        pal = [0x7FC00000, 0xFFC00000, 0x7F800001, 0xFF800001, 0x7F800000, 0xFF800000,
+               0x0, 0x80000000, 0x3F800000, 0xBF800000, 0x40000000]
+        rnd = lambda: int(rng.integers(0, 1 << 32))
+    return [pal[int(rng.integers(0, len(pal)))] if rng.random() < palette_frac else rnd()
+            for _ in range(v)]
+
+
+def check_select_brute_force(lib=None, trials=400, seed=11):
+    """Tiny rows: the oracle's set is the unique subset that holds every
+    forced id and whose non-forced members beat every excluded id."""
+    rng = np.random.default_rng(seed)
+    for trial in range(trials):
+        is_bf16 = bool(trial % 2)
+        M = int(rng.integers(1, 10))
+        nvp = int(rng.integers(0, M + 3))
+        v = min(nvp, M)
+        I = int(rng.integers(0, 3))
+        L = int(rng.integers(0, 3))
+        K = int(rng.integers(max(1, I + L), max(1, I + L) + M + 3))
+        row = _rand_row_bits(rng, M, is_bf16)
+        arr = np.array(row, dtype=np.uint16 if is_bf16 else np.uint32).reshape(1, 1, M)
+        got = oracle.topk_select(arr, [nvp], K, I, L, lib=lib)[0, 0]
+        n = min(K, v)
+        sols = _pins.brute_force_select(row, v, K, I, L, is_bf16)
+        assert len(sols) == 1, (trial, row, v, K, I, L, sols)
+        assert list(got[:n]) == sols[0], (trial, row, v, K, I, L, list(got), sols)
+        assert (got[n:] == -1).all(), (trial, list(got))
+
+
+def check_select_lexsort_special_case(lib=None, trials=200, seed=12):
+    """NaN-free fp32 rows without zeros: selection = numpy lexsort on
+    (forced desc, value desc, id asc), then ascending ids."""
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        M = int(rng.integers(1, 300))
+        v = int(rng.integers(0, M + 1))
+        I = int(rng.integers(0, 3))
+        L = int(rng.integers(0, 4))
+        K = int(rng.integers(max(1, I + L), max(I + L, 1) + 40))
+        vals = (rng.integers(1, 12, size=M) * rng.choice([-1, 1], size=M)).astype(np.float32)
+        arr = vals.reshape(1, 1, M)
+        got = oracle.topk_select(arr, [v], K, I, L, lib=lib)[0, 0]
+        ids = np.arange(v)
+        forced = (ids < I) | (ids >= v - L)
+        order = np.lexsort((ids, -vals[:v].astype(np.float64), -forced.astype(np.int64)))
+        n = min(K, v)
+        want = np.sort(order[:n])
+        assert list(got[:n]) == list(want) and (got[n:] == -1).all()
+
+
+def check_select_short_rows_take_everything(lib=None):
+    """v <= K: the selection is every causal block, whatever the scores."""
+    rng = np.random.default_rng(4)
+    for v in range(0, 17):
+        arr = rng.standard_normal((1, 1, 32)).astype(np.float32)
+        got = oracle.topk_select(arr, [v], 16, 1, 1, lib=lib)[0, 0]
+        assert list(got) == list(range(v)) + [-1] * (16 - v)
+
+
+def check_select_forced_blocks(lib=None):
+    """Init and local blocks are kept even when they hold the lowest scores."""
+    M = 40
+    vals = np.linspace(1.0, 2.0, M, dtype=np.float32)
+    vals[0] = -np.inf
+    vals[36:40] = -1e30
+    arr = vals.reshape(1, 1, M)
+    got = oracle.topk_select(arr, [40], 8, 1, 2, lib=lib)[0, 0]
+    # forced: 0 (init), 38, 39 (local); the other 5 are the largest: 31..35
+    assert list(got) == [0, 31, 32, 33, 34, 35, 38, 39], list(got)
+    got = oracle.topk_select(arr, [37], 8, 2, 1, lib=lib)[0, 0]
+    # v = 37: forced 0, 1 and 36; best others 31..35
+    assert list(got) == [0, 1, 31, 32, 33, 34, 35, 36], list(got)
+
+
+def check_select_ties_lower_id(lib=None):
+    arr = np.zeros((1, 1, 20), dtype=np.float32)
+    got = oracle.topk_select(arr, [20], 4, 0, 0, lib=lib)[0, 0]
+    assert list(got) == [0, 1, 2, 3]
+    arr[0, 0, 7] = 1.0
+    arr[0, 0, 5] = -0.0
+    got = oracle.topk_select(arr, [20], 4, 0, 0, lib=lib)[0, 0]
+    assert list(got) == [0, 1, 2, 7]
+
+
+ALL_CHECKS = [
+    check_total_order_golden,
+    check_total_order_exhaustive_bf16,
+    check_total_order_random_fp32,
+    check_causal_pages_golden,
+    check_varlen_prefill_positions,
+    check_spec_decode_worked_example,
+    check_table_duplicates_ignored,
+    check_table_full_selection_covers_causal_len,
+    check_select_brute_force,
+    check_select_lexsort_special_case,
+    check_select_short_rows_take_everything,
+    check_select_forced_blocks,
+    check_select_ties_lower_id,
+]

@@ -1,0 +1,90 @@
+"""Plants plausible mistakes into copies of the oracle (on the CPU) and
+checks that at least one pin catches each.  This is evidence that the pins
+constrain every part of the oracle: the total order, the causal bound, the
+forced blocks, the tie-break, the output layout and the table expansion."""
+import os
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from tests import oracle_pin_checks as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "bsa_oracle.c")
+
+# (name, original text, mutated text)
+MUTANTS = [
+    ("zero_sign_ignored",
+     "if (a.value == 0.0 && a.negative != b.negative) return a.negative ? -1 : 1;", ""),
+    ("nan_sign_flipped",
+     "if (a.is_nan) return a.negative ? -1 : 1;", "if (a.is_nan) return a.negative ? 1 : -1;"),
+    ("negative_nan_payload_order",
+     "if (a.negative) return a_smaller ? 1 : -1;", "if (a.negative) return a_smaller ? -1 : 1;"),
+    ("page_rounding",
+     "(len + ORACLE_PAGE_SIZE - 1) / ORACLE_PAGE_SIZE", "(len + ORACLE_PAGE_SIZE) / ORACLE_PAGE_SIZE"),
+    ("causal_len_off_by_one",
+     "int64_t causal_len = pos + 1 > 0 ? pos + 1 : 0;\n            out[req * dql + q]",
+     "int64_t causal_len = pos > 0 ? pos : 0;\n            out[req * dql + q]"),
+    ("varlen_position",
+     "int64_t pos = (int64_t)prefix_lens[i] + (row - cu_seqlens_q[i]);",
+     "int64_t pos = (int64_t)prefix_lens[i] + (row - cu_seqlens_q[i]) - 1;"),
+    ("local_window_short",
+     "(b >= v - num_local)", "(b > v - num_local)"),
+    ("init_window_long",
+     "(b < num_init)", "(b <= num_init)"),
+    ("tie_break_higher_id",
+     "return (a->id > b->id) - (a->id < b->id);", "return (a->id < b->id) - (a->id > b->id);"),
+    ("descending_output",
+     "return (a > b) - (a < b);", "return (a < b) - (a > b);"),
+    ("tail_zero_not_minus_one",
+     "dst[i] = i < n ? chosen[i] : -1;", "dst[i] = i < n ? chosen[i] : 0;"),
+    ("forced_not_first",
+     "if (a->forced != b->forced) return a->forced ? -1 : 1;", ""),
+    ("order_reversed",
+     "if (c != 0) return -c;", "if (c != 0) return c;"),
+    ("table_page_bound_inclusive",
+     "(int64_t)p * ORACLE_SUB_PAGE < causal_len", "(int64_t)p * ORACLE_SUB_PAGE <= causal_len"),
+    ("table_ctx_full_blocks",
+     "ctx += tokens < ORACLE_PAGE_SIZE ? tokens : ORACLE_PAGE_SIZE;", "ctx += ORACLE_PAGE_SIZE;"),
+    ("table_accepts_causal_edge",
+     "b >= num_blocks ||", "b > num_blocks ||"),
+    ("table_keeps_duplicates",
+     "if (!dup) blocks[n++] = b;", "(void)dup; blocks[n++] = b;"),
+    ("table_phys_scale",
+     "bt[j * ORACLE_PAGES_PER_BLOCK + p] = phys * ORACLE_PAGES_PER_BLOCK + p;",
+     "bt[j * ORACLE_PAGES_PER_BLOCK + p] = phys + p;"),
+    ("table_row_mapping",
+     "int64_t local_q = r % dql;", "int64_t local_q = dql - 1 - r % dql;"),
+]
+
+
+def _build_mutant(tmp, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutant {name}: pattern must occur exactly once"
+    path = os.path.join(tmp, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    so = os.path.join(tmp, f"lib{name}.so")
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-w", "-fPIC", "-shared", "-o", so, path, "-lm"])
+    return oracle.load_library(so)
+
+
+@pytest.fixture(scope="module")
+def tmpdir_mod():
+    d = tempfile.mkdtemp(prefix="bsa_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmpdir_mod, name, old, new):
+    lib = _build_mutant(tmpdir_mod, name, old, new)
+    caught = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(lib=lib)
+        except AssertionError:
+            caught.append(check.__name__)
+    assert caught, f"no pin catches mutant {name}"
