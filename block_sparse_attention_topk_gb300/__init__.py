@@ -1,0 +1,273 @@
+"""GB300 (sm_103a) block-sparse attention top-k selection.
+
+A thin Python binding over the C ABI in ``include/bsa_topk.h``: each
+function here has the name of the C entry point it calls and only marshals
+arguments (tensor pointers, strides, the current CUDA stream).  Every step of
+the computation runs in the library's own CUDA kernels; there is no CPU or
+PyTorch fallback -- importing this package fails if the library has not been
+built (``python -m block_sparse_attention_topk_gb300.build``).
+
+PyTorch supplies device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+BSA_OK = 0
+BSA_DTYPE_BF16 = 0
+BSA_DTYPE_FP32 = 1
+BSA_PATH_ROW = 0
+BSA_PATH_SPLIT = 1
+PAGE_SIZE = 128
+PAGES_PER_SPARSE_BLOCK = 8
+MAX_TOPK = 1024
+MAX_K_TILES = 65536
+
+_ERRORS = {-1: "BSA_ERR_NULL", -2: "BSA_ERR_SHAPE", -3: "BSA_ERR_TOPK", -4: "BSA_ERR_DTYPE",
+           -5: "BSA_ERR_WORKSPACE", -6: "BSA_ERR_ROWS", -7: "BSA_ERR_ALIGN"}
+
+# Names of every extern "C" symbol the header declares (checked by the tests).
+EXPORTED = [
+    "bsa_status_string", "bsa_num_valid_pages_decode", "bsa_num_valid_pages_varlen",
+    "bsa_topk_workspace_bytes", "bsa_topk_select", "bsa_build_sparse_block_table",
+    "bsa_topk_select_sparse_table", "bsa_select_policy",
+]
+
+
+class BsaError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        self.status = status
+        name = _ERRORS.get(status, f"cudaError {status}" if status > 0 else str(status))
+        super().__init__(f"{fn} failed: {name}: {message}")
+
+
+class LaunchPolicy(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("vecs_per_lane", ctypes.c_int32),
+                ("chunks_per_row", ctypes.c_int32), ("reps_per_lane", ctypes.c_int32),
+                ("warps_per_cta", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("cand_capacity", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing: build it with "
+                    "`python -m block_sparse_attention_topk_gb300.build`")
+            L = ctypes.CDLL(path)
+            vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+            L.bsa_status_string.argtypes = [ctypes.c_int]
+            L.bsa_status_string.restype = ctypes.c_char_p
+            L.bsa_num_valid_pages_decode.argtypes = [vp, i64, i32, vp, vp]
+            L.bsa_num_valid_pages_varlen.argtypes = [vp, vp, i64, i64, vp, vp]
+            L.bsa_topk_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
+            L.bsa_topk_workspace_bytes.restype = sz
+            L.bsa_topk_select.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i32, i32, i32,
+                                          vp, vp, sz, vp]
+            L.bsa_build_sparse_block_table.argtypes = [vp, i64, i64, i32, vp, i64, i64, vp, i32,
+                                                       vp, vp, vp]
+            L.bsa_topk_select_sparse_table.argtypes = [vp, i32, i64, i32, i64, i64, i64, i64, vp,
+                                                       i32, i32, i32, vp, i64, vp, vp, vp, vp, sz,
+                                                       vp]
+            L.bsa_select_policy.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(LaunchPolicy)]
+            for name in EXPORTED[1:]:
+                if name != "bsa_topk_workspace_bytes":
+                    getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != BSA_OK:
+        raise BsaError(fn, status, lib().bsa_status_string(status).decode())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dev_i32(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    return t
+
+
+def _score_dtype(scores: torch.Tensor) -> int:
+    if scores.dtype == torch.bfloat16:
+        return BSA_DTYPE_BF16
+    if scores.dtype == torch.float32:
+        return BSA_DTYPE_FP32
+    raise ValueError(f"scores must be bfloat16 or float32, not {scores.dtype}")
+
+
+# One workspace per device, grown on demand (the library clears the parts it
+# needs cleared on every call).  Calls that share it must not overlap on the
+# GPU: pass your own workspace for concurrent streams.
+_ws_cache: dict = {}
+_ws_lock = threading.Lock()
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    key = (device.type, device.index)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+        return ws
+
+
+def bsa_topk_workspace_bytes(T: int, H: int, M: int, K: int, dtype: int) -> int:
+    return int(lib().bsa_topk_workspace_bytes(T, H, M, K, dtype))
+
+
+def bsa_select_policy(rows: int, M: int, K: int, dtype: int, num_sms: int = 152) -> dict:
+    pol = LaunchPolicy()
+    _check("bsa_select_policy",
+           lib().bsa_select_policy(rows, M, K, dtype, num_sms, ctypes.byref(pol)))
+    return pol.as_dict()
+
+
+def bsa_num_valid_pages_decode(seq_lens: torch.Tensor, decode_query_len: int,
+                               out: torch.Tensor | None = None) -> torch.Tensor:
+    _dev_i32(seq_lens, "seq_lens")
+    T = seq_lens.shape[0] * decode_query_len
+    if out is None:
+        out = torch.empty(T, dtype=torch.int32, device=seq_lens.device)
+    _dev_i32(out, "out")
+    _check("bsa_num_valid_pages_decode",
+           lib().bsa_num_valid_pages_decode(_ptr(seq_lens), seq_lens.shape[0], decode_query_len,
+                                            _ptr(out), _stream(seq_lens.device)))
+    return out
+
+
+def bsa_num_valid_pages_varlen(cu_seqlens_q: torch.Tensor, prefix_lens: torch.Tensor,
+                               total_q: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    _dev_i32(cu_seqlens_q, "cu_seqlens_q")
+    _dev_i32(prefix_lens, "prefix_lens")
+    if out is None:
+        out = torch.empty(total_q, dtype=torch.int32, device=cu_seqlens_q.device)
+    _dev_i32(out, "out")
+    _check("bsa_num_valid_pages_varlen",
+           lib().bsa_num_valid_pages_varlen(_ptr(cu_seqlens_q), _ptr(prefix_lens),
+                                            prefix_lens.shape[0], total_q, _ptr(out),
+                                            _stream(cu_seqlens_q.device)))
+    return out
+
+
+def _score_view(scores: torch.Tensor, M: int | None):
+    if scores.dim() != 3 or not scores.is_cuda:
+        raise ValueError("scores must be a 3-D CUDA tensor [T, H, tiles]")
+    if scores.stride(2) != 1:
+        raise ValueError("scores must be contiguous along the tile dimension")
+    T, H, cap = scores.shape
+    M = cap if M is None else int(M)
+    if M > cap:
+        raise ValueError(f"M={M} exceeds the tile dimension {cap}")
+    return T, H, M, scores.stride(0), scores.stride(1)
+
+
+def bsa_topk_select(scores: torch.Tensor, num_valid_pages: torch.Tensor, K: int,
+                    num_init: int = 1, num_local: int = 1, out_idx: torch.Tensor | None = None,
+                    M: int | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """scores [T, H, tiles] (bf16/fp32, tile dim contiguous; M = tiles used,
+    default all), num_valid_pages int32[T] -> out_idx int32 [T, H, K]."""
+    T, H, M, ts, hs = _score_view(scores, M)
+    dt = _score_dtype(scores)
+    _dev_i32(num_valid_pages, "num_valid_pages")
+    if out_idx is None:
+        out_idx = torch.empty((T, H, K), dtype=torch.int32, device=scores.device)
+    _dev_i32(out_idx, "out_idx")
+    need = bsa_topk_workspace_bytes(T, H, M, K, dt)
+    if workspace is None:
+        workspace = _workspace(scores.device, need)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("bsa_topk_select",
+           lib().bsa_topk_select(_ptr(scores), dt, T, H, M, ts, hs, _ptr(num_valid_pages), K,
+                                 num_init, num_local, _ptr(out_idx), _ptr(workspace), wbytes,
+                                 _stream(scores.device)))
+    return out_idx
+
+
+def bsa_build_sparse_block_table(topk_idx: torch.Tensor, block_table: torch.Tensor,
+                                 seq_lens: torch.Tensor, decode_query_len: int,
+                                 sparse_bt: torch.Tensor | None = None,
+                                 sparse_ctx: torch.Tensor | None = None):
+    """topk_idx int32 [T, H, K] -> (sparse_bt int32 [T, H, K*8], sparse_ctx int32 [T, H])."""
+    _dev_i32(topk_idx, "topk_idx")
+    _dev_i32(block_table, "block_table")
+    _dev_i32(seq_lens, "seq_lens")
+    T, H, K = topk_idx.shape
+    B, MB = block_table.shape
+    if sparse_bt is None:
+        sparse_bt = torch.empty((T, H, K * PAGES_PER_SPARSE_BLOCK), dtype=torch.int32,
+                                device=topk_idx.device)
+    if sparse_ctx is None:
+        sparse_ctx = torch.empty((T, H), dtype=torch.int32, device=topk_idx.device)
+    _check("bsa_build_sparse_block_table",
+           lib().bsa_build_sparse_block_table(_ptr(topk_idx), T, H, K, _ptr(block_table), B, MB,
+                                              _ptr(seq_lens), decode_query_len, _ptr(sparse_bt),
+                                              _ptr(sparse_ctx), _stream(topk_idx.device)))
+    return sparse_bt, sparse_ctx
+
+
+def bsa_topk_select_sparse_table(scores: torch.Tensor, seq_lens: torch.Tensor,
+                                 decode_query_len: int, K: int, num_init: int, num_local: int,
+                                 block_table: torch.Tensor, want_idx: bool = True,
+                                 out_idx: torch.Tensor | None = None,
+                                 sparse_bt: torch.Tensor | None = None,
+                                 sparse_ctx: torch.Tensor | None = None, M: int | None = None,
+                                 workspace: torch.Tensor | None = None):
+    """Fused decode select + sparse table.  Returns (out_idx or None, sparse_bt, sparse_ctx)."""
+    _, H, M, ts, hs = _score_view(scores, M)
+    dt = _score_dtype(scores)
+    _dev_i32(seq_lens, "seq_lens")
+    _dev_i32(block_table, "block_table")
+    B, MB = block_table.shape
+    T = seq_lens.shape[0] * decode_query_len
+    if scores.shape[0] < T:
+        raise ValueError(f"scores holds {scores.shape[0]} token rows, need {T}")
+    dev = scores.device
+    if want_idx and out_idx is None:
+        out_idx = torch.empty((T, H, K), dtype=torch.int32, device=dev)
+    if sparse_bt is None:
+        sparse_bt = torch.empty((T, H, K * PAGES_PER_SPARSE_BLOCK), dtype=torch.int32, device=dev)
+    if sparse_ctx is None:
+        sparse_ctx = torch.empty((T, H), dtype=torch.int32, device=dev)
+    need = bsa_topk_workspace_bytes(T, H, M, K, dt)
+    if workspace is None:
+        workspace = _workspace(dev, need)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("bsa_topk_select_sparse_table",
+           lib().bsa_topk_select_sparse_table(
+               _ptr(scores), dt, seq_lens.shape[0], decode_query_len, H, M, ts, hs,
+               _ptr(seq_lens), K, num_init, num_local, _ptr(block_table), MB, _ptr(out_idx),
+               _ptr(sparse_bt), _ptr(sparse_ctx), _ptr(workspace), wbytes, _stream(dev)))
+    return out_idx, sparse_bt, sparse_ctx

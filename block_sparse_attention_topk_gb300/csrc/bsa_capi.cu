@@ -1,0 +1,294 @@
+// bsa_capi.cu -- the extern "C" entry points declared in include/bsa_topk.h:
+// host-side argument checks, the launch policy and the workspace carve-up.
+// Every compute step runs in the kernels of bsa_select.cu and bsa_table.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "bsa_internal.h"
+
+namespace bsa {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+std::once_flag g_sm_once[kMaxDevices];
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int elem_bytes(int32_t dtype) { return dtype == BSA_DTYPE_BF16 ? 2 : 4; }
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+    std::call_once(g_sm_once[dev], [dev] {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        g_sm_count[dev] = n;
+    });
+    return g_sm_count[dev];
+}
+
+size_t split_workspace_bytes(int64_t rows, int32_t chunks, int32_t K) {
+    if (chunks <= 1 || rows <= 0) return 0;
+    const size_t entries = (size_t)rows * chunks * K;
+    return align_up(entries * 4) + align_up(entries * 4) + align_up((size_t)rows * chunks * 4) +
+           align_up((size_t)rows * 4);
+}
+
+SplitWorkspace carve_split_workspace(void* base, int64_t rows, int32_t chunks, int32_t K) {
+    SplitWorkspace ws{nullptr, nullptr, nullptr, nullptr};
+    if (chunks <= 1 || base == nullptr) return ws;
+    const size_t entries = (size_t)rows * chunks * K;
+    char* p = static_cast<char*>(base);
+    ws.keys = reinterpret_cast<uint32_t*>(p);
+    p += align_up(entries * 4);
+    ws.ids = reinterpret_cast<int32_t*>(p);
+    p += align_up(entries * 4);
+    ws.counts = reinterpret_cast<int32_t*>(p);
+    p += align_up((size_t)rows * chunks * 4);
+    ws.tickets = reinterpret_cast<int32_t*>(p);
+    return ws;
+}
+
+}  // namespace bsa
+
+using namespace bsa;
+
+namespace {
+
+int check_topk_args(int64_t M, int32_t K, int32_t num_init, int32_t num_local) {
+    if (K < 1 || K > BSA_MAX_TOPK || K > M || num_init < 0 || num_local < 0 ||
+        (int64_t)num_init + num_local > K)
+        return BSA_ERR_TOPK;
+    return BSA_OK;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? BSA_OK : (int)e; }
+
+// The launch policy (see bsa_select_policy in the header).
+int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
+                bsa_launch_policy_t* p) {
+    const int vec = dtype == BSA_DTYPE_BF16 ? 8 : 4;
+    // Vectors per lane per pass: smallest of 1, 2, 4 covering the capacity.
+    int nv = 4;
+    if (M <= 32LL * 1 * vec) nv = 1;
+    else if (M <= 32LL * 2 * vec) nv = 2;
+    const int64_t per_pass = 32LL * nv * vec;
+    const int64_t passes = (M + per_pass - 1) / per_pass;
+    // Representatives for the threshold estimate: enough for K' <= K.
+    int reps = 2 * nv;
+    if (K <= 16) reps = 1;
+    else if (K <= 48) reps = 2;
+    // Split a long row over several warps only when rows alone cannot
+    // occupy the GPU (about 32 resident warps per SM).
+    const int64_t resident = (int64_t)num_sms * 32;
+    int64_t chunks = 1;
+    if (passes > 1 && rows < resident) {
+        chunks = resident / (rows > 0 ? rows : 1);
+        if (chunks > passes) chunks = passes;
+        if (chunks < 1) chunks = 1;
+    }
+    int warps = 8;
+    const int cap = (int)((K + 32 * vec + 31) / 32 * 32);
+    const int smem = warps * cap * 8;
+    const int64_t items = rows * chunks;
+    int ctas_per_sm = 4;
+    const int smem_budget = 227 * 1024;
+    while (ctas_per_sm > 1 && ctas_per_sm * smem > smem_budget) --ctas_per_sm;
+    int64_t grid = (items + warps - 1) / warps;
+    const int64_t grid_cap = (int64_t)num_sms * ctas_per_sm;
+    if (grid > grid_cap) grid = grid_cap;
+    if (grid < 1) grid = 1;
+    p->path = chunks > 1 ? BSA_PATH_SPLIT : BSA_PATH_ROW;
+    p->vecs_per_lane = nv;
+    p->chunks_per_row = (int32_t)chunks;
+    p->reps_per_lane = reps;
+    p->warps_per_cta = warps;
+    p->grid = (int32_t)grid;
+    p->cand_capacity = cap;
+    p->smem_bytes = smem;
+    return BSA_OK;
+}
+
+int run_select(SelectArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    bsa_launch_policy_t pol;
+    const int64_t rows = a.T * a.H;
+    make_policy(rows, a.M, a.K, a.dtype, device_sm_count(), &pol);
+    const size_t need = split_workspace_bytes(rows, pol.chunks_per_row, a.K);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+            return BSA_ERR_WORKSPACE;
+    }
+    SplitWorkspace ws = carve_split_workspace(workspace, rows, pol.chunks_per_row, a.K);
+    if (need > 0) {
+        // The merge tickets start at zero on every call, whatever an earlier
+        // call with another layout left in this memory (one memset node when
+        // captured in a graph).
+        cudaError_t e = cudaMemsetAsync(ws.tickets, 0, (size_t)rows * sizeof(int32_t), stream);
+        if (e != cudaSuccess) return (int)e;
+    }
+    return status_of(launch_select(a, pol, ws, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bsa_status_string(int status) {
+    switch (status) {
+        case BSA_OK: return "ok";
+        case BSA_ERR_NULL: return "a required pointer is NULL";
+        case BSA_ERR_SHAPE: return "invalid size or stride";
+        case BSA_ERR_TOPK: return "invalid topk / num_init / num_local";
+        case BSA_ERR_DTYPE: return "unknown score dtype";
+        case BSA_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+        case BSA_ERR_ROWS: return "T != num_reqs * decode_query_len";
+        case BSA_ERR_ALIGN: return "scores pointer not aligned to its element size";
+        default: break;
+    }
+    if (status > 0) return cudaGetErrorString((cudaError_t)status);
+    return "unknown status";
+}
+
+int bsa_select_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
+                      bsa_launch_policy_t* policy) {
+    if (policy == nullptr) return BSA_ERR_NULL;
+    if (dtype != BSA_DTYPE_BF16 && dtype != BSA_DTYPE_FP32) return BSA_ERR_DTYPE;
+    if (rows < 0 || M < 1 || M > BSA_MAX_K_TILES || num_sms < 1) return BSA_ERR_SHAPE;
+    if (K < 1 || K > BSA_MAX_TOPK || K > M) return BSA_ERR_TOPK;
+    return make_policy(rows, M, K, dtype, num_sms, policy);
+}
+
+size_t bsa_topk_workspace_bytes(int64_t T, int64_t H, int64_t M, int32_t K, int32_t dtype) {
+    if (T <= 0 || H <= 0 || M < 1 || M > BSA_MAX_K_TILES || K < 1 || K > BSA_MAX_TOPK || K > M)
+        return 0;
+    if (dtype != BSA_DTYPE_BF16 && dtype != BSA_DTYPE_FP32) return 0;
+    bsa_launch_policy_t pol;
+    make_policy(T * H, M, K, dtype, device_sm_count(), &pol);
+    return split_workspace_bytes(T * H, pol.chunks_per_row, K);
+}
+
+int bsa_num_valid_pages_decode(const int32_t* seq_lens, int64_t num_reqs, int32_t dql,
+                               int32_t* num_valid_pages, void* stream) {
+    if (num_reqs < 0 || dql < 1) return BSA_ERR_SHAPE;
+    if (num_reqs == 0) return BSA_OK;
+    if (seq_lens == nullptr || num_valid_pages == nullptr) return BSA_ERR_NULL;
+    return status_of(launch_num_valid_pages_decode(seq_lens, num_reqs, dql, num_valid_pages,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+int bsa_num_valid_pages_varlen(const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                               int64_t num_seqs, int64_t total_q, int32_t* num_valid_pages,
+                               void* stream) {
+    if (num_seqs < 0 || total_q < 0) return BSA_ERR_SHAPE;
+    if (total_q == 0) return BSA_OK;
+    if (num_valid_pages == nullptr || cu_seqlens_q == nullptr ||
+        (num_seqs > 0 && prefix_lens == nullptr))
+        return BSA_ERR_NULL;
+    return status_of(launch_num_valid_pages_varlen(cu_seqlens_q, prefix_lens, num_seqs, total_q,
+                                                   num_valid_pages,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+int bsa_topk_select(const void* scores, int32_t dtype, int64_t T, int64_t H, int64_t M,
+                    int64_t token_stride, int64_t head_stride, const int32_t* num_valid_pages,
+                    int32_t K, int32_t num_init, int32_t num_local, int32_t* out_idx,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    if (dtype != BSA_DTYPE_BF16 && dtype != BSA_DTYPE_FP32) return BSA_ERR_DTYPE;
+    if (T < 0 || H < 0 || M < 1 || M > BSA_MAX_K_TILES) return BSA_ERR_SHAPE;
+    int rc = check_topk_args(M, K, num_init, num_local);
+    if (rc != BSA_OK) return rc;
+    if (head_stride < M || token_stride < (H > 0 ? (H - 1) * head_stride + M : M))
+        return BSA_ERR_SHAPE;
+    if (T == 0 || H == 0) return BSA_OK;
+    if (scores == nullptr || num_valid_pages == nullptr || out_idx == nullptr) return BSA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(scores) % elem_bytes(dtype)) != 0) return BSA_ERR_ALIGN;
+    SelectArgs a{};
+    a.scores = scores;
+    a.dtype = dtype;
+    a.T = T;
+    a.H = H;
+    a.M = M;
+    a.token_stride = token_stride;
+    a.head_stride = head_stride;
+    a.num_valid_pages = num_valid_pages;
+    a.dql = 1;
+    a.K = K;
+    a.num_init = num_init;
+    a.num_local = num_local;
+    a.out_idx = out_idx;
+    a.fused = false;
+    return run_select(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int bsa_build_sparse_block_table(const int32_t* topk_idx, int64_t T, int64_t H, int32_t K,
+                                 const int32_t* block_table, int64_t num_reqs,
+                                 int64_t max_blocks, const int32_t* seq_lens,
+                                 int32_t decode_query_len, int32_t* sparse_bt,
+                                 int32_t* sparse_ctx, void* stream) {
+    if (T < 0 || H < 0 || num_reqs < 0 || max_blocks < 0 || decode_query_len < 1)
+        return BSA_ERR_SHAPE;
+    if (K < 1 || K > BSA_MAX_TOPK) return BSA_ERR_TOPK;
+    if (T != num_reqs * decode_query_len) return BSA_ERR_ROWS;
+    if (T == 0 || H == 0) return BSA_OK;
+    if (topk_idx == nullptr || seq_lens == nullptr || sparse_bt == nullptr ||
+        sparse_ctx == nullptr || (max_blocks > 0 && block_table == nullptr))
+        return BSA_ERR_NULL;
+    return status_of(launch_build_sparse_block_table(topk_idx, T, H, K, block_table, max_blocks,
+                                                     seq_lens, decode_query_len, sparse_bt,
+                                                     sparse_ctx,
+                                                     static_cast<cudaStream_t>(stream)));
+}
+
+int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_reqs,
+                                 int32_t decode_query_len, int64_t H, int64_t M,
+                                 int64_t token_stride, int64_t head_stride,
+                                 const int32_t* seq_lens, int32_t K, int32_t num_init,
+                                 int32_t num_local, const int32_t* block_table,
+                                 int64_t max_blocks, int32_t* out_idx, int32_t* sparse_bt,
+                                 int32_t* sparse_ctx, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    if (dtype != BSA_DTYPE_BF16 && dtype != BSA_DTYPE_FP32) return BSA_ERR_DTYPE;
+    if (num_reqs < 0 || decode_query_len < 1 || H < 0 || M < 1 || M > BSA_MAX_K_TILES ||
+        max_blocks < 0)
+        return BSA_ERR_SHAPE;
+    int rc = check_topk_args(M, K, num_init, num_local);
+    if (rc != BSA_OK) return rc;
+    if (head_stride < M || token_stride < (H > 0 ? (H - 1) * head_stride + M : M))
+        return BSA_ERR_SHAPE;
+    const int64_t T = num_reqs * decode_query_len;
+    if (T == 0 || H == 0) return BSA_OK;
+    if (scores == nullptr || seq_lens == nullptr || sparse_bt == nullptr ||
+        sparse_ctx == nullptr || (max_blocks > 0 && block_table == nullptr))
+        return BSA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(scores) % elem_bytes(dtype)) != 0) return BSA_ERR_ALIGN;
+    SelectArgs a{};
+    a.scores = scores;
+    a.dtype = dtype;
+    a.T = T;
+    a.H = H;
+    a.M = M;
+    a.token_stride = token_stride;
+    a.head_stride = head_stride;
+    a.seq_lens = seq_lens;
+    a.dql = decode_query_len;
+    a.K = K;
+    a.num_init = num_init;
+    a.num_local = num_local;
+    a.out_idx = out_idx;
+    a.block_table = block_table;
+    a.max_blocks = max_blocks;
+    a.sparse_bt = sparse_bt;
+    a.sparse_ctx = sparse_ctx;
+    a.fused = true;
+    return run_select(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

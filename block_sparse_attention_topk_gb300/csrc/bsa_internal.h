@@ -1,0 +1,64 @@
+// bsa_internal.h -- declarations shared by the library's translation units
+// (host launchers and the launch policy).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/bsa_topk.h"
+
+namespace bsa {
+
+constexpr int kPageSize = BSA_PAGE_SIZE;              // tokens per sparse block
+constexpr int kSubPage = BSA_SUB_PAGE_SIZE;           // tokens per table entry
+constexpr int kPagesPerBlock = BSA_PAGES_PER_SPARSE_BLOCK;
+constexpr int kLogPageSize = 7;
+
+// Everything one selector launch needs.  Pointers are device pointers.
+struct SelectArgs {
+    const void* scores;
+    int32_t dtype;
+    int64_t T, H, M;
+    int64_t token_stride, head_stride;
+    const int32_t* num_valid_pages;   // select mode: int32[T]
+    const int32_t* seq_lens;          // fused mode: int32[T / dql]
+    int32_t dql;
+    int32_t K, num_init, num_local;
+    int32_t* out_idx;                 // may be null in fused mode
+    const int32_t* block_table;       // fused mode
+    int64_t max_blocks;
+    int32_t* sparse_bt;
+    int32_t* sparse_ctx;
+    bool fused;
+};
+
+// Workspace carve-up for the split path (all offsets 256-byte aligned).
+struct SplitWorkspace {
+    uint32_t* keys;     // [rows, chunks, K]
+    int32_t* ids;       // [rows, chunks, K]
+    int32_t* counts;    // [rows, chunks]
+    int32_t* tickets;   // [rows]
+};
+
+size_t split_workspace_bytes(int64_t rows, int32_t chunks, int32_t K);
+SplitWorkspace carve_split_workspace(void* base, int64_t rows, int32_t chunks, int32_t K);
+
+int device_sm_count();
+
+// Launches the selector (plain or fused) with a policy from bsa_select_policy.
+cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
+                          const SplitWorkspace& ws, cudaStream_t stream);
+
+cudaError_t launch_num_valid_pages_decode(const int32_t* seq_lens, int64_t num_reqs,
+                                          int32_t dql, int32_t* out, cudaStream_t stream);
+cudaError_t launch_num_valid_pages_varlen(const int32_t* cu, const int32_t* prefix,
+                                          int64_t num_seqs, int64_t total_q, int32_t* out,
+                                          cudaStream_t stream);
+cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, int64_t H,
+                                            int32_t K, const int32_t* block_table,
+                                            int64_t max_blocks, const int32_t* seq_lens,
+                                            int32_t dql, int32_t* sparse_bt,
+                                            int32_t* sparse_ctx, cudaStream_t stream);
+
+}  // namespace bsa

@@ -1,0 +1,612 @@
+// bsa_select.cu -- the top-k block selector (plain and fused with the sparse
+// block table) for GB300 / sm_103a.
+//
+// What it computes (vLLM PR #47502 report, "Using sparse_topk_select from MSA
+// instead of triton kernels", sections 实现拆解 and 关键源码片段, indexer_msa.py):
+// for every row (token t, index head h) of the unified token-major score
+// buffer, the top-K block ids among the causal prefix b < v = min(M,
+// num_valid_pages[t]), with the init blocks [0, I) and the local blocks
+// [v - L, v) always kept.  Scores are ordered by IEEE totalOrder, ties go to
+// the lower block id (vLLM PR #55235 report, sections 执行摘要 and 评论区精华:
+// NaN, +-Inf, +-0 and tied scores each have a fixed place).  The fused variant
+// adds the page-16 sparse block-table epilogue of vLLM PR #47984 report
+// ("Support speculative decode with AITER sparse PA", 实现拆解 items 1 and 3)
+// and of the EMIT_SPARSE_TABLE flag in PR #55235.
+//
+// How (a design for this GPU, not the pages' Triton/ROCm kernels):
+//  * One warp owns one work item: a whole row, or one chunk of a long row
+//    when there are too few rows to fill 152 SMs (split path).  The causal
+//    prefix is streamed with 16-byte vector loads (lane l loads vectors l,
+//    l+32, ...; a warp instruction moves 512 contiguous bytes); forced blocks
+//    and ids outside the row's range are replaced at load time by the bit
+//    pattern 0x8000 (bf16) / 0x80000000 (fp32), the most negative signed
+//    integer.
+//  * Threshold estimate.  On the raw bits read as signed integers, any two
+//    non-negative floats compare like the floats (+NaN above +Inf above
+//    finite), and every negative float or masked slot compares below them.
+//    Each lane keeps R representatives (maxima of its elements; bf16 pairs
+//    are maxed with one packed max.s16x2).  If at least K' representatives
+//    are >= 0, the K'-th largest of them, theta, is a lower bound on the K'-th
+//    best score of the chunk: K' distinct elements reach it.  Only elements
+//    >= theta can be selected, and for N(0,1)-like scores that is ~K' to 2K'
+//    elements.  When the estimate does not exist (few lanes with data, mostly
+//    negative scores) the chunk falls back to taking every valid element as
+//    a candidate, filtered in the order-preserving key space instead.
+//  * Candidates (order-preserving key, id) are appended in ascending id order
+//    to a per-warp shared-memory buffer.  When it would overflow, and at the
+//    end, an exact warp select keeps the K' best: a bit-by-bit search for the
+//    K'-th largest key (warp-reduced counts), then ties at that key resolved
+//    by buffer order, which is id order.  Later elements have higher ids, so
+//    after a compaction only keys strictly above the K'-th kept key can still
+//    enter; the raw-space threshold is raised accordingly.
+//  * Split rows: each chunk's warp writes its <= K' candidates to the
+//    caller's workspace and takes a ticket with atomicAdd; the warp that draws
+//    the last ticket merges the chunks' lists (chunk order = id order) with
+//    the same buffer logic, writes the output, and sets the ticket back to 0.
+//    The host also clears the tickets before every launch, so graph replays
+//    and workspaces reused across layouts start from zero (PR #55235:
+//    counters reset under graph replay).  Nothing ever waits on another warp.
+//  * Output: slots [0, n) = init ids, the K' selected ids, the local ids --
+//    ascending by construction -- then -1.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bsa_internal.h"
+
+namespace bsa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kWarpsPerCta = 8;
+constexpr int kThreads = kWarpsPerCta * 32;
+
+__device__ __forceinline__ uint32_t max_s16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.s16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// Element types.  `raw` is the bit pattern sign-extended to int32; `key` is
+// the order-preserving unsigned key: larger key <=> later in totalOrder.
+// ---------------------------------------------------------------------------
+template <bool BF16>
+struct Elem;
+
+template <>
+struct Elem<true> {
+    static constexpr int kVec = 8;                 // elements per 16 bytes
+    static constexpr int kBytes = 2;
+    static constexpr int kKeyBits = 16;
+    static constexpr uint32_t kKeyMax = 0xFFFFu;
+    static constexpr uint32_t kKeyOfPlusZero = 0x8000u;
+    static constexpr uint32_t kMaskWord = 0x80008000u;
+    static constexpr int kThetaTop = 14, kThetaLow = 0;  // bits searched for theta
+    __device__ static int32_t raw(const uint4& w, int e) {
+        uint32_t word = e < 2 ? w.x : e < 4 ? w.y : e < 6 ? w.z : w.w;
+        return (int32_t)(int16_t)(uint16_t)(word >> ((e & 1) * 16));
+    }
+    __device__ static uint32_t key(int32_t raw) {
+        uint32_t u = (uint32_t)raw & 0xFFFFu;
+        return (u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u);
+    }
+    __device__ static int32_t raw_of_nonneg_key(uint32_t k) { return (int32_t)(k - 0x8000u); }
+    __device__ static int32_t load_one(const char* p) {
+        return (int32_t)(int16_t)__ldg(reinterpret_cast<const unsigned short*>(p));
+    }
+    __device__ static void set(uint4& w, int e, int32_t raw) {
+        uint32_t* word = e < 2 ? &w.x : e < 4 ? &w.y : e < 6 ? &w.z : &w.w;
+        int sh = (e & 1) * 16;
+        *word = (*word & ~(0xFFFFu << sh)) | (((uint32_t)raw & 0xFFFFu) << sh);
+    }
+    // Per-lane representatives: q = 0 / 1 are the two halves.
+    __device__ static uint32_t slot_pack_max(const uint4& w) {
+        return max_s16x2(max_s16x2(w.x, w.y), max_s16x2(w.z, w.w));
+    }
+    __device__ static int32_t pack_lo(uint32_t p) { return (int32_t)(int16_t)(uint16_t)p; }
+    __device__ static int32_t pack_hi(uint32_t p) { return (int32_t)(int16_t)(uint16_t)(p >> 16); }
+    // does any element of the packed maximum reach theta (theta >= 0)?
+    __device__ static bool pack_any_ge(uint32_t p, int32_t theta) {
+        return pack_lo(p) >= theta || pack_hi(p) >= theta;
+    }
+};
+
+template <>
+struct Elem<false> {
+    static constexpr int kVec = 4;
+    static constexpr int kBytes = 4;
+    static constexpr int kKeyBits = 32;
+    static constexpr uint32_t kKeyMax = 0xFFFFFFFFu;
+    static constexpr uint32_t kKeyOfPlusZero = 0x80000000u;
+    static constexpr uint32_t kMaskWord = 0x80000000u;
+    static constexpr int kThetaTop = 30, kThetaLow = 16;  // bf16-resolution bound suffices
+    __device__ static int32_t raw(const uint4& w, int e) {
+        return (int32_t)(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
+    }
+    __device__ static uint32_t key(int32_t raw) {
+        uint32_t u = (uint32_t)raw;
+        return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    __device__ static int32_t raw_of_nonneg_key(uint32_t k) { return (int32_t)(k - 0x80000000u); }
+    __device__ static int32_t load_one(const char* p) {
+        return (int32_t)__ldg(reinterpret_cast<const unsigned int*>(p));
+    }
+    __device__ static void set(uint4& w, int e, int32_t raw) {
+        uint32_t* word = e == 0 ? &w.x : e == 1 ? &w.y : e == 2 ? &w.z : &w.w;
+        *word = (uint32_t)raw;
+    }
+    // "packed" maximum of a vector: (max of elements 0,2) | (max of 1,3) kept
+    // as two int32 in a uint2-like pair; represented here as max over all for
+    // q = 0 and the odd elements for q = 1 (see reps below).
+    __device__ static int32_t even_max(const uint4& w) { return max((int32_t)w.x, (int32_t)w.z); }
+    __device__ static int32_t odd_max(const uint4& w) { return max((int32_t)w.y, (int32_t)w.w); }
+};
+
+// ---------------------------------------------------------------------------
+// Exact warp select on the shared candidate buffer: keep the `keep` best
+// entries (key descending, buffer position ascending), preserving order.
+// Returns the key of the worst kept entry.
+// ---------------------------------------------------------------------------
+template <int KEY_BITS>
+__device__ uint32_t warp_compact(uint32_t* keys, int32_t* ids, int n, int keep, int lane) {
+    const int rounds = (n + 31) >> 5;
+    uint32_t kappa = 0;
+    for (int bit = KEY_BITS - 1; bit >= 0; --bit) {
+        const uint32_t t = kappa | (1u << bit);
+        int c = 0;
+        for (int s = 0; s < rounds; ++s) {
+            const int e = (s << 5) + lane;
+            c += (e < n && keys[e] >= t) ? 1 : 0;
+        }
+        c = __reduce_add_sync(kFull, c);
+        if (c >= keep) kappa = t;
+    }
+    int above = 0;
+    for (int s = 0; s < rounds; ++s) {
+        const int e = (s << 5) + lane;
+        above += (e < n && keys[e] > kappa) ? 1 : 0;
+    }
+    above = __reduce_add_sync(kFull, above);
+    const int ties_wanted = keep - above;
+    int ties_seen = 0, kept = 0;
+    const unsigned lt = lanemask_lt();
+    for (int s = 0; s < rounds; ++s) {
+        const int e = (s << 5) + lane;
+        const bool in = e < n;
+        const uint32_t k = in ? keys[e] : 0u;
+        const int32_t id = in ? ids[e] : 0;
+        const bool gt = in && k > kappa;
+        const bool eq = in && k == kappa;
+        const unsigned eqb = __ballot_sync(kFull, eq);
+        const bool take = gt || (eq && ties_seen + __popc(eqb & lt) < ties_wanted);
+        ties_seen += __popc(eqb);
+        const unsigned tb = __ballot_sync(kFull, take);
+        const int pos = kept + __popc(tb & lt);
+        __syncwarp();
+        if (take) {
+            keys[pos] = k;
+            ids[pos] = id;
+        }
+        kept += __popc(tb);
+        __syncwarp();
+    }
+    return kappa;
+}
+
+// Warp-wide exclusive prefix sum of `x`; `total` gets the sum.
+__device__ __forceinline__ int warp_excl_scan(int x, int lane, int& total) {
+    int incl = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl += y;
+    }
+    total = __shfl_sync(kFull, incl, 31);
+    return incl - x;
+}
+
+struct Split {
+    uint32_t* keys;
+    int32_t* ids;
+    int32_t* counts;
+    int32_t* tickets;
+};
+
+struct KernelParams {
+    SelectArgs a;
+    Split ws;
+    int32_t chunks_per_row;   // work items per row
+    int32_t vecs_per_chunk;   // vectors (16 B) per work item
+    int32_t cap;              // candidate buffer entries per warp
+    int64_t rows;
+};
+
+// Candidate-buffer state of one warp.
+struct Buf {
+    uint32_t* keys;
+    int32_t* ids;
+    int n;            // entries held
+    uint32_t kb;      // only keys >= kb can still be selected
+    bool closed;      // nothing can enter any more (kept key is the maximum)
+};
+
+// Shrink the buffer to the `keep` best entries and raise the entry bound.
+template <int KEY_BITS, uint32_t KEY_MAX>
+__device__ __forceinline__ void buf_compact(Buf& b, int keep, int lane) {
+    const uint32_t kappa = warp_compact<KEY_BITS>(b.keys, b.ids, b.n, keep, lane);
+    b.n = keep;
+    if (kappa == KEY_MAX) b.closed = true;
+    else if (kappa + 1 > b.kb) b.kb = kappa + 1;
+}
+
+// Appends the candidates of one 32-lane group: lane holds `m` (bit i set =
+// element i of its group is a candidate, keys/ids produced by `emit`).  The
+// caller recomputes `m` after a compaction (the bound may have risen), so this
+// returns false when it compacted and appended nothing.
+template <int KEY_BITS, uint32_t KEY_MAX>
+__device__ __forceinline__ bool buf_try_append(Buf& b, unsigned m, int cap, int keep, int lane,
+                                               int& excl_out) {
+    int total;
+    const int excl = warp_excl_scan(__popc(m), lane, total);
+    if (total == 0) {
+        excl_out = -1;
+        return true;
+    }
+    if (b.n + total > cap) {
+        buf_compact<KEY_BITS, KEY_MAX>(b, keep, lane);
+        return false;
+    }
+    excl_out = b.n + excl;
+    b.n += total;
+    return true;
+}
+
+// Output epilogue: ids, and in fused mode the page-16 table and ctx.
+// sel(j): j < lo -> j (init); j - lo < kp -> buffered id; else hi + (j - lo - kp).
+__device__ __forceinline__ int32_t selected_id(int j, int lo, int hi, int kp, bool all,
+                                               const int32_t* buf_ids) {
+    if (all || j < lo) return j;
+    if (j - lo < kp) return buf_ids[j - lo];
+    return hi + (j - lo - kp);
+}
+
+__device__ void write_outputs(const KernelParams& P, int64_t row, int n, int lo, int hi, int kp,
+                              bool all, const int32_t* buf_ids, int64_t causal_len,
+                              int64_t req, int lane) {
+    const SelectArgs& a = P.a;
+    const int K = a.K;
+    if (a.out_idx != nullptr) {
+        int32_t* out = a.out_idx + row * K;
+        for (int s = lane; s < K; s += 32)
+            out[s] = s < n ? selected_id(s, lo, hi, kp, all, buf_ids) : -1;
+    }
+    if (a.fused) {
+        const int width = K * kPagesPerBlock;
+        int32_t* bt = a.sparse_bt + row * (int64_t)width;
+        const int32_t* table = a.block_table + req * a.max_blocks;
+        for (int e = lane; e < width; e += 32) {
+            const int j = e >> 3;
+            const int pg = e & 7;
+            int32_t val = 0;
+            if (j < n) {
+                const int32_t b = selected_id(j, lo, hi, kp, all, buf_ids);
+                if (b < a.max_blocks &&
+                    (int64_t)b * kPageSize + (int64_t)pg * kSubPage < causal_len)
+                    val = __ldg(table + b) * kPagesPerBlock + pg;
+            }
+            bt[e] = val;
+        }
+        int ctx = 0;
+        for (int j = lane; j < n; j += 32) {
+            const int32_t b = selected_id(j, lo, hi, kp, all, buf_ids);
+            if (b < a.max_blocks) {
+                const int64_t rem = causal_len - (int64_t)b * kPageSize;
+                ctx += (int)(rem < kPageSize ? rem : kPageSize);
+            }
+        }
+        ctx = __reduce_add_sync(kFull, ctx);
+        if (lane == 0) a.sparse_ctx[row] = ctx;
+    }
+}
+
+template <bool BF16, int NV, int R>
+__global__ void __launch_bounds__(kThreads, 4) select_kernel(const KernelParams P) {
+    using E = Elem<BF16>;
+    constexpr int VEC = E::kVec;
+    constexpr int S = E::kBytes;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const SelectArgs& a = P.a;
+    const int cap = P.cap;
+    uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem_raw) + (size_t)warp * cap * 2;
+    int32_t* s_ids = reinterpret_cast<int32_t*>(s_keys + cap);
+
+    const int64_t items = P.rows * P.chunks_per_row;
+    const int64_t warps_total = (int64_t)gridDim.x * kWarpsPerCta;
+    for (int64_t item = (int64_t)blockIdx.x * kWarpsPerCta + warp; item < items;
+         item += warps_total) {
+        const int64_t row = item / P.chunks_per_row;
+        const int chunk = (int)(item - row * P.chunks_per_row);
+        const int64_t t = row / a.H;
+        const int64_t h = row - t * a.H;
+
+        // ---- causal bound of the row ----
+        int64_t causal_len = 0, req = 0, pages;
+        if (a.fused) {
+            req = t / a.dql;
+            const int64_t lq = t - req * a.dql;
+            const int64_t pos = (int64_t)__ldg(a.seq_lens + req) - a.dql + lq;
+            causal_len = pos + 1 > 0 ? pos + 1 : 0;
+            pages = (causal_len + kPageSize - 1) >> kLogPageSize;
+        } else {
+            pages = __ldg(a.num_valid_pages + t);
+        }
+        const int v = (int)(pages < 0 ? 0 : (pages > a.M ? a.M : pages));
+        const int lo = a.num_init < v ? a.num_init : v;
+        const int hi = max(v - a.num_local, lo);
+        const int n = a.K < v ? a.K : v;
+        const int kp = n - lo - (v - hi);            // non-forced ids to select
+        const bool all = kp >= hi - lo;              // every non-forced id fits
+        const bool need = kp > 0 && !all;
+
+        if (!need) {
+            if (chunk == 0) write_outputs(P, row, n, lo, hi, kp, all, s_ids, causal_len, req, lane);
+            continue;
+        }
+
+        // ---- vector grid over the non-forced range [lo, hi) ----
+        const char* row_ptr = reinterpret_cast<const char*>(a.scores) +
+                              (t * a.token_stride + h * a.head_stride) * S;
+        const uintptr_t a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)lo * S;
+        const uintptr_t a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)hi * S;
+        const uintptr_t v0 = a_lo & ~(uintptr_t)15;
+        const int nvec = (int)((a_hi - v0 + 15) >> 4);
+        const int base_id = lo - (int)((a_lo - v0) / S);
+        const int nchunks = (nvec + P.vecs_per_chunk - 1) / P.vecs_per_chunk;
+        if (chunk >= nchunks) continue;
+        const int k_begin = chunk * P.vecs_per_chunk;
+        const int k_end = min(nvec, k_begin + P.vecs_per_chunk);
+
+        Buf b{s_keys, s_ids, 0, 0u, false};
+
+        for (int pass = k_begin; pass < k_end && !b.closed; pass += 32 * NV) {
+            // ---- load NV vectors per lane (masked outside [lo, hi)) ----
+            uint4 w[NV];
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                const int k = pass + j * 32 + lane;
+                const uintptr_t addr = v0 + ((uintptr_t)k << 4);
+                w[j] = make_uint4(E::kMaskWord, E::kMaskWord, E::kMaskWord, E::kMaskWord);
+                if (k < k_end) {
+                    if (addr >= a_lo && addr + 16 <= a_hi) {
+                        w[j] = ld_stream_v4(reinterpret_cast<const void*>(addr));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) {
+                            const int id = base_id + k * VEC + e;
+                            if (id >= lo && id < hi)
+                                E::set(w[j], e, E::load_one(row_ptr + (int64_t)id * S));
+                        }
+                    }
+                }
+            }
+
+            // ---- representatives and the chunk's lower bound theta ----
+            int32_t rep[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) rep[r] = INT32_MIN;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                int32_t q0, q1;
+                if constexpr (BF16) {
+                    const uint32_t pm = E::slot_pack_max(w[j]);
+                    q0 = E::pack_lo(pm);
+                    q1 = E::pack_hi(pm);
+                } else {
+                    q0 = E::even_max(w[j]);
+                    q1 = E::odd_max(w[j]);
+                }
+                if constexpr (R == 1) {
+                    rep[0] = max(rep[0], max(q0, q1));
+                } else if constexpr (R == 2) {
+                    rep[0] = max(rep[0], q0);
+                    rep[1] = max(rep[1], q1);
+                } else {
+                    rep[(2 * j) % R] = max(rep[(2 * j) % R], q0);
+                    rep[(2 * j + 1) % R] = max(rep[(2 * j + 1) % R], q1);
+                }
+            }
+            int c0 = 0;
+#pragma unroll
+            for (int r = 0; r < R; ++r) c0 += rep[r] >= 0 ? 1 : 0;
+            c0 = __reduce_add_sync(kFull, c0);
+            bool have_theta = c0 >= kp;
+            int32_t theta = 0;
+            if (have_theta) {
+                for (int bit = E::kThetaTop; bit >= E::kThetaLow; --bit) {
+                    const int32_t tt = theta | (1 << bit);
+                    int c = 0;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) c += rep[r] >= tt ? 1 : 0;
+                    c = __reduce_add_sync(kFull, c);
+                    if (c >= kp) theta = tt;
+                }
+            }
+
+            // ---- filter + append, one 32-vector slot at a time ----
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                if (pass + j * 32 >= k_end || b.closed) break;
+                const int k = pass + j * 32 + lane;
+                const int first_id = base_id + k * VEC;
+                while (true) {
+                    // Raw-space filter when the bound is a non-negative float.
+                    const bool kb_nonneg = b.kb >= E::kKeyOfPlusZero;
+                    const bool fast = have_theta || kb_nonneg;
+                    int32_t th = 0;
+                    if (fast) {
+                        th = have_theta ? theta : 0;
+                        if (kb_nonneg) th = max(th, E::raw_of_nonneg_key(b.kb));
+                    }
+                    unsigned m = 0;
+                    if (fast) {
+                        bool any;
+                        if constexpr (BF16) {
+                            any = E::pack_any_ge(E::slot_pack_max(w[j]), th);
+                        } else {
+                            any = max(E::even_max(w[j]), E::odd_max(w[j])) >= th;
+                        }
+                        if (any) {
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e)
+                                if (E::raw(w[j], e) >= th) m |= 1u << e;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) {
+                            const int id = first_id + e;
+                            if (id >= lo && id < hi && E::key(E::raw(w[j], e)) >= b.kb)
+                                m |= 1u << e;
+                        }
+                    }
+                    int pos;
+                    if (!buf_try_append<E::kKeyBits, E::kKeyMax>(b, m, cap, kp, lane, pos)) {
+                        if (b.closed) break;
+                        continue;  // bound rose: recompute this slot's mask
+                    }
+                    if (pos >= 0) {
+                        while (m) {
+                            const int e = __ffs(m) - 1;
+                            m &= m - 1;
+                            b.keys[pos] = E::key(E::raw(w[j], e));
+                            b.ids[pos] = first_id + e;
+                            ++pos;
+                        }
+                    }
+                    __syncwarp();
+                    break;
+                }
+            }
+        }
+        if (b.n > kp) buf_compact<E::kKeyBits, E::kKeyMax>(b, kp, lane);
+
+        if (nchunks > 1) {
+            // ---- split row: publish this chunk, the last arriver merges ----
+            const int64_t slot = row * P.chunks_per_row + chunk;
+            uint32_t* wk = P.ws.keys + slot * a.K;
+            int32_t* wi = P.ws.ids + slot * a.K;
+            for (int e = lane; e < b.n; e += 32) {
+                wk[e] = b.keys[e];
+                wi[e] = b.ids[e];
+            }
+            if (lane == 0) P.ws.counts[slot] = b.n;
+            __threadfence();
+            __syncwarp();
+            int ticket = 0;
+            if (lane == 0) ticket = atomicAdd(P.ws.tickets + row, 1);
+            ticket = __shfl_sync(kFull, ticket, 0);
+            if (ticket != nchunks - 1) continue;
+            __threadfence();
+            if (lane == 0) P.ws.tickets[row] = 0;  // ready for the next launch / replay
+            b.n = 0;
+            b.kb = 0;
+            b.closed = false;
+            for (int c = 0; c < nchunks && !b.closed; ++c) {
+                const int64_t cs = row * P.chunks_per_row + c;
+                const int cnt = __ldcg(P.ws.counts + cs);
+                for (int g = 0; g < cnt && !b.closed; g += 32) {
+                    const int e = g + lane;
+                    const bool in = e < cnt;
+                    const uint32_t key = in ? __ldcg(P.ws.keys + cs * a.K + e) : 0u;
+                    const int32_t id = in ? __ldcg(P.ws.ids + cs * a.K + e) : 0;
+                    while (true) {
+                        const unsigned m = (in && key >= b.kb) ? 1u : 0u;
+                        int pos;
+                        if (!buf_try_append<E::kKeyBits, E::kKeyMax>(b, m, cap, kp, lane, pos)) {
+                            if (b.closed) break;
+                            continue;
+                        }
+                        if (pos >= 0 && m) {
+                            b.keys[pos] = key;
+                            b.ids[pos] = id;
+                        }
+                        __syncwarp();
+                        break;
+                    }
+                }
+            }
+            if (b.n > kp) buf_compact<E::kKeyBits, E::kKeyMax>(b, kp, lane);
+        }
+        __syncwarp();
+        write_outputs(P, row, n, lo, hi, kp, false, b.ids, causal_len, req, lane);
+        __syncwarp();
+    }
+}
+
+template <bool BF16, int NV, int R>
+cudaError_t launch_t(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
+    auto kern = select_kernel<BF16, NV, R>;
+    if (pol.smem_bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             pol.smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<pol.grid, kThreads, pol.smem_bytes, st>>>(P);
+    return cudaGetLastError();
+}
+
+template <bool BF16, int NV>
+cudaError_t launch_nv(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
+    switch (pol.reps_per_lane) {
+        case 1: return launch_t<BF16, NV, 1>(P, pol, st);
+        case 2: return launch_t<BF16, NV, 2>(P, pol, st);
+        default: return launch_t<BF16, NV, 2 * NV>(P, pol, st);
+    }
+}
+
+template <bool BF16>
+cudaError_t launch_dt(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
+    switch (pol.vecs_per_lane) {
+        case 1: return launch_nv<BF16, 1>(P, pol, st);
+        case 2: return launch_nv<BF16, 2>(P, pol, st);
+        default: return launch_nv<BF16, 4>(P, pol, st);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
+                          const SplitWorkspace& ws, cudaStream_t stream) {
+    KernelParams P;
+    P.a = a;
+    P.ws = Split{ws.keys, ws.ids, ws.counts, ws.tickets};
+    P.chunks_per_row = pol.chunks_per_row;
+    P.cap = pol.cand_capacity;
+    P.rows = a.T * a.H;
+    const int vec = a.dtype == BSA_DTYPE_BF16 ? 8 : 4;
+    const int64_t max_vecs = (a.M + vec - 1) / vec + 1;
+    int64_t vpc = (max_vecs + pol.chunks_per_row - 1) / pol.chunks_per_row;
+    const int64_t pass = 32LL * pol.vecs_per_lane;
+    vpc = (vpc + pass - 1) / pass * pass;
+    P.vecs_per_chunk = (int32_t)vpc;
+    if (P.rows == 0) return cudaSuccess;
+    return a.dtype == BSA_DTYPE_BF16 ? launch_dt<true>(P, pol, stream)
+                                     : launch_dt<false>(P, pol, stream);
+}
+
+}  // namespace bsa

@@ -1,0 +1,177 @@
+// bsa_table.cu -- causal page counts and the page-16 sparse block table.
+//
+// Causal page count: vLLM PR #47502 report ("Using sparse_topk_select from MSA
+// instead of triton kernels"), section 关键源码片段, indexer_msa.py metadata
+// field "per-token causal page count cdiv(seq_pos+1, PAGE_SIZE)" with
+// PAGE_SIZE = 128, and the batch-wide topk_cu_seqlens_q / topk_prefix_lens.
+// Decode row mapping and the sparse table: vLLM PR #47984 report ("Support
+// speculative decode with AITER sparse PA"), sections 实现拆解 items 1-3 and
+// 关键源码片段: row = req*dql + local_q, query position
+// seq_len[req] - dql + local_q, causal_len = max(pos + 1, 0); each kept
+// 128-token block becomes 8 page-16 entries through the request's block
+// table; ids outside [0, cdiv(causal_len, 128)) and -1 are ignored; padded
+// rows give an empty context.
+//
+// Both kernels are tiny integer passes bound by memory latency; the table
+// builder gives one warp to each (token, head) row and deduplicates and sorts
+// the row's ids in shared memory by counting ranks (K <= 1024 ids).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bsa_internal.h"
+
+namespace bsa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__global__ void nvp_decode_kernel(const int32_t* __restrict__ seq_lens, int64_t num_reqs,
+                                  int32_t dql, int32_t* __restrict__ out) {
+    const int64_t total = num_reqs * dql;
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < total;
+         r += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t req = r / dql;
+        const int64_t pos = (int64_t)__ldg(seq_lens + req) - dql + (r - req * dql);
+        out[r] = pos >= 0 ? (int32_t)((pos + kPageSize) >> kLogPageSize) : 0;
+    }
+}
+
+__global__ void nvp_varlen_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ prefix,
+                                  int64_t num_seqs, int64_t total_q, int32_t* __restrict__ out) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < total_q;
+         r += (int64_t)gridDim.x * blockDim.x) {
+        int32_t pages = 0;
+        if (num_seqs > 0 && r >= __ldg(cu) && r < __ldg(cu + num_seqs)) {
+            // largest i with cu[i] <= r
+            int64_t lo = 0, hi = num_seqs;  // cu[lo] <= r < cu[hi]
+            while (hi - lo > 1) {
+                const int64_t mid = (lo + hi) >> 1;
+                if (__ldg(cu + mid) <= r) lo = mid;
+                else hi = mid;
+            }
+            const int64_t pos = (int64_t)__ldg(prefix + lo) + (r - __ldg(cu + lo));
+            pages = pos >= 0 ? (int32_t)((pos + kPageSize) >> kLogPageSize) : 0;
+        }
+        out[r] = pages;
+    }
+}
+
+constexpr int kTableWarps = 4;
+
+// Shared memory per warp: ids[K], first-occurrence flags[K], sorted[K].
+__global__ void __launch_bounds__(kTableWarps * 32)
+sparse_table_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t H, int32_t K,
+                    const int32_t* __restrict__ block_table, int64_t max_blocks,
+                    const int32_t* __restrict__ seq_lens, int32_t dql,
+                    int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx) {
+    extern __shared__ int32_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    int32_t* s_ids = smem + (size_t)warp * 3 * K;
+    int32_t* s_first = s_ids + K;
+    int32_t* s_sorted = s_first + K;
+    const int width = K * kPagesPerBlock;
+    for (int64_t row = (int64_t)blockIdx.x * kTableWarps + warp; row < rows;
+         row += (int64_t)gridDim.x * kTableWarps) {
+        const int64_t t = row / H;
+        const int64_t req = t / dql;
+        const int64_t pos = (int64_t)__ldg(seq_lens + req) - dql + (t - req * dql);
+        const int64_t causal_len = pos + 1 > 0 ? pos + 1 : 0;
+        const int64_t nblk = (causal_len + kPageSize - 1) >> kLogPageSize;
+        const int64_t limit = nblk < max_blocks ? nblk : max_blocks;
+        const int32_t* ids = topk_idx + row * K;
+        for (int i = lane; i < K; i += 32) {
+            const int32_t x = __ldg(ids + i);
+            s_ids[i] = (x >= 0 && x < limit) ? x : -1;
+        }
+        __syncwarp();
+        // first occurrence of each valid id
+        for (int i = lane; i < K; i += 32) {
+            const int32_t x = s_ids[i];
+            bool first = x >= 0;
+            for (int j = 0; j < i && first; ++j) first = s_ids[j] != x;
+            s_first[i] = first ? 1 : 0;
+        }
+        __syncwarp();
+        // rank = number of distinct valid ids below x; scatter to sorted order
+        int count = 0;
+        for (int i = lane; i < K; i += 32) {
+            if (!s_first[i]) continue;
+            const int32_t x = s_ids[i];
+            int rank = 0;
+            for (int j = 0; j < K; ++j) rank += (s_first[j] && s_ids[j] < x) ? 1 : 0;
+            s_sorted[rank] = x;
+            ++count;
+        }
+        const int n = __reduce_add_sync(kFull, count);
+        __syncwarp();
+        const int32_t* table = block_table + req * max_blocks;
+        int32_t* bt = sparse_bt + row * (int64_t)width;
+        for (int e = lane; e < width; e += 32) {
+            const int j = e >> 3;
+            const int pg = e & 7;
+            int32_t val = 0;
+            if (j < n) {
+                const int32_t b = s_sorted[j];
+                if ((int64_t)b * kPageSize + (int64_t)pg * kSubPage < causal_len)
+                    val = __ldg(table + b) * kPagesPerBlock + pg;
+            }
+            bt[e] = val;
+        }
+        int ctx = 0;
+        for (int j = lane; j < n; j += 32) {
+            const int64_t rem = causal_len - (int64_t)s_sorted[j] * kPageSize;
+            ctx += (int)(rem < kPageSize ? rem : kPageSize);
+        }
+        ctx = __reduce_add_sync(kFull, ctx);
+        if (lane == 0) sparse_ctx[row] = ctx;
+        __syncwarp();
+    }
+}
+
+int grid_for(int64_t work, int per_block, int max_blocks_per_sm) {
+    int64_t g = (work + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)device_sm_count() * max_blocks_per_sm;
+    if (g > cap) g = cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_num_valid_pages_decode(const int32_t* seq_lens, int64_t num_reqs, int32_t dql,
+                                          int32_t* out, cudaStream_t stream) {
+    const int64_t total = num_reqs * dql;
+    if (total == 0) return cudaSuccess;
+    nvp_decode_kernel<<<grid_for(total, 256, 8), 256, 0, stream>>>(seq_lens, num_reqs, dql, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_num_valid_pages_varlen(const int32_t* cu, const int32_t* prefix,
+                                          int64_t num_seqs, int64_t total_q, int32_t* out,
+                                          cudaStream_t stream) {
+    if (total_q == 0) return cudaSuccess;
+    nvp_varlen_kernel<<<grid_for(total_q, 256, 8), 256, 0, stream>>>(cu, prefix, num_seqs,
+                                                                     total_q, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, int64_t H,
+                                            int32_t K, const int32_t* block_table,
+                                            int64_t max_blocks, const int32_t* seq_lens,
+                                            int32_t dql, int32_t* sparse_bt,
+                                            int32_t* sparse_ctx, cudaStream_t stream) {
+    const int64_t rows = T * H;
+    if (rows == 0) return cudaSuccess;
+    const size_t smem = (size_t)kTableWarps * 3 * K * sizeof(int32_t);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(sparse_table_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    sparse_table_kernel<<<grid_for(rows, kTableWarps, 16), kTableWarps * 32, smem, stream>>>(
+        topk_idx, rows, H, K, block_table, max_blocks, seq_lens, dql, sparse_bt, sparse_ctx);
+    return cudaGetLastError();
+}
+
+}  // namespace bsa

@@ -1,0 +1,139 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+symbol the header declares, and its host-side logic (argument checks, the
+launch policy and its capacity boundaries) behaves as documented.  No call
+here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bsa_topk.h")
+
+
+@pytest.fixture(scope="module")
+def bsa():
+    from block_sparse_attention_topk_gb300 import build
+    build.build()
+    import block_sparse_attention_topk_gb300 as m
+    m.lib()
+    return m
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names(bsa):
+    assert _declared() == sorted(bsa.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(bsa):
+    L = ctypes.CDLL(bsa.library_path())
+    for name in _declared():
+        assert hasattr(L, name), f"{name} not exported"
+
+
+def test_library_is_built_for_sm103a(bsa):
+    from block_sparse_attention_topk_gb300 import build
+    assert "arch=compute_103a,code=sm_103a" in build.ARCH
+
+
+def test_status_strings(bsa):
+    L = bsa.lib()
+    for code in range(-7, 1):
+        s = L.bsa_status_string(code).decode()
+        assert s and s != "unknown status"
+
+
+def _policy(bsa, rows, M, K, dtype, sms=152):
+    return bsa.bsa_select_policy(rows, M, K, dtype, sms)
+
+
+BF, FP = 0, 1
+
+
+@pytest.mark.parametrize("M,dtype,nv", [
+    (16, FP, 1), (74, BF, 1), (128, BF, 1), (129, BF, 1), (256, BF, 1), (257, BF, 2),
+    (512, BF, 2), (513, BF, 4), (1024, BF, 4), (8192, BF, 4),
+    (74, FP, 1), (128, FP, 1), (129, FP, 2), (256, FP, 2), (257, FP, 4), (1024, FP, 4)])
+def test_policy_vectors_per_lane(bsa, M, dtype, nv):
+    assert _policy(bsa, 1000, M, 16, dtype)["vecs_per_lane"] == nv
+
+
+def test_policy_production_capacity_single_pass(bsa):
+    """The production 8k+1k graph (74 blocks, query length 4, topk 16) and
+    every capacity up to 128 run one warp per row in a single pass."""
+    for M in (65, 74, 128):
+        for rows in (4, 64 * 4 * 4, 10**6):
+            p = _policy(bsa, rows, M, 16, BF)
+            assert p["path"] == bsa.BSA_PATH_ROW and p["chunks_per_row"] == 1
+            assert p["vecs_per_lane"] == 1
+
+
+@pytest.mark.parametrize("K,reps", [(1, 1), (16, 1), (17, 2), (48, 2), (49, 8), (64, 8)])
+def test_policy_representatives(bsa, K, reps):
+    assert _policy(bsa, 1000, 1024, K, BF)["reps_per_lane"] == reps
+
+
+def test_policy_split_only_for_few_long_rows(bsa):
+    # 1024 bf16 tiles fit one pass: never split
+    assert _policy(bsa, 8, 1024, 16, BF)["chunks_per_row"] == 1
+    # 8192 tiles, few rows: split over up to 8 warps
+    p = _policy(bsa, 48, 8192, 16, BF)
+    assert p["path"] == bsa.BSA_PATH_SPLIT and p["chunks_per_row"] == 8
+    # many rows fill the GPU by themselves
+    assert _policy(bsa, 1 << 20, 8192, 16, BF)["chunks_per_row"] == 1
+    # chunks shrink as rows grow
+    assert _policy(bsa, 2432, 8192, 16, BF)["chunks_per_row"] == 2
+
+
+def test_policy_capacity_and_grid(bsa):
+    p = _policy(bsa, 10**6, 1024, 16, BF)
+    assert p["cand_capacity"] >= 16 + 32 * 8 and p["cand_capacity"] % 32 == 0
+    assert p["smem_bytes"] == p["warps_per_cta"] * p["cand_capacity"] * 8
+    assert p["grid"] == 152 * 4
+    assert _policy(bsa, 10, 74, 16, BF)["grid"] == 2
+
+
+def test_policy_rejects(bsa):
+    L = bsa.lib()
+    pol = bsa.LaunchPolicy()
+    assert L.bsa_select_policy(10, 74, 16, 5, 152, ctypes.byref(pol)) == -4
+    assert L.bsa_select_policy(10, 0, 1, 0, 152, ctypes.byref(pol)) == -2
+    assert L.bsa_select_policy(10, 74, 75, 0, 152, ctypes.byref(pol)) == -3
+    assert L.bsa_select_policy(10, 74, 16, 0, 152, None) == -1
+
+
+def test_host_argument_checks_launch_nothing(bsa):
+    """Invalid arguments are rejected on the host before any CUDA call."""
+    L = bsa.lib()
+    nul = ctypes.c_void_p(0)
+    sel = L.bsa_topk_select
+    # K out of range, K < init + local, unknown dtype, bad sizes, null pointers
+    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 0, 0, 0, nul, nul, 0, nul) == -3
+    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 33, 0, 0, nul, nul, 0, nul) == -3
+    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 2, 2, 1, nul, nul, 0, nul) == -3
+    assert sel(nul, 9, 4, 1, 32, 32, 32, nul, 4, 1, 1, nul, nul, 0, nul) == -4
+    assert sel(nul, 0, 4, 1, 0, 32, 32, nul, 4, 1, 1, nul, nul, 0, nul) == -2
+    assert sel(nul, 0, 4, 2, 32, 40, 32, nul, 4, 1, 1, nul, nul, 0, nul) == -2
+    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 4, 1, 1, nul, nul, 0, nul) == -1
+    assert sel(ctypes.c_void_p(0x1001), 0, 4, 1, 32, 32, 32, ctypes.c_void_p(0x2000), 4, 1, 1,
+               ctypes.c_void_p(0x3000), nul, 0, nul) == -7
+    # empty batches are a no-op
+    assert sel(nul, 0, 0, 1, 32, 32, 32, nul, 4, 1, 1, nul, nul, 0, nul) == 0
+    tbl = L.bsa_build_sparse_block_table
+    assert tbl(nul, 5, 1, 4, nul, 2, 3, nul, 2, nul, nul, nul) == -6
+    assert tbl(nul, 4, 1, 0, nul, 2, 3, nul, 2, nul, nul, nul) == -3
+    assert tbl(nul, 4, 1, 4, nul, 2, 3, nul, 2, nul, nul, nul) == -1
+    fused = L.bsa_topk_select_sparse_table
+    assert fused(nul, 0, 4, 0, 1, 32, 32, 32, nul, 4, 1, 1, nul, 3, nul, nul, nul, nul, 0,
+                 nul) == -2
+    assert fused(nul, 0, 4, 1, 1, 32, 32, 32, nul, 40, 1, 1, nul, 3, nul, nul, nul, nul, 0,
+                 nul) == -3
+    assert L.bsa_num_valid_pages_decode(nul, 4, 0, nul, nul) == -2
+    assert L.bsa_num_valid_pages_decode(nul, 4, 1, nul, nul) == -1
+    assert L.bsa_num_valid_pages_varlen(nul, nul, 2, -1, nul, nul) == -2
