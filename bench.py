@@ -388,8 +388,9 @@ def run_e2e(args, w, table, device, stream, rows):
 
 
 def config_latencies(device):
-    """Latency of one fused/select call on each workload as given (inputs
-    resident in HBM; L2 flushed before each timed call by writing 256 MB)."""
+    """Latency of one fused/select call on each workload as given: the call is
+    captured in a CUDA graph and each replay is timed with events (inputs
+    resident in HBM; L2 flushed before each replay by writing 256 MB)."""
     import synth
     import block_sparse_attention_topk_gb300 as bsa
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=device)
@@ -419,12 +420,20 @@ def config_latencies(device):
                 bsa.bsa_topk_select(w.scores, nvp, w.K, w.num_init, w.num_local)
         for _ in range(5):
             call()
+        torch.cuda.synchronize()
+        # capture once, replay: the timed span holds the kernel(s) only
+        graph = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream(device)
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(graph, stream=st):
+                call()
+        torch.cuda.synchronize()
         times = []
         for _ in range(30):
             flush.fill_(1)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            call()
+            graph.replay()
             b.record()
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b) * 1e3)

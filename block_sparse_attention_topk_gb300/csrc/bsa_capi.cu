@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <climits>
 #include <mutex>
 
 #include "bsa_internal.h"
@@ -96,7 +97,31 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
     }
     int warps = 8;
     const int cap = (int)((K + 32 * vec + 31) / 32 * 32);
-    const int smem = warps * cap * 8;
+    int smem = warps * cap * 8;
+    // Group path (4 lanes per row, 8 rows per warp) for topk <= 32 and rows
+    // of at most 2 KB; its overflow fallback is the warp path with one pass.
+    const int elem = dtype == BSA_DTYPE_BF16 ? 2 : 4;
+    if (K <= kGroupMaxK && M * elem <= kGroupMaxBytes) {
+        const int gsmem = warps * (int)(dtype == BSA_DTYPE_BF16
+                                            ? sizeof(GroupSmem<uint32_t>)
+                                            : sizeof(GroupSmem<unsigned long long>));
+        int ctas = 3;
+        while (ctas > 1 && ctas * (gsmem + 1024) > 228 * 1024) --ctas;
+        const int64_t items = (rows + kGroupRows - 1) / kGroupRows;
+        int64_t grid = (items + warps - 1) / warps;
+        const int64_t grid_cap = (int64_t)num_sms * ctas;
+        if (grid > grid_cap) grid = grid_cap;
+        if (grid < 1) grid = 1;
+        p->path = BSA_PATH_GROUP;
+        p->vecs_per_lane = 4;
+        p->chunks_per_row = 1;
+        p->reps_per_lane = K <= 16 ? 4 : 8;
+        p->warps_per_cta = warps;
+        p->grid = (int32_t)grid;
+        p->cand_capacity = cap;
+        p->smem_bytes = gsmem;
+        return BSA_OK;
+    }
     const int64_t items = rows * chunks;
     int ctas_per_sm = 4;
     const int smem_budget = 227 * 1024;
@@ -119,6 +144,7 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
 int run_select(SelectArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     bsa_launch_policy_t pol;
     const int64_t rows = a.T * a.H;
+    if (rows > INT32_MAX) return BSA_ERR_SHAPE;
     make_policy(rows, a.M, a.K, a.dtype, device_sm_count(), &pol);
     const size_t need = split_workspace_bytes(rows, pol.chunks_per_row, a.K);
     if (need > 0) {

@@ -15,6 +15,40 @@ constexpr int kSubPage = BSA_SUB_PAGE_SIZE;           // tokens per table entry
 constexpr int kPagesPerBlock = BSA_PAGES_PER_SPARSE_BLOCK;
 constexpr int kLogPageSize = 7;
 
+// Group path: 4 lanes per row, 8 rows per warp (see bsa_select.cu).
+constexpr int kGroupLanes = 4;       // lanes per row
+constexpr int kGroupRows = 8;        // rows per warp
+constexpr int kGroupMaxVecs = 130;   // 16-byte vectors per row the group path covers
+constexpr int kGroupCand = 64;       // candidate capacity per row
+constexpr int kGroupMaxK = 32;       // largest topk the group path serves
+constexpr int kGroupMaxBytes = 2048; // capacity x element size the group path covers
+
+struct GroupRowDesc {
+    unsigned long long v0;       // first 16-byte vector of the non-forced range
+    unsigned long long row_ptr;  // address of element 0 of the row
+    int32_t base_id, lo, hi, theta;
+    int32_t fast, pad;
+};
+
+// Shared memory of one warp of the group path.  CK is the composite key type
+// (uint32 for bf16, uint64 for fp32).
+template <typename CK>
+struct GroupSmem {
+    int16_t vmax[kGroupRows][kGroupMaxVecs];   // per-vector maxima (raw signed)
+    union {
+        uint16_t queue[kGroupRows * kGroupMaxVecs];  // (row << 13 | vector) work items
+        struct {
+            int32_t sel[kGroupRows][kGroupMaxK];     // selected ids, any order
+            int32_t sorted[kGroupRows][kGroupMaxK];  // selected ids, ascending
+        } s;
+    } q;
+    CK cand[kGroupRows][kGroupCand + 1];       // candidate composite keys
+    int32_t ccount[kGroupRows];
+    int32_t scount[kGroupRows];
+    int32_t ovf[kGroupRows];
+    GroupRowDesc desc[kGroupRows];
+};
+
 // Everything one selector launch needs.  Pointers are device pointers.
 struct SelectArgs {
     const void* scores;

@@ -51,6 +51,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "bsa_internal.h"
 
 namespace bsa {
@@ -323,50 +325,62 @@ __device__ void write_outputs(const KernelParams& P, int64_t row, int n, int lo,
     }
 }
 
+// Row geometry shared by both paths: causal bound, forced ranges, how many
+// non-forced ids to select.
+struct RowInfo {
+    int64_t t, h, req, causal_len;
+    int v, lo, hi, n, kp;
+    bool all, need;
+};
+
+__device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int64_t row) {
+    RowInfo r;
+    // rows < 2^31 (checked on the host): 32-bit division is exact
+    const uint32_t t32 = (uint32_t)row / (uint32_t)a.H;
+    r.t = t32;
+    r.h = row - r.t * a.H;
+    int64_t pages;
+    r.causal_len = 0;
+    r.req = 0;
+    if (a.fused) {
+        const uint32_t req32 = t32 / (uint32_t)a.dql;
+        r.req = req32;
+        const int64_t lq = r.t - r.req * a.dql;
+        const int64_t pos = (int64_t)__ldg(a.seq_lens + r.req) - a.dql + lq;
+        r.causal_len = pos + 1 > 0 ? pos + 1 : 0;
+        pages = (r.causal_len + kPageSize - 1) >> kLogPageSize;
+    } else {
+        pages = __ldg(a.num_valid_pages + r.t);
+    }
+    r.v = (int)(pages < 0 ? 0 : (pages > a.M ? a.M : pages));
+    r.lo = a.num_init < r.v ? a.num_init : r.v;
+    r.hi = max(r.v - a.num_local, r.lo);
+    r.n = a.K < r.v ? a.K : r.v;
+    r.kp = r.n - r.lo - (r.v - r.hi);         // non-forced ids to select
+    r.all = r.kp >= r.hi - r.lo;              // every non-forced id fits
+    r.need = r.kp > 0 && !r.all;
+    return r;
+}
+
+// One work item (row, chunk) processed by a whole warp: the warp path, and
+// the fallback of the group path for rows whose candidates overflow.
 template <bool BF16, int NV, int R>
-__global__ void __launch_bounds__(kThreads, 4) select_kernel(const KernelParams P) {
+__device__ void warp_item(const KernelParams& P, int64_t row, int chunk, uint32_t* s_keys,
+                          int32_t* s_ids, int lane) {
     using E = Elem<BF16>;
     constexpr int VEC = E::kVec;
     constexpr int S = E::kBytes;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
     const SelectArgs& a = P.a;
     const int cap = P.cap;
-    uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem_raw) + (size_t)warp * cap * 2;
-    int32_t* s_ids = reinterpret_cast<int32_t*>(s_keys + cap);
-
-    const int64_t items = P.rows * P.chunks_per_row;
-    const int64_t warps_total = (int64_t)gridDim.x * kWarpsPerCta;
-    for (int64_t item = (int64_t)blockIdx.x * kWarpsPerCta + warp; item < items;
-         item += warps_total) {
-        const int64_t row = item / P.chunks_per_row;
-        const int chunk = (int)(item - row * P.chunks_per_row);
-        const int64_t t = row / a.H;
-        const int64_t h = row - t * a.H;
-
-        // ---- causal bound of the row ----
-        int64_t causal_len = 0, req = 0, pages;
-        if (a.fused) {
-            req = t / a.dql;
-            const int64_t lq = t - req * a.dql;
-            const int64_t pos = (int64_t)__ldg(a.seq_lens + req) - a.dql + lq;
-            causal_len = pos + 1 > 0 ? pos + 1 : 0;
-            pages = (causal_len + kPageSize - 1) >> kLogPageSize;
-        } else {
-            pages = __ldg(a.num_valid_pages + t);
-        }
-        const int v = (int)(pages < 0 ? 0 : (pages > a.M ? a.M : pages));
-        const int lo = a.num_init < v ? a.num_init : v;
-        const int hi = max(v - a.num_local, lo);
-        const int n = a.K < v ? a.K : v;
-        const int kp = n - lo - (v - hi);            // non-forced ids to select
-        const bool all = kp >= hi - lo;              // every non-forced id fits
-        const bool need = kp > 0 && !all;
+    {
+        const RowInfo ri = row_info(a, row);
+        const int64_t t = ri.t, h = ri.h, causal_len = ri.causal_len, req = ri.req;
+        const int lo = ri.lo, hi = ri.hi, n = ri.n, kp = ri.kp;
+        const bool all = ri.all, need = ri.need;
 
         if (!need) {
             if (chunk == 0) write_outputs(P, row, n, lo, hi, kp, all, s_ids, causal_len, req, lane);
-            continue;
+            return;
         }
 
         // ---- vector grid over the non-forced range [lo, hi) ----
@@ -378,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const KernelParams 
         const int nvec = (int)((a_hi - v0 + 15) >> 4);
         const int base_id = lo - (int)((a_lo - v0) / S);
         const int nchunks = (nvec + P.vecs_per_chunk - 1) / P.vecs_per_chunk;
-        if (chunk >= nchunks) continue;
+        if (chunk >= nchunks) return;
         const int k_begin = chunk * P.vecs_per_chunk;
         const int k_end = min(nvec, k_begin + P.vecs_per_chunk);
 
@@ -520,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const KernelParams 
             int ticket = 0;
             if (lane == 0) ticket = atomicAdd(P.ws.tickets + row, 1);
             ticket = __shfl_sync(kFull, ticket, 0);
-            if (ticket != nchunks - 1) continue;
+            if (ticket != nchunks - 1) return;
             __threadfence();
             if (lane == 0) P.ws.tickets[row] = 0;  // ready for the next launch / replay
             b.n = 0;
@@ -555,6 +569,396 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const KernelParams 
         __syncwarp();
         write_outputs(P, row, n, lo, hi, kp, false, b.ids, causal_len, req, lane);
         __syncwarp();
+    }
+}
+
+template <bool BF16, int NV, int R>
+__global__ void __launch_bounds__(kThreads, 4) select_kernel(const KernelParams P) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem_raw) + (size_t)warp * P.cap * 2;
+    int32_t* s_ids = reinterpret_cast<int32_t*>(s_keys + P.cap);
+    const int64_t items = P.rows * P.chunks_per_row;
+    const int64_t warps_total = (int64_t)gridDim.x * kWarpsPerCta;
+    for (int64_t item = (int64_t)blockIdx.x * kWarpsPerCta + warp; item < items;
+         item += warps_total) {
+        int64_t row = item;
+        int chunk = 0;
+        if (P.chunks_per_row > 1) {
+            row = (uint32_t)item / (uint32_t)P.chunks_per_row;
+            chunk = (int)(item - row * P.chunks_per_row);
+        }
+        warp_item<BF16, NV, R>(P, row, chunk, s_keys, s_ids, lane);
+    }
+}
+
+
+// ===========================================================================
+// Group path: 4 lanes per row, 8 rows per warp.
+//
+// The warp path spends a full warp instruction on every per-row step (the
+// threshold search, scans, the exact select), which bounds it by instruction
+// issue long before HBM.  Here the 8 rows of a warp run those steps side by
+// side, 4 lanes each:
+//  1. pass 1: the 4 lanes of a row stream its non-forced range (64 contiguous
+//     bytes per row per load instruction), store every 16-byte vector's
+//     maximum (raw signed; fp32 keeps its top 16 bits) in shared memory, and
+//     keep R representatives per lane;
+//  2. theta = the K'-th largest of the row's 4R representatives (a 12-bit
+//     search with 4-lane shuffle counts; coarse bits only make theta lower);
+//  3. the vectors whose maximum reaches theta are queued warp-wide, so the
+//     32 lanes share the detailed work of all 8 rows evenly;
+//  4. the queued vectors are reloaded (L1/L2) and their elements >= theta are
+//     appended to the row's candidate list as unique composite keys
+//     (key << 16 | 0xFFFF - id for bf16, key << 32 | ~id for fp32), so their
+//     order in the list does not matter;
+//  5. each candidate's rank among the row's candidates decides selection;
+//     the K' selected ids are sorted ascending by rank counting;
+//  6. the 4 lanes write ids, and in fused mode the table and ctx.
+// A row without a theta (fewer than K' non-negative representatives) takes
+// every valid element as a candidate when they fit; a row whose candidates
+// overflow the list is redone by the whole warp with the warp path.
+// ===========================================================================
+
+template <bool BF16>
+__device__ __forceinline__ uint4 group_load(int k, uintptr_t v0, uintptr_t a_lo, uintptr_t a_hi,
+                                            int base_id, int lo, int hi, const char* row_ptr) {
+    using E = Elem<BF16>;
+    constexpr int VEC = E::kVec;
+    constexpr int S = E::kBytes;
+    const uintptr_t addr = v0 + ((uintptr_t)k << 4);
+    if (addr >= a_lo && addr + 16 <= a_hi)
+        return __ldg(reinterpret_cast<const uint4*>(addr));
+    uint4 w = make_uint4(E::kMaskWord, E::kMaskWord, E::kMaskWord, E::kMaskWord);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        const int id = base_id + k * VEC + e;
+        if (id >= lo && id < hi) E::set(w, e, E::load_one(row_ptr + (int64_t)id * S));
+    }
+    return w;
+}
+
+// Two partial maxima of a vector (bf16: the two halves of the packed max;
+// fp32: even and odd elements), raw signed.
+template <bool BF16>
+__device__ __forceinline__ void vec_max_pair(const uint4& w, int32_t& x0, int32_t& x1) {
+    using E = Elem<BF16>;
+    if constexpr (BF16) {
+        const uint32_t pm = E::slot_pack_max(w);
+        x0 = E::pack_lo(pm);
+        x1 = E::pack_hi(pm);
+    } else {
+        x0 = E::even_max(w);
+        x1 = E::odd_max(w);
+    }
+}
+
+template <typename CK>
+__device__ __forceinline__ CK make_ck(uint32_t key, int id);
+template <>
+__device__ __forceinline__ uint32_t make_ck<uint32_t>(uint32_t key, int id) {
+    return (key << 16) | (0xFFFFu - (uint32_t)id);
+}
+template <>
+__device__ __forceinline__ unsigned long long make_ck<unsigned long long>(uint32_t key, int id) {
+    return ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)id);
+}
+__device__ __forceinline__ int32_t ck_id(uint32_t ck) { return (int32_t)(0xFFFFu - (ck & 0xFFFFu)); }
+__device__ __forceinline__ int32_t ck_id(unsigned long long ck) {
+    return (int32_t)(0xFFFFFFFFu - (uint32_t)ck);
+}
+
+__device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,
+                                             const int32_t* sorted) {
+    if (all || j < r.lo) return j;
+    if (j - r.lo < r.kp) return sorted[j - r.lo];
+    return r.hi + (j - r.lo - r.kp);
+}
+
+// Outputs of one row by its 4 lanes.  Every lane of the warp calls this
+// (the ctx sum shuffles within each group); `write` masks the stores.
+__device__ void group_write_outputs(const KernelParams& P, int64_t row, const RowInfo& r,
+                                    bool all, const int32_t* sorted, int q, bool write) {
+    const SelectArgs& a = P.a;
+    const int K = a.K;
+    if (write && a.out_idx != nullptr) {
+        int32_t* out = a.out_idx + row * K;
+        for (int s = q; s < K; s += kGroupLanes)
+            out[s] = s < r.n ? group_sel(s, r, all, sorted) : -1;
+    }
+    if (!a.fused) return;
+    int ctx = 0;
+    if (write) {
+        const int width = K * kPagesPerBlock;
+        int32_t* bt = a.sparse_bt + row * (int64_t)width;
+        const int32_t* table = a.block_table + r.req * a.max_blocks;
+        const bool vec_ok = ((reinterpret_cast<uintptr_t>(bt)) & 15) == 0;
+        // chunk c holds entries [4c, 4c + 4): one block j = c / 2, pages 4 (c & 1) + 0..3
+        for (int c = q; c * 4 < width; c += kGroupLanes) {
+            const int j = c >> 1;
+            const int pg0 = (c & 1) * 4;
+            int v[4] = {0, 0, 0, 0};
+            if (j < r.n) {
+                const int32_t b = group_sel(j, r, all, sorted);
+                const int64_t tok0 = (int64_t)b * kPageSize + (int64_t)pg0 * kSubPage;
+                if (b < a.max_blocks && tok0 < r.causal_len) {
+                    const int32_t phys8 = __ldg(table + b) * kPagesPerBlock + pg0;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        v[u] = tok0 + (int64_t)u * kSubPage < r.causal_len ? phys8 + u : 0;
+                }
+            }
+            if (vec_ok) {
+                *reinterpret_cast<int4*>(bt + 4 * c) = make_int4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) bt[4 * c + u] = v[u];
+            }
+        }
+        for (int j = q; j < r.n; j += kGroupLanes) {
+            const int32_t b = group_sel(j, r, all, sorted);
+            if (b < a.max_blocks) {
+                const int64_t rem = r.causal_len - (int64_t)b * kPageSize;
+                ctx += (int)(rem < kPageSize ? rem : kPageSize);
+            }
+        }
+    }
+    ctx += __shfl_xor_sync(kFull, ctx, 1);
+    ctx += __shfl_xor_sync(kFull, ctx, 2);
+    if (write && q == 0) a.sparse_ctx[row] = ctx;
+}
+
+template <bool BF16, int R>
+__global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelParams P) {
+    using E = Elem<BF16>;
+    using CK = typename std::conditional<BF16, uint32_t, unsigned long long>::type;
+    using G = GroupSmem<CK>;
+    constexpr int VEC = E::kVec;
+    constexpr int S = E::kBytes;
+    constexpr int H2 = R / 2;  // representative pairs per lane (divides 4)
+    static_assert(R == 2 || R == 4 || R == 8, "R must be 2, 4 or 8");
+    constexpr int kTop = BF16 ? 14 : 30;
+    constexpr int kLow = BF16 ? 3 : 19;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int g = lane >> 2;
+    const int q = lane & 3;
+    G& sm = *reinterpret_cast<G*>(smem_raw + (size_t)warp * sizeof(G));
+    const SelectArgs& a = P.a;
+    const unsigned lt = lanemask_lt();
+    const int64_t ngroups = (P.rows + kGroupRows - 1) / kGroupRows;
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
+
+    for (int64_t wg = (int64_t)blockIdx.x * kWarpsPerCta + warp; wg < ngroups; wg += stride) {
+        const int64_t row = wg * kGroupRows + g;
+        const bool active = row < P.rows;
+        RowInfo r{};
+        r.all = true;
+        if (active) r = row_info(a, row);
+        const bool need = active && r.need;
+
+        // ---- geometry of the non-forced range [lo, hi) ----
+        const char* row_ptr = nullptr;
+        uintptr_t a_lo = 0, a_hi = 0, v0 = 0;
+        int nvec = 0, base_id = 0;
+        if (need) {
+            row_ptr = reinterpret_cast<const char*>(a.scores) +
+                      (r.t * a.token_stride + r.h * a.head_stride) * S;
+            a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * S;
+            a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * S;
+            v0 = a_lo & ~(uintptr_t)15;
+            nvec = (int)((a_hi - v0 + 15) >> 4);
+            base_id = r.lo - (int)((a_lo - v0) / S);
+        }
+        const int my_steps = need ? (nvec - q + kGroupLanes - 1) / kGroupLanes : 0;
+
+        // ---- pass 1: vector maxima and representatives ----
+        int32_t rep[R];
+#pragma unroll
+        for (int x = 0; x < R; ++x) rep[x] = INT32_MIN;
+        for (int i0 = 0; i0 < my_steps; i0 += 4) {
+            uint4 w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                w[u] = i < my_steps ? group_load<BF16>(q + kGroupLanes * i, v0, a_lo, a_hi,
+                                                       base_id, r.lo, r.hi, row_ptr)
+                                    : make_uint4(E::kMaskWord, E::kMaskWord, E::kMaskWord,
+                                                 E::kMaskWord);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                if (i < my_steps) {
+                    int32_t x0, x1;
+                    vec_max_pair<BF16>(w[u], x0, x1);
+                    const int32_t m = max(x0, x1);
+                    sm.vmax[g][q + kGroupLanes * i] = (int16_t)(BF16 ? m : (m >> 16));
+                    rep[(u % H2) * 2] = max(rep[(u % H2) * 2], x0);
+                    rep[(u % H2) * 2 + 1] = max(rep[(u % H2) * 2 + 1], x1);
+                }
+            }
+        }
+
+        // ---- theta: K'-th largest representative of the row ----
+        int c0 = 0;
+#pragma unroll
+        for (int x = 0; x < R; ++x) c0 += rep[x] >= 0 ? 1 : 0;
+        c0 += __shfl_xor_sync(kFull, c0, 1);
+        c0 += __shfl_xor_sync(kFull, c0, 2);
+        const bool fast = need && c0 >= r.kp;
+        int32_t theta = 0;
+        for (int bit = kTop; bit >= kLow; --bit) {
+            const int32_t tt = theta | (1 << bit);
+            int c = 0;
+#pragma unroll
+            for (int x = 0; x < R; ++x) c += rep[x] >= tt ? 1 : 0;
+            c += __shfl_xor_sync(kFull, c, 1);
+            c += __shfl_xor_sync(kFull, c, 2);
+            if (c >= r.kp) theta = tt;
+        }
+        const bool ovf0 = need && !fast && (r.hi - r.lo) > kGroupCand;
+        if (q == 0) {
+            sm.ccount[g] = 0;
+            sm.scount[g] = 0;
+            sm.ovf[g] = ovf0 ? 1 : 0;
+            GroupRowDesc d;
+            d.v0 = v0;
+            d.row_ptr = reinterpret_cast<uintptr_t>(row_ptr);
+            d.base_id = base_id;
+            d.lo = r.lo;
+            d.hi = r.hi;
+            d.theta = theta;
+            d.fast = fast ? 1 : 0;
+            d.pad = 0;
+            sm.desc[g] = d;
+        }
+        const int32_t th16 = BF16 ? theta : (theta >> 16);
+        __syncwarp();
+
+        // ---- queue the vectors that can hold candidates ----
+        const int qsteps_lane = (need && !ovf0) ? my_steps : 0;
+        const int qsteps = __reduce_max_sync(kFull, qsteps_lane);
+        int qn = 0;
+        for (int i = 0; i < qsteps; ++i) {
+            const int k = q + kGroupLanes * i;
+            const bool hot = i < qsteps_lane && (!fast || sm.vmax[g][k] >= th16);
+            const unsigned b = __ballot_sync(kFull, hot);
+            if (hot) sm.q.queue[qn + __popc(b & lt)] = (uint16_t)((g << 13) | k);
+            qn += __popc(b);
+        }
+        __syncwarp();
+
+        // ---- candidates from the queued vectors, 32 at a time ----
+        for (int base = 0; base < qn; base += 32) {
+            const int e = base + lane;
+            if (e < qn) {
+                const int ent = sm.q.queue[e];
+                const int gg = ent >> 13;
+                const int k = ent & 0x1FFF;
+                const GroupRowDesc d = sm.desc[gg];
+                const char* rp = reinterpret_cast<const char*>(d.row_ptr);
+                const uintptr_t lo_addr = (uintptr_t)d.row_ptr + (uintptr_t)d.lo * S;
+                const uintptr_t hi_addr = (uintptr_t)d.row_ptr + (uintptr_t)d.hi * S;
+                const uint4 w = group_load<BF16>(k, (uintptr_t)d.v0, lo_addr, hi_addr, d.base_id,
+                                                 d.lo, d.hi, rp);
+                const int first_id = d.base_id + k * VEC;
+                unsigned m = 0;
+                if (d.fast) {
+#pragma unroll
+                    for (int x = 0; x < VEC; ++x)
+                        if (E::raw(w, x) >= d.theta) m |= 1u << x;
+                } else {
+#pragma unroll
+                    for (int x = 0; x < VEC; ++x) {
+                        const int id = first_id + x;
+                        if (id >= d.lo && id < d.hi) m |= 1u << x;
+                    }
+                }
+                const int nc = __popc(m);
+                if (nc) {
+                    int p = atomicAdd(&sm.ccount[gg], nc);
+                    if (p + nc <= kGroupCand) {
+                        while (m) {
+                            const int x = __ffs(m) - 1;
+                            m &= m - 1;
+                            sm.cand[gg][p++] = make_ck<CK>(E::key(E::raw(w, x)), first_id + x);
+                        }
+                    } else {
+                        sm.ovf[gg] = 1;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+
+        // ---- exact select: rank of each candidate among the row's ----
+        const bool ovf = sm.ovf[g] != 0;
+        const int cn = sm.ccount[g];
+        const bool sel_ok = need && !ovf;
+        if (sel_ok) {
+            for (int j = q; j < cn; j += kGroupLanes) {
+                const CK ck = sm.cand[g][j];
+                int rank = 0;
+                for (int m2 = 0; m2 < cn; ++m2) rank += sm.cand[g][m2] > ck ? 1 : 0;
+                if (rank < r.kp) {
+                    const int p = atomicAdd(&sm.scount[g], 1);
+                    sm.q.s.sel[g][p] = ck_id(ck);
+                }
+            }
+        }
+        __syncwarp();
+        if (sel_ok) {
+            for (int p = q; p < r.kp; p += kGroupLanes) {
+                const int32_t x = sm.q.s.sel[g][p];
+                int rk = 0;
+                for (int p2 = 0; p2 < r.kp; ++p2) rk += sm.q.s.sel[g][p2] < x ? 1 : 0;
+                sm.q.s.sorted[g][rk] = x;
+            }
+        }
+        __syncwarp();
+
+        // ---- outputs ----
+        group_write_outputs(P, row, r, r.all, sm.q.s.sorted[g], q, active && (!need || !ovf));
+
+        // ---- rows whose candidates overflowed: the whole warp redoes them ----
+        unsigned fb = __ballot_sync(kFull, q == 0 && need && ovf);
+        __syncwarp();
+        while (fb) {
+            const int bit = __ffs(fb) - 1;
+            fb &= fb - 1;
+            const int64_t frow = wg * kGroupRows + (bit >> 2);
+            uint32_t* s_keys = reinterpret_cast<uint32_t*>(&sm);
+            warp_item<BF16, 4, 2>(P, frow, 0, s_keys, reinterpret_cast<int32_t*>(s_keys + P.cap),
+                                  lane);
+            __syncwarp();
+        }
+        __syncwarp();
+    }
+}
+
+template <bool BF16, int R>
+cudaError_t launch_group_t(const KernelParams& P, const bsa_launch_policy_t& pol,
+                           cudaStream_t st) {
+    auto kern = group_select_kernel<BF16, R>;
+    if (pol.smem_bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             pol.smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<pol.grid, kThreads, pol.smem_bytes, st>>>(P);
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_group(const KernelParams& P, const bsa_launch_policy_t& pol,
+                         cudaStream_t st) {
+    switch (pol.reps_per_lane) {
+        case 2: return launch_group_t<BF16, 2>(P, pol, st);
+        case 4: return launch_group_t<BF16, 4>(P, pol, st);
+        default: return launch_group_t<BF16, 8>(P, pol, st);
     }
 }
 
@@ -605,6 +1009,9 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
     vpc = (vpc + pass - 1) / pass * pass;
     P.vecs_per_chunk = (int32_t)vpc;
     if (P.rows == 0) return cudaSuccess;
+    if (pol.path == BSA_PATH_GROUP)
+        return a.dtype == BSA_DTYPE_BF16 ? launch_group<true>(P, pol, stream)
+                                         : launch_group<false>(P, pol, stream);
     return a.dtype == BSA_DTYPE_BF16 ? launch_dt<true>(P, pol, stream)
                                      : launch_dt<false>(P, pol, stream);
 }

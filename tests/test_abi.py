@@ -56,31 +56,50 @@ def _policy(bsa, rows, M, K, dtype, sms=152):
 BF, FP = 0, 1
 
 
+@pytest.mark.parametrize("M,dtype,K,path", [
+    # group path: topk <= 32 and a row of at most 2 KB
+    (16, FP, 4, 2), (74, BF, 16, 2), (128, BF, 16, 2), (129, BF, 16, 2), (1024, BF, 16, 2),
+    (1025, BF, 16, 0), (512, FP, 16, 2), (513, FP, 16, 0), (1024, BF, 32, 2), (1024, BF, 33, 0),
+    (74, BF, 64, 0), (8192, BF, 16, 0)])
+def test_policy_path(bsa, M, dtype, K, path):
+    assert _policy(bsa, 10**6, M, K, dtype)["path"] == path
+
+
 @pytest.mark.parametrize("M,dtype,nv", [
-    (16, FP, 1), (74, BF, 1), (128, BF, 1), (129, BF, 1), (256, BF, 1), (257, BF, 2),
+    (74, BF, 1), (128, BF, 1), (129, BF, 1), (256, BF, 1), (257, BF, 2),
     (512, BF, 2), (513, BF, 4), (1024, BF, 4), (8192, BF, 4),
     (74, FP, 1), (128, FP, 1), (129, FP, 2), (256, FP, 2), (257, FP, 4), (1024, FP, 4)])
-def test_policy_vectors_per_lane(bsa, M, dtype, nv):
-    assert _policy(bsa, 1000, M, 16, dtype)["vecs_per_lane"] == nv
+def test_policy_vectors_per_lane_warp_path(bsa, M, dtype, nv):
+    """Warp path (topk 64): vectors per lane per pass switch at 32 lanes x
+    16 bytes x {1, 2}: bf16 at 256/257 and 512/513, fp32 at 128/129 and
+    256/257."""
+    assert _policy(bsa, 1000, M, 64, dtype)["vecs_per_lane"] == nv
 
 
-def test_policy_production_capacity_single_pass(bsa):
+def test_policy_production_capacity(bsa):
     """The production 8k+1k graph (74 blocks, query length 4, topk 16) and
-    every capacity up to 128 run one warp per row in a single pass."""
+    every capacity up to 128 run on the group path; at topk 64 they run one
+    warp per row in a single pass."""
     for M in (65, 74, 128):
         for rows in (4, 64 * 4 * 4, 10**6):
             p = _policy(bsa, rows, M, 16, BF)
-            assert p["path"] == bsa.BSA_PATH_ROW and p["chunks_per_row"] == 1
-            assert p["vecs_per_lane"] == 1
+            assert p["path"] == bsa.BSA_PATH_GROUP and p["chunks_per_row"] == 1
+            p = _policy(bsa, rows, M, 64, BF)
+            assert p["path"] == bsa.BSA_PATH_ROW and p["vecs_per_lane"] == 1
 
 
-@pytest.mark.parametrize("K,reps", [(1, 1), (16, 1), (17, 2), (48, 2), (49, 8), (64, 8)])
-def test_policy_representatives(bsa, K, reps):
+@pytest.mark.parametrize("K,reps", [(1, 4), (16, 4), (17, 8), (32, 8)])
+def test_policy_representatives_group(bsa, K, reps):
+    assert _policy(bsa, 1000, 1024, K, BF)["reps_per_lane"] == reps
+
+
+@pytest.mark.parametrize("K,reps", [(33, 2), (48, 2), (49, 8), (64, 8)])
+def test_policy_representatives_warp(bsa, K, reps):
     assert _policy(bsa, 1000, 1024, K, BF)["reps_per_lane"] == reps
 
 
 def test_policy_split_only_for_few_long_rows(bsa):
-    # 1024 bf16 tiles fit one pass: never split
+    # 1024 bf16 tiles: group path, never split
     assert _policy(bsa, 8, 1024, 16, BF)["chunks_per_row"] == 1
     # 8192 tiles, few rows: split over up to 8 warps
     p = _policy(bsa, 48, 8192, 16, BF)
@@ -92,11 +111,15 @@ def test_policy_split_only_for_few_long_rows(bsa):
 
 
 def test_policy_capacity_and_grid(bsa):
-    p = _policy(bsa, 10**6, 1024, 16, BF)
-    assert p["cand_capacity"] >= 16 + 32 * 8 and p["cand_capacity"] % 32 == 0
+    p = _policy(bsa, 10**6, 1024, 64, BF)
+    assert p["cand_capacity"] >= 64 + 32 * 8 and p["cand_capacity"] % 32 == 0
     assert p["smem_bytes"] == p["warps_per_cta"] * p["cand_capacity"] * 8
     assert p["grid"] == 152 * 4
-    assert _policy(bsa, 10, 74, 16, BF)["grid"] == 2
+    g = _policy(bsa, 10**6, 1024, 16, BF)
+    assert g["path"] == bsa.BSA_PATH_GROUP and g["grid"] == 152 * 3
+    # the warp fallback's buffer fits in a group warp's shared memory
+    assert g["cand_capacity"] * 8 <= g["smem_bytes"] // g["warps_per_cta"]
+    assert _policy(bsa, 10, 74, 16, BF)["grid"] == 1
 
 
 def test_policy_rejects(bsa):
