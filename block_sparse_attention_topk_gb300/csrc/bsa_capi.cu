@@ -115,7 +115,7 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
         p->path = BSA_PATH_GROUP;
         p->vecs_per_lane = 4;
         p->chunks_per_row = 1;
-        p->reps_per_lane = K <= 16 ? 4 : 8;
+        p->reps_per_lane = 8;
         p->warps_per_cta = warps;
         p->grid = (int32_t)grid;
         p->cand_capacity = cap;

@@ -19,32 +19,33 @@ constexpr int kLogPageSize = 7;
 constexpr int kGroupLanes = 4;       // lanes per row
 constexpr int kGroupRows = 8;        // rows per warp
 constexpr int kGroupMaxVecs = 130;   // 16-byte vectors per row the group path covers
-constexpr int kGroupCand = 64;       // candidate capacity per row
+constexpr int kGroupCand = 32;       // candidate capacity per row (one 4-lane sort)
 constexpr int kGroupMaxK = 32;       // largest topk the group path serves
 constexpr int kGroupMaxBytes = 2048; // capacity x element size the group path covers
+constexpr int kGroupStepsPad = 40;   // >= ceil(kGroupMaxVecs / kGroupLanes), multiple of 8
 
 struct GroupRowDesc {
     unsigned long long v0;       // first 16-byte vector of the non-forced range
     unsigned long long row_ptr;  // address of element 0 of the row
     int32_t base_id, lo, hi, theta;
-    int32_t fast, pad;
+    int32_t fast, nvec;
 };
 
 // Shared memory of one warp of the group path.  CK is the composite key type
 // (uint32 for bf16, uint64 for fp32).
 template <typename CK>
 struct GroupSmem {
-    int16_t vmax[kGroupRows][kGroupMaxVecs];   // per-vector maxima (raw signed)
+    // per-vector maxima (raw signed), lane-major: vector k = q + 4 i of row g
+    // at vmax[g][q][i]
+    int16_t vmax[kGroupRows][kGroupLanes][kGroupStepsPad];
     union {
         uint16_t queue[kGroupRows * kGroupMaxVecs];  // (row << 13 | vector) work items
         struct {
-            int32_t sel[kGroupRows][kGroupMaxK];     // selected ids, any order
             int32_t sorted[kGroupRows][kGroupMaxK];  // selected ids, ascending
         } s;
     } q;
-    CK cand[kGroupRows][kGroupCand + 1];       // candidate composite keys
+    CK cand[kGroupRows][kGroupCand];           // candidate composite keys
     int32_t ccount[kGroupRows];
-    int32_t scount[kGroupRows];
     int32_t ovf[kGroupRows];
     GroupRowDesc desc[kGroupRows];
 };

@@ -235,6 +235,7 @@ struct KernelParams {
     int32_t vecs_per_chunk;   // vectors (16 B) per work item
     int32_t cap;              // candidate buffer entries per warp
     int64_t rows;
+    uintptr_t buf_lo, buf_hi; // [first, last + 1) byte of the score buffer
 };
 
 // Candidate-buffer state of one warp.
@@ -333,9 +334,17 @@ struct RowInfo {
     bool all, need;
 };
 
-__device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int64_t row) {
-    RowInfo r;
+// The per-row metadata word: num_valid_pages[t] (select) or seq_lens[req]
+// (fused).  Split from row_info so the group path can load it one item early.
+__device__ __forceinline__ int32_t row_meta(const SelectArgs& a, int64_t row) {
     // rows < 2^31 (checked on the host): 32-bit division is exact
+    const uint32_t t32 = (uint32_t)row / (uint32_t)a.H;
+    if (a.fused) return __ldg(a.seq_lens + t32 / (uint32_t)a.dql);
+    return __ldg(a.num_valid_pages + t32);
+}
+
+__device__ __forceinline__ RowInfo row_info_from(const SelectArgs& a, int64_t row, int32_t meta) {
+    RowInfo r;
     const uint32_t t32 = (uint32_t)row / (uint32_t)a.H;
     r.t = t32;
     r.h = row - r.t * a.H;
@@ -346,11 +355,11 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int64_t row) {
         const uint32_t req32 = t32 / (uint32_t)a.dql;
         r.req = req32;
         const int64_t lq = r.t - r.req * a.dql;
-        const int64_t pos = (int64_t)__ldg(a.seq_lens + r.req) - a.dql + lq;
+        const int64_t pos = (int64_t)meta - a.dql + lq;
         r.causal_len = pos + 1 > 0 ? pos + 1 : 0;
         pages = (r.causal_len + kPageSize - 1) >> kLogPageSize;
     } else {
-        pages = __ldg(a.num_valid_pages + r.t);
+        pages = meta;
     }
     r.v = (int)(pages < 0 ? 0 : (pages > a.M ? a.M : pages));
     r.lo = a.num_init < r.v ? a.num_init : r.v;
@@ -360,6 +369,10 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int64_t row) {
     r.all = r.kp >= r.hi - r.lo;              // every non-forced id fits
     r.need = r.kp > 0 && !r.all;
     return r;
+}
+
+__device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int64_t row) {
+    return row_info_from(a, row, row_meta(a, row));
 }
 
 // One work item (row, chunk) processed by a whole warp: the warp path, and
@@ -621,22 +634,41 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const KernelParams 
 // overflow the list is redone by the whole warp with the warp path.
 // ===========================================================================
 
+// Load vector k of a row's non-forced range.  Vectors that stick out of
+// [lo, hi) (the first and the last) are loaded whole when they lie inside the
+// score buffer, element by element otherwise, and the ids outside [lo, hi)
+// are replaced by the mask pattern.
 template <bool BF16>
-__device__ __forceinline__ uint4 group_load(int k, uintptr_t v0, uintptr_t a_lo, uintptr_t a_hi,
-                                            int base_id, int lo, int hi, const char* row_ptr) {
+__device__ __forceinline__ uint4 group_load_edge(const KernelParams& P, int k, uintptr_t v0,
+                                                 int base_id, int lo, int hi,
+                                                 const char* row_ptr) {
     using E = Elem<BF16>;
     constexpr int VEC = E::kVec;
     constexpr int S = E::kBytes;
     const uintptr_t addr = v0 + ((uintptr_t)k << 4);
-    if (addr >= a_lo && addr + 16 <= a_hi)
-        return __ldg(reinterpret_cast<const uint4*>(addr));
-    uint4 w = make_uint4(E::kMaskWord, E::kMaskWord, E::kMaskWord, E::kMaskWord);
+    uint4 w;
+    if (addr >= P.buf_lo && addr + 16 <= P.buf_hi) {
+        w = __ldg(reinterpret_cast<const uint4*>(addr));
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        const int id = base_id + k * VEC + e;
-        if (id >= lo && id < hi) E::set(w, e, E::load_one(row_ptr + (int64_t)id * S));
+        for (int e = 0; e < VEC; ++e) {
+            const int id = base_id + k * VEC + e;
+            if (id < lo || id >= hi) E::set(w, e, (int32_t)E::kMaskWord);
+        }
+    } else {
+        w = make_uint4(E::kMaskWord, E::kMaskWord, E::kMaskWord, E::kMaskWord);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int id = base_id + k * VEC + e;
+            if (id >= lo && id < hi) E::set(w, e, E::load_one(row_ptr + (int64_t)id * S));
+        }
     }
     return w;
+}
+
+// Ask L2 to fetch [addr, addr + bytes) (16-byte aligned, multiple of 16)
+// ahead of use; no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(uintptr_t addr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
 }
 
 // Two partial maxima of a vector (bf16: the two halves of the packed max;
@@ -664,9 +696,103 @@ template <>
 __device__ __forceinline__ unsigned long long make_ck<unsigned long long>(uint32_t key, int id) {
     return ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)id);
 }
-__device__ __forceinline__ int32_t ck_id(uint32_t ck) { return (int32_t)(0xFFFFu - (ck & 0xFFFFu)); }
-__device__ __forceinline__ int32_t ck_id(unsigned long long ck) {
-    return (int32_t)(0xFFFFFFFFu - (uint32_t)ck);
+// The low field of a composite: 0xFFFF - id (bf16) or 0xFFFFFFFF - id (fp32);
+// larger means a lower id.
+__device__ __forceinline__ uint32_t ck_low(uint32_t ck) { return ck & 0xFFFFu; }
+__device__ __forceinline__ uint32_t ck_low(unsigned long long ck) { return (uint32_t)ck; }
+
+template <typename T>
+__device__ __forceinline__ T shfl_xor_any(T v, int m) {
+    if constexpr (sizeof(T) == 8) {
+        const uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, m);
+        const uint32_t hi = __shfl_xor_sync(kFull, (uint32_t)(v >> 32), m);
+        return ((T)hi << 32) | lo;
+    } else {
+        return __shfl_xor_sync(kFull, v, m);
+    }
+}
+
+// Bitonic sort, descending, of the 32 values a group of 4 lanes holds: lane
+// q keeps positions 8q .. 8q + 7 in x[0..7].  Compare-exchanges within a lane
+// stay in registers; those 8 or 16 positions apart use one shuffle per
+// register.  Every lane of the warp must call this.
+template <typename T>
+__device__ __forceinline__ void group_sort32_desc(T (&x)[8], int q) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= 8) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const T y = shfl_xor_any(x[r], j >> 3);
+                    const int p = q * 8 + r;
+                    const bool keep_max = ((p & j) == 0) == ((p & k) == 0);
+                    const T mx = x[r] > y ? x[r] : y;
+                    const T mn = x[r] > y ? y : x[r];
+                    x[r] = keep_max ? mx : mn;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    if ((r & j) == 0) {
+                        const int p = q * 8 + r;
+                        const bool desc = (p & k) == 0;
+                        const T a = x[r], b = x[r | j];
+                        const T mx = a > b ? a : b;
+                        const T mn = a > b ? b : a;
+                        x[r] = desc ? mx : mn;
+                        x[r | j] = desc ? mn : mx;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Bitonic sort, descending, of the 16 values a group of 4 lanes holds: lane
+// q keeps positions 4q .. 4q + 3 in x[0..3].
+template <typename T>
+__device__ __forceinline__ void group_sort16_desc(T (&x)[4], int q) {
+#pragma unroll
+    for (int k = 2; k <= 16; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= 4) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const T y = shfl_xor_any(x[r], j >> 2);
+                    const int p = q * 4 + r;
+                    const bool keep_max = ((p & j) == 0) == ((p & k) == 0);
+                    const T mx = x[r] > y ? x[r] : y;
+                    const T mn = x[r] > y ? y : x[r];
+                    x[r] = keep_max ? mx : mn;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if ((r & j) == 0) {
+                        const int p = q * 4 + r;
+                        const bool desc = (p & k) == 0;
+                        const T a = x[r], b = x[r | j];
+                        const T mx = a > b ? a : b;
+                        const T mn = a > b ? b : a;
+                        x[r] = desc ? mx : mn;
+                        x[r | j] = desc ? mn : mx;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// x[idx] for a register array and a runtime index (a chain of selects).
+template <typename T, int N>
+__device__ __forceinline__ T pick(const T (&x)[N], int idx) {
+    T v = x[0];
+#pragma unroll
+    for (int r = 1; r < N; ++r) v = idx == r ? x[r] : v;
+    return v;
 }
 
 __device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,
@@ -676,60 +802,69 @@ __device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,
     return r.hi + (j - r.lo - r.kp);
 }
 
-// Outputs of one row by its 4 lanes.  Every lane of the warp calls this
-// (the ctx sum shuffles within each group); `write` masks the stores.
+// Outputs of one row by its 4 lanes: lane q owns the output slots (= blocks)
+// j = q, q + 4, ...: it writes their ids, their 8 table entries (two 16-byte
+// stores) and their part of ctx.  Every lane of the warp calls this (ctx is
+// summed with shuffles inside each group); `write` masks the stores.
 __device__ void group_write_outputs(const KernelParams& P, int64_t row, const RowInfo& r,
                                     bool all, const int32_t* sorted, int q, bool write) {
     const SelectArgs& a = P.a;
     const int K = a.K;
-    if (write && a.out_idx != nullptr) {
-        int32_t* out = a.out_idx + row * K;
-        for (int s = q; s < K; s += kGroupLanes)
-            out[s] = s < r.n ? group_sel(s, r, all, sorted) : -1;
-    }
-    if (!a.fused) return;
     int ctx = 0;
     if (write) {
+        int32_t* out = a.out_idx != nullptr ? a.out_idx + row * K : nullptr;
         const int width = K * kPagesPerBlock;
-        int32_t* bt = a.sparse_bt + row * (int64_t)width;
-        const int32_t* table = a.block_table + r.req * a.max_blocks;
+        int32_t* bt = a.fused ? a.sparse_bt + row * (int64_t)width : nullptr;
+        const int32_t* table = a.fused ? a.block_table + r.req * a.max_blocks : nullptr;
         const bool vec_ok = ((reinterpret_cast<uintptr_t>(bt)) & 15) == 0;
-        // chunk c holds entries [4c, 4c + 4): one block j = c / 2, pages 4 (c & 1) + 0..3
-        for (int c = q; c * 4 < width; c += kGroupLanes) {
-            const int j = c >> 1;
-            const int pg0 = (c & 1) * 4;
-            int v[4] = {0, 0, 0, 0};
-            if (j < r.n) {
-                const int32_t b = group_sel(j, r, all, sorted);
-                const int64_t tok0 = (int64_t)b * kPageSize + (int64_t)pg0 * kSubPage;
-                if (b < a.max_blocks && tok0 < r.causal_len) {
-                    const int32_t phys8 = __ldg(table + b) * kPagesPerBlock + pg0;
+        // 4 slots per lane at a time: ids first, then all table gathers in
+        // flight together, then the stores
+        for (int j0 = q; j0 < K; j0 += 4 * kGroupLanes) {
+            int32_t bs[4], phys[4] = {0, 0, 0, 0};
+            bool okb[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        v[u] = tok0 + (int64_t)u * kSubPage < r.causal_len ? phys8 + u : 0;
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * kGroupLanes;
+                bs[u] = (j < K && j < r.n) ? group_sel(j, r, all, sorted) : -1;
+                okb[u] = bt != nullptr && bs[u] >= 0 && bs[u] < a.max_blocks;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (okb[u]) phys[u] = __ldg(table + bs[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * kGroupLanes;
+                if (j >= K) break;
+                if (out != nullptr) out[j] = bs[u];
+                if (bt == nullptr) continue;
+                int v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if (okb[u]) {
+                    // tokens of this block inside the causal prefix (b < v <= pages, so >= 1)
+                    const int rem = (int)min(r.causal_len - (int64_t)bs[u] * kPageSize,
+                                             (int64_t)kPageSize);
+                    const int32_t phys8 = phys[u] * kPagesPerBlock;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = e * kSubPage < rem ? phys8 + e : 0;
+                    ctx += rem;
                 }
-            }
-            if (vec_ok) {
-                *reinterpret_cast<int4*>(bt + 4 * c) = make_int4(v[0], v[1], v[2], v[3]);
-            } else {
+                int32_t* dst = bt + 8 * j;
+                if (vec_ok) {
+                    reinterpret_cast<int4*>(dst)[0] = make_int4(v[0], v[1], v[2], v[3]);
+                    reinterpret_cast<int4*>(dst)[1] = make_int4(v[4], v[5], v[6], v[7]);
+                } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) bt[4 * c + u] = v[u];
-            }
-        }
-        for (int j = q; j < r.n; j += kGroupLanes) {
-            const int32_t b = group_sel(j, r, all, sorted);
-            if (b < a.max_blocks) {
-                const int64_t rem = r.causal_len - (int64_t)b * kPageSize;
-                ctx += (int)(rem < kPageSize ? rem : kPageSize);
+                    for (int e = 0; e < 8; ++e) dst[e] = v[e];
+                }
             }
         }
     }
+    if (!a.fused) return;
     ctx += __shfl_xor_sync(kFull, ctx, 1);
     ctx += __shfl_xor_sync(kFull, ctx, 2);
     if (write && q == 0) a.sparse_ctx[row] = ctx;
 }
 
-template <bool BF16, int R>
+template <bool BF16, int R, bool SMALLK>
 __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelParams P) {
     using E = Elem<BF16>;
     using CK = typename std::conditional<BF16, uint32_t, unsigned long long>::type;
@@ -738,8 +873,7 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
     constexpr int S = E::kBytes;
     constexpr int H2 = R / 2;  // representative pairs per lane (divides 4)
     static_assert(R == 2 || R == 4 || R == 8, "R must be 2, 4 or 8");
-    constexpr int kTop = BF16 ? 14 : 30;
-    constexpr int kLow = BF16 ? 3 : 19;
+    static_assert(kGroupCand == 32, "the candidate sort holds 32 values");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -747,62 +881,95 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
     const int q = lane & 3;
     G& sm = *reinterpret_cast<G*>(smem_raw + (size_t)warp * sizeof(G));
     const SelectArgs& a = P.a;
-    const unsigned lt = lanemask_lt();
     const int64_t ngroups = (P.rows + kGroupRows - 1) / kGroupRows;
     const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
 
-    for (int64_t wg = (int64_t)blockIdx.x * kWarpsPerCta + warp; wg < ngroups; wg += stride) {
+    int64_t wg = (int64_t)blockIdx.x * kWarpsPerCta + warp;
+    int32_t meta = 0;
+    if (wg < ngroups && wg * kGroupRows + g < P.rows) meta = row_meta(a, wg * kGroupRows + g);
+    for (; wg < ngroups; wg += stride) {
         const int64_t row = wg * kGroupRows + g;
         const bool active = row < P.rows;
+        // metadata of the next item, loaded now and used after pass 1
+        const int64_t nrow = (wg + stride) * kGroupRows + g;
+        const bool nactive = wg + stride < ngroups && nrow < P.rows;
+        const int32_t nmeta = nactive ? row_meta(a, nrow) : 0;
         RowInfo r{};
         r.all = true;
-        if (active) r = row_info(a, row);
+        if (active) r = row_info_from(a, row, meta);
+        meta = nmeta;
         const bool need = active && r.need;
 
         // ---- geometry of the non-forced range [lo, hi) ----
         const char* row_ptr = nullptr;
-        uintptr_t a_lo = 0, a_hi = 0, v0 = 0;
+        uintptr_t v0 = 0;
         int nvec = 0, base_id = 0;
         if (need) {
             row_ptr = reinterpret_cast<const char*>(a.scores) +
                       (r.t * a.token_stride + r.h * a.head_stride) * S;
-            a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * S;
-            a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * S;
+            const uintptr_t a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * S;
+            const uintptr_t a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * S;
             v0 = a_lo & ~(uintptr_t)15;
             nvec = (int)((a_hi - v0 + 15) >> 4);
             base_id = r.lo - (int)((a_lo - v0) / S);
         }
-        const int my_steps = need ? (nvec - q + kGroupLanes - 1) / kGroupLanes : 0;
 
         // ---- pass 1: vector maxima and representatives ----
+        // Step 0 holds vectors 0..3 (the first one is an edge), the interior
+        // vectors 4 .. nvec-2 need no masking, the last one is an edge.
         int32_t rep[R];
 #pragma unroll
         for (int x = 0; x < R; ++x) rep[x] = INT32_MIN;
-        for (int i0 = 0; i0 < my_steps; i0 += 4) {
+        auto take = [&](const uint4& w, int k, int slot) {
+            int32_t x0, x1;
+            vec_max_pair<BF16>(w, x0, x1);
+            const int32_t m = max(x0, x1);
+            sm.vmax[g][q][(k - q) >> 2] = (int16_t)(BF16 ? m : (m >> 16));
+            rep[(slot % H2) * 2] = max(rep[(slot % H2) * 2], x0);
+            rep[(slot % H2) * 2 + 1] = max(rep[(slot % H2) * 2 + 1], x1);
+        };
+        if (need && q < nvec) {
+            take(group_load_edge<BF16>(P, q, v0, base_id, r.lo, r.hi, row_ptr), q, 0);
+        }
+        // interior vectors k = q + 4 i, i >= 1, k <= nvec - 2
+        const int n_int = need ? max(0, (nvec - 2 - q) / kGroupLanes) : 0;
+        for (int i0 = 1; i0 <= n_int; i0 += 4) {
             uint4 w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int i = i0 + u;
-                w[u] = i < my_steps ? group_load<BF16>(q + kGroupLanes * i, v0, a_lo, a_hi,
-                                                       base_id, r.lo, r.hi, row_ptr)
-                                    : make_uint4(E::kMaskWord, E::kMaskWord, E::kMaskWord,
-                                                 E::kMaskWord);
+                const uintptr_t addr = v0 + ((uintptr_t)(q + kGroupLanes * i) << 4);
+                if (i <= n_int) w[u] = __ldg(reinterpret_cast<const uint4*>(addr));
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int i = i0 + u;
-                if (i < my_steps) {
-                    int32_t x0, x1;
-                    vec_max_pair<BF16>(w[u], x0, x1);
-                    const int32_t m = max(x0, x1);
-                    sm.vmax[g][q + kGroupLanes * i] = (int16_t)(BF16 ? m : (m >> 16));
-                    rep[(u % H2) * 2] = max(rep[(u % H2) * 2], x0);
-                    rep[(u % H2) * 2 + 1] = max(rep[(u % H2) * 2 + 1], x1);
-                }
+                if (i <= n_int) take(w[u], q + kGroupLanes * i, u + 1);
+            }
+        }
+        if (need && nvec > kGroupLanes && (nvec - 1) % kGroupLanes == q) {
+            take(group_load_edge<BF16>(P, nvec - 1, v0, base_id, r.lo, r.hi, row_ptr), nvec - 1,
+                 3);
+        }
+        // the rows of this warp's next item start streaming into L2 while
+        // this item is being selected
+        if (q == 0 && nactive) {
+            const RowInfo nr = row_info_from(a, nrow, nmeta);
+            if (nr.need) {
+                const uintptr_t nrp = reinterpret_cast<uintptr_t>(a.scores) +
+                                      (uintptr_t)((nr.t * a.token_stride + nr.h * a.head_stride) * S);
+                const uintptr_t nlo = (nrp + (uintptr_t)nr.lo * S) & ~(uintptr_t)15;
+                uintptr_t nhi = (nrp + (uintptr_t)nr.hi * S + 15) & ~(uintptr_t)15;
+                if (nhi > P.buf_hi) nhi = P.buf_hi & ~(uintptr_t)15;
+                if (nlo >= P.buf_lo && nhi > nlo) prefetch_l2(nlo, (uint32_t)(nhi - nlo));
             }
         }
 
-        // ---- theta: K'-th largest representative of the row ----
+        // ---- theta: the K'-th largest representative of the row ----
+        // 12-bit search from the top (bf16: 1/16-binade resolution; fp32 uses
+        // its top 12 bits); the bits left at zero only lower theta
+        constexpr int kTop = BF16 ? 14 : 30;
+        constexpr int kLow = BF16 ? 3 : 19;
         int c0 = 0;
 #pragma unroll
         for (int x = 0; x < R; ++x) c0 += rep[x] >= 0 ? 1 : 0;
@@ -822,7 +989,6 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
         const bool ovf0 = need && !fast && (r.hi - r.lo) > kGroupCand;
         if (q == 0) {
             sm.ccount[g] = 0;
-            sm.scount[g] = 0;
             sm.ovf[g] = ovf0 ? 1 : 0;
             GroupRowDesc d;
             d.v0 = v0;
@@ -832,23 +998,34 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
             d.hi = r.hi;
             d.theta = theta;
             d.fast = fast ? 1 : 0;
-            d.pad = 0;
+            d.nvec = nvec;
             sm.desc[g] = d;
         }
         const int32_t th16 = BF16 ? theta : (theta >> 16);
-        __syncwarp();
 
         // ---- queue the vectors that can hold candidates ----
-        const int qsteps_lane = (need && !ovf0) ? my_steps : 0;
-        const int qsteps = __reduce_max_sync(kFull, qsteps_lane);
-        int qn = 0;
-        for (int i = 0; i < qsteps; ++i) {
-            const int k = q + kGroupLanes * i;
-            const bool hot = i < qsteps_lane && (!fast || sm.vmax[g][k] >= th16);
-            const unsigned b = __ballot_sync(kFull, hot);
-            if (hot) sm.q.queue[qn + __popc(b & lt)] = (uint16_t)((g << 13) | k);
-            qn += __popc(b);
+        // Each lane marks its hot vectors in a bitmask (8 maxima per 16-byte
+        // shared load), the warp scans the counts, and every lane writes its
+        // entries contiguously: the queue's order does not matter.
+        const int my_steps = (need && !ovf0) ? (nvec - q + kGroupLanes - 1) / kGroupLanes : 0;
+        unsigned long long hot = 0;
+        for (int i0 = 0; i0 < my_steps; i0 += 8) {
+            const uint4 pk = *reinterpret_cast<const uint4*>(&sm.vmax[g][q][i0]);
+            const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int32_t vm = (int32_t)(int16_t)(uint16_t)(wv[u >> 1] >> ((u & 1) * 16));
+                if (i0 + u < my_steps && (!fast || vm >= th16)) hot |= 1ull << (i0 + u);
+            }
         }
+        int qtotal;
+        int qpos = warp_excl_scan(__popcll(hot), lane, qtotal);
+        while (hot) {
+            const int i = __ffsll((long long)hot) - 1;
+            hot &= hot - 1;
+            sm.q.queue[qpos++] = (uint16_t)((g << 13) | (q + kGroupLanes * i));
+        }
+        const int qn = qtotal;
         __syncwarp();
 
         // ---- candidates from the queued vectors, 32 at a time ----
@@ -859,11 +1036,12 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
                 const int gg = ent >> 13;
                 const int k = ent & 0x1FFF;
                 const GroupRowDesc d = sm.desc[gg];
-                const char* rp = reinterpret_cast<const char*>(d.row_ptr);
-                const uintptr_t lo_addr = (uintptr_t)d.row_ptr + (uintptr_t)d.lo * S;
-                const uintptr_t hi_addr = (uintptr_t)d.row_ptr + (uintptr_t)d.hi * S;
-                const uint4 w = group_load<BF16>(k, (uintptr_t)d.v0, lo_addr, hi_addr, d.base_id,
-                                                 d.lo, d.hi, rp);
+                uint4 w;
+                if (k == 0 || k == d.nvec - 1)
+                    w = group_load_edge<BF16>(P, k, (uintptr_t)d.v0, d.base_id, d.lo, d.hi,
+                                              reinterpret_cast<const char*>(d.row_ptr));
+                else
+                    w = __ldg(reinterpret_cast<const uint4*>((uintptr_t)d.v0 + ((uintptr_t)k << 4)));
                 const int first_id = d.base_id + k * VEC;
                 unsigned m = 0;
                 if (d.fast) {
@@ -894,28 +1072,51 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
         }
         __syncwarp();
 
-        // ---- exact select: rank of each candidate among the row's ----
+        // ---- exact select: sort the row's candidates, keep the first K' ----
         const bool ovf = sm.ovf[g] != 0;
-        const int cn = sm.ccount[g];
+        const int cn = min(sm.ccount[g], kGroupCand);
         const bool sel_ok = need && !ovf;
-        if (sel_ok) {
-            for (int j = q; j < cn; j += kGroupLanes) {
-                const CK ck = sm.cand[g][j];
-                int rank = 0;
-                for (int m2 = 0; m2 < cn; ++m2) rank += sm.cand[g][m2] > ck ? 1 : 0;
-                if (rank < r.kp) {
-                    const int p = atomicAdd(&sm.scount[g], 1);
-                    sm.q.s.sel[g][p] = ck_id(ck);
+        CK x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int pos = q * 8 + u;
+            x[u] = (sel_ok && pos < cn) ? sm.cand[g][pos] : (CK)0;
+        }
+        group_sort32_desc<CK>(x, q);
+        // keep positions < K'; re-sort the kept ids ascending (descending low field)
+        constexpr uint32_t kLowMax = BF16 ? 0xFFFFu : 0xFFFFFFFFu;
+        if (SMALLK) {
+            // K' <= 16: positions 0..15 live in lanes 0 and 1; lane q takes 4q .. 4q+3
+            uint32_t y[4];
+            const int src = (g << 2) | (q >> 1);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                // position 4q + u is register 4 (q & 1) + u of lane q >> 1
+                const uint32_t got0 = __shfl_sync(kFull, ck_low(x[u]), src);
+                const uint32_t got1 = __shfl_sync(kFull, ck_low(x[u + 4]), src);
+                y[u] = (q * 4 + u < r.kp) ? ((q & 1) ? got1 : got0) : 0u;
+            }
+            group_sort16_desc<uint32_t>(y, q);
+            __syncwarp();
+            if (sel_ok) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int pos = q * 4 + u;
+                    if (pos < r.kp) sm.q.s.sorted[g][pos] = (int32_t)(kLowMax - y[u]);
                 }
             }
-        }
-        __syncwarp();
-        if (sel_ok) {
-            for (int p = q; p < r.kp; p += kGroupLanes) {
-                const int32_t x = sm.q.s.sel[g][p];
-                int rk = 0;
-                for (int p2 = 0; p2 < r.kp; ++p2) rk += sm.q.s.sel[g][p2] < x ? 1 : 0;
-                sm.q.s.sorted[g][rk] = x;
+        } else {
+            uint32_t y[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) y[u] = (q * 8 + u < r.kp) ? ck_low(x[u]) : 0u;
+            group_sort32_desc<uint32_t>(y, q);
+            __syncwarp();
+            if (sel_ok) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int pos = q * 8 + u;
+                    if (pos < r.kp) sm.q.s.sorted[g][pos] = (int32_t)(kLowMax - y[u]);
+                }
             }
         }
         __syncwarp();
@@ -942,7 +1143,9 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
 template <bool BF16, int R>
 cudaError_t launch_group_t(const KernelParams& P, const bsa_launch_policy_t& pol,
                            cudaStream_t st) {
-    auto kern = group_select_kernel<BF16, R>;
+    // K' <= K - num_init - num_local: a 16-entry id sort suffices for K' <= 16
+    const bool small = P.a.K - P.a.num_init - P.a.num_local <= 16;
+    auto kern = small ? group_select_kernel<BF16, R, true> : group_select_kernel<BF16, R, false>;
     if (pol.smem_bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              pol.smem_bytes);
@@ -955,11 +1158,7 @@ cudaError_t launch_group_t(const KernelParams& P, const bsa_launch_policy_t& pol
 template <bool BF16>
 cudaError_t launch_group(const KernelParams& P, const bsa_launch_policy_t& pol,
                          cudaStream_t st) {
-    switch (pol.reps_per_lane) {
-        case 2: return launch_group_t<BF16, 2>(P, pol, st);
-        case 4: return launch_group_t<BF16, 4>(P, pol, st);
-        default: return launch_group_t<BF16, 8>(P, pol, st);
-    }
+    return launch_group_t<BF16, 8>(P, pol, st);
 }
 
 template <bool BF16, int NV, int R>
@@ -1003,6 +1202,10 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
     P.cap = pol.cand_capacity;
     P.rows = a.T * a.H;
     const int vec = a.dtype == BSA_DTYPE_BF16 ? 8 : 4;
+    const int64_t esz = a.dtype == BSA_DTYPE_BF16 ? 2 : 4;
+    P.buf_lo = reinterpret_cast<uintptr_t>(a.scores);
+    P.buf_hi = P.buf_lo + (uintptr_t)(((a.T > 0 ? a.T - 1 : 0) * a.token_stride +
+                                        (a.H > 0 ? a.H - 1 : 0) * a.head_stride + a.M) * esz);
     const int64_t max_vecs = (a.M + vec - 1) / vec + 1;
     int64_t vpc = (max_vecs + pol.chunks_per_row - 1) / pol.chunks_per_row;
     const int64_t pass = 32LL * pol.vecs_per_lane;

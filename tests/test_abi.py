@@ -88,7 +88,7 @@ def test_policy_production_capacity(bsa):
             assert p["path"] == bsa.BSA_PATH_ROW and p["vecs_per_lane"] == 1
 
 
-@pytest.mark.parametrize("K,reps", [(1, 4), (16, 4), (17, 8), (32, 8)])
+@pytest.mark.parametrize("K,reps", [(1, 8), (16, 8), (17, 8), (32, 8)])
 def test_policy_representatives_group(bsa, K, reps):
     assert _policy(bsa, 1000, 1024, K, BF)["reps_per_lane"] == reps
 
