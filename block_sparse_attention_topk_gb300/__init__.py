@@ -25,6 +25,7 @@ BSA_DTYPE_FP32 = 1
 BSA_PATH_ROW = 0
 BSA_PATH_SPLIT = 1
 BSA_PATH_GROUP = 2
+BSA_PATH_PAIR = 3
 PAGE_SIZE = 128
 PAGES_PER_SPARSE_BLOCK = 8
 MAX_TOPK = 1024

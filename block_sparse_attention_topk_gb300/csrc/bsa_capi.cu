@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <climits>
 #include <mutex>
@@ -72,6 +73,20 @@ int check_topk_args(int64_t M, int32_t K, int32_t num_init, int32_t num_local) {
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? BSA_OK : (int)e; }
 
+// BSA_SELECT_PATH=row|group|pair overrides the policy's choice among the
+// paths that can serve a call (for benchmarking); -1 when unset.
+int forced_path() {
+    static const int v = [] {
+        const char* e = getenv("BSA_SELECT_PATH");
+        if (e == nullptr) return -1;
+        if (strcmp(e, "row") == 0) return BSA_PATH_ROW;
+        if (strcmp(e, "group") == 0) return BSA_PATH_GROUP;
+        if (strcmp(e, "pair") == 0) return BSA_PATH_PAIR;
+        return -1;
+    }();
+    return v;
+}
+
 // The launch policy (see bsa_select_policy in the header).
 int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
                 bsa_launch_policy_t* p) {
@@ -98,10 +113,34 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
     int warps = 8;
     const int cap = (int)((K + 32 * vec + 31) / 32 * 32);
     int smem = warps * cap * 8;
-    // Group path (4 lanes per row, 8 rows per warp) for topk <= 32 and rows
-    // of at most 2 KB; its overflow fallback is the warp path with one pass.
+    // Pair path (2 lanes per row, 16 rows per warp) for topk <= 32 and rows
+    // of at most 2 KB; the group path (4 lanes per row) is kept selectable for
+    // comparison.  Both fall back to the warp path for overflowing rows.
     const int elem = dtype == BSA_DTYPE_BF16 ? 2 : 4;
-    if (K <= kGroupMaxK && M * elem <= kGroupMaxBytes) {
+    const int forced = forced_path();
+    if (K <= kGroupMaxK && M * elem <= kGroupMaxBytes && forced != BSA_PATH_ROW &&
+        forced != BSA_PATH_GROUP) {
+        const int gsmem = kPairWarps * (int)(dtype == BSA_DTYPE_BF16
+                                                 ? sizeof(PairSmem<uint32_t>)
+                                                 : sizeof(PairSmem<unsigned long long>));
+        int ctas = 5;  // the kernel's register bound: 5 CTAs of 4 warps per SM
+        while (ctas > 1 && ctas * (gsmem + 1024) > 228 * 1024) --ctas;
+        const int64_t items = (rows + kPairRows - 1) / kPairRows;
+        int64_t grid = (items + kPairWarps - 1) / kPairWarps;
+        const int64_t grid_cap = (int64_t)num_sms * ctas;
+        if (grid > grid_cap) grid = grid_cap;
+        if (grid < 1) grid = 1;
+        p->path = BSA_PATH_PAIR;
+        p->vecs_per_lane = 4;
+        p->chunks_per_row = 1;
+        p->reps_per_lane = 16;
+        p->warps_per_cta = kPairWarps;
+        p->grid = (int32_t)grid;
+        p->cand_capacity = cap;
+        p->smem_bytes = gsmem;
+        return BSA_OK;
+    }
+    if (K <= kGroupMaxK && M * elem <= kGroupMaxBytes && forced != BSA_PATH_ROW) {
         const int gsmem = warps * (int)(dtype == BSA_DTYPE_BF16
                                             ? sizeof(GroupSmem<uint32_t>)
                                             : sizeof(GroupSmem<unsigned long long>));

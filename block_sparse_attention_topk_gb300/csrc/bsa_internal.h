@@ -50,6 +50,36 @@ struct GroupSmem {
     GroupRowDesc desc[kGroupRows];
 };
 
+// Pair path: 2 lanes per row, 16 rows per warp, 32-byte chunks (see bsa_select.cu).
+constexpr int kPairRows = 16;        // rows per warp
+constexpr int kPairMaxChunks = 66;   // 32-byte chunks per row (2 KB + alignment)
+constexpr int kPairStepsPad = 40;    // >= ceil(kPairMaxChunks / 2), multiple of 8
+constexpr int kPairCand = 32;        // candidate capacity per row (one 2-lane sort)
+constexpr int kPairWarps = 4;        // warps per CTA
+
+struct PairRowDesc {
+    unsigned long long c0;       // first 32-byte chunk of the non-forced range
+    unsigned long long row_ptr;  // address of element 0 of the row
+    int32_t base_id, lo, hi, theta;
+    int32_t fast, nchunk;
+};
+
+template <typename CK>
+struct PairSmem {
+    // chunk maxima (raw signed; fp32 keeps the top 16 bits), lane-major:
+    // chunk k = s + 2 i of row p at vmax[p][s][i]
+    int16_t vmax[kPairRows][2][kPairStepsPad];
+    union {
+        uint16_t queue[kPairRows * kPairMaxChunks];  // (row << 8 | chunk) work items
+        int32_t sorted[kPairRows][kGroupMaxK];      // selected ids, ascending
+    } q;
+    CK cand[kPairRows][kPairCand];                  // candidate composite keys
+    uint32_t scratch[32][8];                        // one 32-byte chunk per lane
+    int32_t ccount[kPairRows];
+    int32_t ovf[kPairRows];
+    PairRowDesc desc[kPairRows];
+};
+
 // Everything one selector launch needs.  Pointers are device pointers.
 struct SelectArgs {
     const void* scores;

@@ -68,6 +68,12 @@ __device__ __forceinline__ uint32_t max_s16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -802,10 +808,12 @@ __device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,
     return r.hi + (j - r.lo - r.kp);
 }
 
-// Outputs of one row by its 4 lanes: lane q owns the output slots (= blocks)
-// j = q, q + 4, ...: it writes their ids, their 8 table entries (two 16-byte
-// stores) and their part of ctx.  Every lane of the warp calls this (ctx is
-// summed with shuffles inside each group); `write` masks the stores.
+// Outputs of one row by its LANES lanes: lane q owns a contiguous run of
+// output slots (= blocks): it writes their ids, their 8 table entries each
+// (two 16-byte stores) and their part of ctx.  Every lane of the warp calls
+// this (ctx is summed with shuffles inside each row's lanes); `write` masks
+// the stores.
+template <int LANES>
 __device__ void group_write_outputs(const KernelParams& P, int64_t row, const RowInfo& r,
                                     bool all, const int32_t* sorted, int q, bool write) {
     const SelectArgs& a = P.a;
@@ -817,26 +825,42 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
         int32_t* bt = a.fused ? a.sparse_bt + row * (int64_t)width : nullptr;
         const int32_t* table = a.fused ? a.block_table + r.req * a.max_blocks : nullptr;
         const bool vec_ok = ((reinterpret_cast<uintptr_t>(bt)) & 15) == 0;
-        // 4 slots per lane at a time: ids first, then all table gathers in
-        // flight together, then the stores
-        for (int j0 = q; j0 < K; j0 += 4 * kGroupLanes) {
-            int32_t bs[4], phys[4] = {0, 0, 0, 0};
-            bool okb[4];
+        // lane q owns the contiguous slots [q * per, q * per + per); 8 at a
+        // time: ids first, then all table gathers in flight together, then
+        // the stores
+        const int per = (K + LANES - 1) / LANES;
+        const int jbeg = q * per;
+        const int jend = min(K, jbeg + per);
+        for (int j0 = jbeg; j0 < jend; j0 += 8) {
+            int32_t bs[8], phys[8];
+            bool okb[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = j0 + u * kGroupLanes;
-                bs[u] = (j < K && j < r.n) ? group_sel(j, r, all, sorted) : -1;
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u;
+                bs[u] = (j < jend && j < r.n) ? group_sel(j, r, all, sorted) : -1;
                 okb[u] = bt != nullptr && bs[u] >= 0 && bs[u] < a.max_blocks;
+                phys[u] = 0;
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
                 if (okb[u]) phys[u] = __ldg(table + bs[u]);
+            if (out != nullptr) {
+                const bool ovec = j0 + 8 <= jend &&
+                                  ((reinterpret_cast<uintptr_t>(out + j0)) & 15) == 0;
+                if (ovec) {
+                    reinterpret_cast<int4*>(out + j0)[0] = make_int4(bs[0], bs[1], bs[2], bs[3]);
+                    reinterpret_cast<int4*>(out + j0)[1] = make_int4(bs[4], bs[5], bs[6], bs[7]);
+                } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = j0 + u * kGroupLanes;
-                if (j >= K) break;
-                if (out != nullptr) out[j] = bs[u];
-                if (bt == nullptr) continue;
+                    for (int u = 0; u < 8; ++u)
+                        if (j0 + u < jend) out[j0 + u] = bs[u];
+                }
+            }
+            if (bt == nullptr) continue;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u;
+                if (j >= jend) break;
                 int v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                 if (okb[u]) {
                     // tokens of this block inside the causal prefix (b < v <= pages, so >= 1)
@@ -859,8 +883,8 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
         }
     }
     if (!a.fused) return;
-    ctx += __shfl_xor_sync(kFull, ctx, 1);
-    ctx += __shfl_xor_sync(kFull, ctx, 2);
+#pragma unroll
+    for (int m = 1; m < LANES; m <<= 1) ctx += __shfl_xor_sync(kFull, ctx, m);
     if (write && q == 0) a.sparse_ctx[row] = ctx;
 }
 
@@ -1122,7 +1146,8 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
         __syncwarp();
 
         // ---- outputs ----
-        group_write_outputs(P, row, r, r.all, sm.q.s.sorted[g], q, active && (!need || !ovf));
+        group_write_outputs<kGroupLanes>(P, row, r, r.all, sm.q.s.sorted[g], q,
+                                         active && (!need || !ovf));
 
         // ---- rows whose candidates overflowed: the whole warp redoes them ----
         unsigned fb = __ballot_sync(kFull, q == 0 && need && ovf);
@@ -1138,6 +1163,461 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
         }
         __syncwarp();
     }
+}
+
+
+// ===========================================================================
+// Pair path: 2 lanes per row, 16 rows per warp.
+//
+// Same algorithm as the group path with half the lanes per row, so that the
+// fixed per-row steps (threshold search, sorts, outputs) cover 16 rows per
+// warp instruction, and with 32-byte chunks (one 256-bit load per lane, a
+// row's pair reads 64 contiguous bytes per instruction).  Representatives
+// stay packed: bf16 keeps 16 per lane in 8 registers updated with max.s16x2.
+// ===========================================================================
+
+__device__ __forceinline__ void ld32(uintptr_t addr, uint32_t (&w)[8]) {
+    asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+          "=r"(w[7])
+        : "l"(addr));
+}
+
+template <bool BF16>
+__device__ __forceinline__ int32_t chunk_raw(const uint32_t (&w)[8], int e) {
+    if constexpr (BF16) return (int32_t)(int16_t)(uint16_t)(w[e >> 1] >> ((e & 1) * 16));
+    else return (int32_t)w[e];
+}
+
+template <bool BF16>
+__device__ __forceinline__ void chunk_set(uint32_t (&w)[8], int e, int32_t raw) {
+    if constexpr (BF16) {
+        const int sh = (e & 1) * 16;
+        w[e >> 1] = (w[e >> 1] & ~(0xFFFFu << sh)) | (((uint32_t)raw & 0xFFFFu) << sh);
+    } else {
+        w[e] = (uint32_t)raw;
+    }
+}
+
+// Chunk k of a row's non-forced range, with ids outside [lo, hi) masked.
+template <bool BF16>
+__device__ __forceinline__ void pair_load_edge(const KernelParams& P, int k, uintptr_t c0,
+                                               int base_id, int lo, int hi,
+                                               const char* row_ptr, uint32_t (&w)[8]) {
+    using E = Elem<BF16>;
+    constexpr int S = E::kBytes;
+    constexpr int CE = 32 / S;
+    const uintptr_t addr = c0 + ((uintptr_t)k << 5);
+    if (addr >= P.buf_lo && addr + 32 <= P.buf_hi) {
+        ld32(addr, w);
+#pragma unroll
+        for (int e = 0; e < CE; ++e) {
+            const int id = base_id + k * CE + e;
+            if (id < lo || id >= hi) chunk_set<BF16>(w, e, (int32_t)E::kMaskWord);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = E::kMaskWord;
+#pragma unroll
+        for (int e = 0; e < CE; ++e) {
+            const int id = base_id + k * CE + e;
+            if (id >= lo && id < hi) chunk_set<BF16>(w, e, E::load_one(row_ptr + (int64_t)id * S));
+        }
+    }
+}
+
+// Bitonic sort, descending, of the 32 values a lane pair holds: lane s keeps
+// positions 16 s .. 16 s + 15 in x[0..15].  Every lane of the warp calls it.
+template <typename T>
+__device__ __forceinline__ void pair_sort32_desc(T (&x)[16], int s) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j == 16) {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const T y = shfl_xor_any(x[r], 1);
+                    const T mx = x[r] > y ? x[r] : y;
+                    const T mn = x[r] > y ? y : x[r];
+                    x[r] = s == 0 ? mx : mn;  // k == 32: descending, lane 0 is the upper half
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    if ((r & j) == 0) {
+                        const bool desc = k < 16 ? ((r & k) == 0) : (k == 32 || s == 0);
+                        const T a = x[r], b = x[r | j];
+                        const T mx = a > b ? a : b;
+                        const T mn = a > b ? b : a;
+                        x[r] = desc ? mx : mn;
+                        x[r | j] = desc ? mn : mx;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Bitonic sort, descending, of 16 values in one lane's registers.
+template <typename T>
+__device__ __forceinline__ void lane_sort16_desc(T (&x)[16]) {
+#pragma unroll
+    for (int k = 2; k <= 16; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                if ((r & j) == 0) {
+                    const bool desc = (r & k) == 0 || k == 16;
+                    const T a = x[r], b = x[r | j];
+                    const T mx = a > b ? a : b;
+                    const T mn = a > b ? b : a;
+                    x[r] = desc ? mx : mn;
+                    x[r | j] = desc ? mn : mx;
+                }
+            }
+        }
+    }
+}
+
+template <bool BF16, bool SMALLK>
+__global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const KernelParams P) {
+    using E = Elem<BF16>;
+    using CK = typename std::conditional<BF16, uint32_t, unsigned long long>::type;
+    using G = PairSmem<CK>;
+    constexpr int S = E::kBytes;
+    constexpr int CE = 32 / S;                 // elements per 32-byte chunk
+    constexpr int kTop = BF16 ? 14 : 30;
+    constexpr int kLow = BF16 ? 3 : 19;
+    constexpr uint32_t kLowMax = BF16 ? 0xFFFFu : 0xFFFFFFFFu;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int p = lane >> 1;   // row of the warp's item
+    const int s = lane & 1;    // lane within the row's pair
+    G& sm = *reinterpret_cast<G*>(smem_raw + (size_t)warp * sizeof(G));
+    const SelectArgs& a = P.a;
+    const int64_t nitems = (P.rows + kPairRows - 1) / kPairRows;
+    const int64_t stride = (int64_t)gridDim.x * kPairWarps;
+
+    int64_t it = (int64_t)blockIdx.x * kPairWarps + warp;
+    int32_t meta = 0;
+    if (it < nitems && it * kPairRows + p < P.rows) meta = row_meta(a, it * kPairRows + p);
+    for (; it < nitems; it += stride) {
+        const int64_t row = it * kPairRows + p;
+        const bool active = row < P.rows;
+        const int64_t nrow = (it + stride) * kPairRows + p;
+        const bool nactive = it + stride < nitems && nrow < P.rows;
+        const int32_t nmeta = nactive ? row_meta(a, nrow) : 0;
+        RowInfo r{};
+        r.all = true;
+        if (active) r = row_info_from(a, row, meta);
+        meta = nmeta;
+        const bool need = active && r.need;
+
+        // ---- geometry of the non-forced range [lo, hi), 32-byte chunks ----
+        const char* row_ptr = nullptr;
+        uintptr_t c0 = 0;
+        int nchunk = 0, base_id = 0;
+        if (need) {
+            row_ptr = reinterpret_cast<const char*>(a.scores) +
+                      (r.t * a.token_stride + r.h * a.head_stride) * S;
+            const uintptr_t a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * S;
+            const uintptr_t a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * S;
+            c0 = a_lo & ~(uintptr_t)31;
+            nchunk = (int)((a_hi - c0 + 31) >> 5);
+            base_id = r.lo - (int)((a_lo - c0) / S);
+            // one bulk request brings the whole range towards L2 while the
+            // lanes' own loads walk it in batches
+            if (s == 0) {
+                const uintptr_t plo = c0 < P.buf_lo ? (P.buf_lo + 15) & ~(uintptr_t)15 : c0;
+                uintptr_t phi = c0 + ((uintptr_t)nchunk << 5);
+                if (phi > P.buf_hi) phi = P.buf_hi & ~(uintptr_t)15;
+                if (phi > plo) prefetch_l2(plo, (uint32_t)(phi - plo));
+            }
+        }
+
+        // ---- pass 1: chunk maxima and representatives ----
+        // Step i covers chunks 4i .. 4i+3 (one 128-byte line of the row): lane
+        // s takes chunks 4i + 2s and 4i + 2s + 1.  Chunk maxima go to
+        // vmax[p][s][2i + c]; representatives: 4 classes (by step and chunk
+        // parity) x 4 disjoint element subsets.
+        uint32_t rp[8];   // bf16: packed pairs; fp32 uses rq
+        int32_t rq[16];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) rp[x] = 0x80008000u;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) rq[x] = INT32_MIN;
+        auto take = [&](const uint32_t (&w)[8], int j, int cls) {
+            int32_t vm;
+            if constexpr (BF16) {
+                const uint32_t pa = max_s16x2(max_s16x2(w[0], w[2]), max_s16x2(w[4], w[6]));
+                const uint32_t pb = max_s16x2(max_s16x2(w[1], w[3]), max_s16x2(w[5], w[7]));
+                rp[cls * 2] = max_s16x2(rp[cls * 2], pa);
+                rp[cls * 2 + 1] = max_s16x2(rp[cls * 2 + 1], pb);
+                const uint32_t mm = max_s16x2(pa, pb);
+                vm = max(E::pack_lo(mm), E::pack_hi(mm));
+            } else {
+                int32_t m4[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    m4[jj] = max((int32_t)w[jj], (int32_t)w[jj + 4]);
+                    rq[cls * 4 + jj] = max(rq[cls * 4 + jj], m4[jj]);
+                }
+                vm = max(max(m4[0], m4[1]), max(m4[2], m4[3])) >> 16;
+            }
+            sm.vmax[p][s][j] = (int16_t)vm;
+        };
+        const int nsteps = need ? (nchunk + 3) >> 2 : 0;
+        // step 0 and the last step hold the row's edge chunks: masked loads
+        auto edge_step = [&](int i, int cls0) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int k = 4 * i + 2 * s + c;
+                if (k < nchunk) {
+                    uint32_t w[8];
+                    pair_load_edge<BF16>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
+                    take(w, 2 * i + c, cls0 + c);
+                }
+            }
+        };
+        if (nsteps > 0) edge_step(0, 0);
+        // interior steps 1 .. i_last hold chunks <= nchunk - 2 only; a rolling
+        // window of 2 steps (4 chunks per lane) stays in flight
+        const int i_last = nsteps >= 2 ? (nchunk - 5) / 4 : 0;
+        {
+            uint32_t w[2][2][8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (1 + u <= i_last) {
+                    const uintptr_t ad = c0 + ((uintptr_t)(4 * (1 + u) + 2 * s) << 5);
+                    ld32(ad, w[u][0]);
+                    ld32(ad + 32, w[u][1]);
+                }
+            for (int ib = 1; ib <= i_last; ib += 2) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int i = ib + u;
+                    if (i <= i_last) {
+                        take(w[u][0], 2 * i, 2 * u);
+                        take(w[u][1], 2 * i + 1, 2 * u + 1);
+                        if (i + 2 <= i_last) {
+                            const uintptr_t ad = c0 + ((uintptr_t)(4 * (i + 2) + 2 * s) << 5);
+                            ld32(ad, w[u][0]);
+                            ld32(ad + 32, w[u][1]);
+                        }
+                    }
+                }
+            }
+        }
+        if (nsteps >= 2) edge_step(nsteps - 1, 2);
+
+        // ---- theta: the K'-th largest of the row's 32 representatives ----
+        int32_t rep[16];
+        if constexpr (BF16) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                rep[2 * x] = E::pack_lo(rp[x]);
+                rep[2 * x + 1] = E::pack_hi(rp[x]);
+            }
+        } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) rep[x] = rq[x];
+        }
+        int c0n = 0;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) c0n += rep[x] >= 0 ? 1 : 0;
+        c0n += __shfl_xor_sync(kFull, c0n, 1);
+        const bool fast = need && c0n >= r.kp;
+        int32_t theta = 0;
+        for (int bit = kTop; bit >= kLow; --bit) {
+            const int32_t tt = theta | (1 << bit);
+            int c = 0;
+#pragma unroll
+            for (int x = 0; x < 16; ++x) c += rep[x] >= tt ? 1 : 0;
+            c += __shfl_xor_sync(kFull, c, 1);
+            if (c >= r.kp) theta = tt;
+        }
+        const bool ovf0 = need && !fast && (r.hi - r.lo) > kPairCand;
+        if (s == 0) {
+            sm.ccount[p] = 0;
+            sm.ovf[p] = ovf0 ? 1 : 0;
+            PairRowDesc d;
+            d.c0 = c0;
+            d.row_ptr = reinterpret_cast<uintptr_t>(row_ptr);
+            d.base_id = base_id;
+            d.lo = r.lo;
+            d.hi = r.hi;
+            d.theta = theta;
+            d.fast = fast ? 1 : 0;
+            d.nchunk = nchunk;
+            sm.desc[p] = d;
+        }
+        const int32_t th16 = BF16 ? theta : (theta >> 16);
+
+        // ---- queue the chunks that can hold candidates ----
+        // lane-local entry j holds chunk 4 (j >> 1) + 2 s + (j & 1)
+        const int my_n = (need && !ovf0) ? 2 * nsteps : 0;
+        unsigned long long hot = 0;
+        for (int i0 = 0; i0 < my_n; i0 += 8) {
+            const uint4 pk = *reinterpret_cast<const uint4*>(&sm.vmax[p][s][i0]);
+            const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = i0 + u;
+                const int k = 4 * (j >> 1) + 2 * s + (j & 1);
+                const int32_t vm = (int32_t)(int16_t)(uint16_t)(wv[u >> 1] >> ((u & 1) * 16));
+                if (j < my_n && k < nchunk && (!fast || vm >= th16)) hot |= 1ull << j;
+            }
+        }
+        int qtotal;
+        int qpos = warp_excl_scan(__popcll(hot), lane, qtotal);
+        while (hot) {
+            const int j = __ffsll((long long)hot) - 1;
+            hot &= hot - 1;
+            sm.q.queue[qpos++] = (uint16_t)((p << 8) | (4 * (j >> 1) + 2 * s + (j & 1)));
+        }
+        const int qn = qtotal;
+        __syncwarp();
+
+        // ---- candidates from the queued chunks, 32 at a time ----
+        // Every chunk is loaded whole (it lies inside the score buffer unless
+        // the row's edges cross the buffer's ends, which the descriptor flags);
+        // ids outside [lo, hi) are cut by a range mask; elements >= theta are
+        // found with packed compares and emitted through a per-lane scratch.
+        for (int base = 0; base < qn; base += 32) {
+            const int e = base + lane;
+            if (e < qn) {
+                const int ent = sm.q.queue[e];
+                const int pp = ent >> 8;
+                const int k = ent & 0xFF;
+                const PairRowDesc d = sm.desc[pp];
+                uint32_t w[8];
+                const uintptr_t addr = (uintptr_t)d.c0 + ((uintptr_t)k << 5);
+                if (addr >= P.buf_lo && addr + 32 <= P.buf_hi)
+                    ld32(addr, w);
+                else
+                    pair_load_edge<BF16>(P, k, (uintptr_t)d.c0, d.base_id, d.lo, d.hi,
+                                         reinterpret_cast<const char*>(d.row_ptr), w);
+                const int first_id = d.base_id + k * CE;
+                const int lo_e = min(max(d.lo - first_id, 0), CE);
+                const int hi_e = min(max(d.hi - first_id, 0), CE);
+                uint32_t m = ((1u << hi_e) - 1u) & ~((1u << lo_e) - 1u);
+                if (d.fast) {
+                    if constexpr (BF16) {
+                        // per half: 1 if raw >= theta (signed), gathered into 16 bits
+                        const uint32_t t2 = ((uint32_t)(d.theta - 1) & 0xFFFFu) * 0x10001u;
+                        uint32_t b[8];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            b[x] = min_u16x2(max_s16x2(w[x], t2) ^ t2, 0x00010001u);
+                        uint32_t bits = 0;
+#pragma unroll
+                        for (int x = 0; x < 8; x += 2) {
+                            // bytes: element 2x, 2x+1, 2x+2, 2x+3 as 0/1
+                            const uint32_t v4 = __byte_perm(b[x], b[x + 1], 0x6420);
+                            bits |= ((v4 * 0x01020408u) >> 24) << (2 * x);
+                        }
+                        m &= bits;
+                    } else {
+                        uint32_t bits = 0;
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) bits |= ((int32_t)w[x] >= d.theta ? 1u : 0u) << x;
+                        m &= bits;
+                    }
+                }
+                const int nc = __popc(m);
+                if (nc) {
+                    int pos = atomicAdd(&sm.ccount[pp], nc);
+                    if (pos + nc <= kPairCand) {
+                        uint32_t* scr = sm.scratch[lane];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) scr[x] = w[x];
+                        while (m) {
+                            const int x = __ffs(m) - 1;
+                            m &= m - 1;
+                            int32_t raw;
+                            if constexpr (BF16)
+                                raw = reinterpret_cast<const int16_t*>(scr)[x];
+                            else
+                                raw = (int32_t)scr[x];
+                            sm.cand[pp][pos++] = make_ck<CK>(E::key(raw), first_id + x);
+                        }
+                    } else {
+                        sm.ovf[pp] = 1;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+
+        // ---- exact select: sort the row's candidates, keep the first K' ----
+        const bool ovf = sm.ovf[p] != 0;
+        const int cn = min(sm.ccount[p], kPairCand);
+        const bool sel_ok = need && !ovf;
+        CK x[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int pos = s * 16 + u;
+            x[u] = (sel_ok && pos < cn) ? sm.cand[p][pos] : (CK)0;
+        }
+        pair_sort32_desc<CK>(x, s);
+        __syncwarp();
+        if constexpr (SMALLK) {
+            // K' <= 16: the kept positions are lane 0's registers
+            uint32_t y[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) y[u] = (s == 0 && u < r.kp) ? ck_low(x[u]) : 0u;
+            lane_sort16_desc<uint32_t>(y);
+            if (sel_ok && s == 0) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (u < r.kp) sm.q.sorted[p][u] = (int32_t)(kLowMax - y[u]);
+            }
+        } else {
+            uint32_t y[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) y[u] = (s * 16 + u < r.kp) ? ck_low(x[u]) : 0u;
+            pair_sort32_desc<uint32_t>(y, s);
+            if (sel_ok) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (s * 16 + u < r.kp) sm.q.sorted[p][s * 16 + u] = (int32_t)(kLowMax - y[u]);
+            }
+        }
+        __syncwarp();
+
+        // ---- outputs ----
+        group_write_outputs<2>(P, row, r, r.all, sm.q.sorted[p], s, active && (!need || !ovf));
+
+        // ---- rows whose candidates overflowed: the whole warp redoes them ----
+        unsigned fb = __ballot_sync(kFull, s == 0 && need && ovf);
+        __syncwarp();
+        while (fb) {
+            const int bit = __ffs(fb) - 1;
+            fb &= fb - 1;
+            const int64_t frow = it * kPairRows + (bit >> 1);
+            uint32_t* s_keys = reinterpret_cast<uint32_t*>(&sm);
+            warp_item<BF16, 4, 2>(P, frow, 0, s_keys, reinterpret_cast<int32_t*>(s_keys + P.cap),
+                                  lane);
+            __syncwarp();
+        }
+        __syncwarp();
+    }
+}
+
+template <bool BF16>
+cudaError_t launch_pair(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
+    const bool small = P.a.K - P.a.num_init - P.a.num_local <= 16;
+    auto kern = small ? pair_select_kernel<BF16, true> : pair_select_kernel<BF16, false>;
+    if (pol.smem_bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             pol.smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<pol.grid, kPairWarps * 32, pol.smem_bytes, st>>>(P);
+    return cudaGetLastError();
 }
 
 template <bool BF16, int R>
@@ -1215,6 +1695,9 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
     if (pol.path == BSA_PATH_GROUP)
         return a.dtype == BSA_DTYPE_BF16 ? launch_group<true>(P, pol, stream)
                                          : launch_group<false>(P, pol, stream);
+    if (pol.path == BSA_PATH_PAIR)
+        return a.dtype == BSA_DTYPE_BF16 ? launch_pair<true>(P, pol, stream)
+                                         : launch_pair<false>(P, pol, stream);
     return a.dtype == BSA_DTYPE_BF16 ? launch_dt<true>(P, pol, stream)
                                      : launch_dt<false>(P, pol, stream);
 }

@@ -73,6 +73,7 @@ extern "C" {
 #define BSA_PATH_ROW 0      /* one warp streams a whole row                 */
 #define BSA_PATH_SPLIT 1    /* several warps per row + last-arriver merge   */
 #define BSA_PATH_GROUP 2    /* 4 lanes per row, 8 rows per warp (K <= 32)   */
+#define BSA_PATH_PAIR 3     /* 2 lanes per row, 16 rows per warp (K <= 32)  */
 
 typedef struct bsa_launch_policy {
     int32_t path;             /* BSA_PATH_*                                   */

@@ -57,9 +57,9 @@ BF, FP = 0, 1
 
 
 @pytest.mark.parametrize("M,dtype,K,path", [
-    # group path: topk <= 32 and a row of at most 2 KB
-    (16, FP, 4, 2), (74, BF, 16, 2), (128, BF, 16, 2), (129, BF, 16, 2), (1024, BF, 16, 2),
-    (1025, BF, 16, 0), (512, FP, 16, 2), (513, FP, 16, 0), (1024, BF, 32, 2), (1024, BF, 33, 0),
+    # pair path: topk <= 32 and a row of at most 2 KB
+    (16, FP, 4, 3), (74, BF, 16, 3), (128, BF, 16, 3), (129, BF, 16, 3), (1024, BF, 16, 3),
+    (1025, BF, 16, 0), (512, FP, 16, 3), (513, FP, 16, 0), (1024, BF, 32, 3), (1024, BF, 33, 0),
     (74, BF, 64, 0), (8192, BF, 16, 0)])
 def test_policy_path(bsa, M, dtype, K, path):
     assert _policy(bsa, 10**6, M, K, dtype)["path"] == path
@@ -78,18 +78,18 @@ def test_policy_vectors_per_lane_warp_path(bsa, M, dtype, nv):
 
 def test_policy_production_capacity(bsa):
     """The production 8k+1k graph (74 blocks, query length 4, topk 16) and
-    every capacity up to 128 run on the group path; at topk 64 they run one
+    every capacity up to 128 run on the pair path; at topk 64 they run one
     warp per row in a single pass."""
     for M in (65, 74, 128):
         for rows in (4, 64 * 4 * 4, 10**6):
             p = _policy(bsa, rows, M, 16, BF)
-            assert p["path"] == bsa.BSA_PATH_GROUP and p["chunks_per_row"] == 1
+            assert p["path"] == bsa.BSA_PATH_PAIR and p["chunks_per_row"] == 1
             p = _policy(bsa, rows, M, 64, BF)
             assert p["path"] == bsa.BSA_PATH_ROW and p["vecs_per_lane"] == 1
 
 
-@pytest.mark.parametrize("K,reps", [(1, 8), (16, 8), (17, 8), (32, 8)])
-def test_policy_representatives_group(bsa, K, reps):
+@pytest.mark.parametrize("K,reps", [(1, 16), (16, 16), (17, 16), (32, 16)])
+def test_policy_representatives_pair(bsa, K, reps):
     assert _policy(bsa, 1000, 1024, K, BF)["reps_per_lane"] == reps
 
 
@@ -116,7 +116,7 @@ def test_policy_capacity_and_grid(bsa):
     assert p["smem_bytes"] == p["warps_per_cta"] * p["cand_capacity"] * 8
     assert p["grid"] == 152 * 4
     g = _policy(bsa, 10**6, 1024, 16, BF)
-    assert g["path"] == bsa.BSA_PATH_GROUP and g["grid"] == 152 * 3
+    assert g["path"] == bsa.BSA_PATH_PAIR and g["grid"] == 152 * 5
     # the warp fallback's buffer fits in a group warp's shared memory
     assert g["cand_capacity"] * 8 <= g["smem_bytes"] // g["warps_per_cta"]
     assert _policy(bsa, 10, 74, 16, BF)["grid"] == 1
