@@ -32,13 +32,15 @@ MAX_TOPK = 1024
 MAX_K_TILES = 65536
 
 _ERRORS = {-1: "BSA_ERR_NULL", -2: "BSA_ERR_SHAPE", -3: "BSA_ERR_TOPK", -4: "BSA_ERR_DTYPE",
-           -5: "BSA_ERR_WORKSPACE", -6: "BSA_ERR_ROWS", -7: "BSA_ERR_ALIGN"}
+           -5: "BSA_ERR_WORKSPACE", -6: "BSA_ERR_ROWS", -7: "BSA_ERR_ALIGN",
+           -8: "BSA_ERR_CAPACITY"}
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Names of every extern "C" symbol the header declares (checked by the tests).
 EXPORTED = [
     "bsa_status_string", "bsa_num_valid_pages_decode", "bsa_num_valid_pages_varlen",
     "bsa_topk_workspace_bytes", "bsa_topk_select", "bsa_build_sparse_block_table",
-    "bsa_topk_select_sparse_table", "bsa_select_policy",
+    "bsa_topk_select_sparse_table", "bsa_select_policy", "bsa_topk_select_noalloc",
 ]
 
 
@@ -93,6 +95,8 @@ def lib() -> ctypes.CDLL:
                                                        i32, i32, i32, vp, i64, vp, vp, vp, vp, sz,
                                                        vp]
             L.bsa_select_policy.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(LaunchPolicy)]
+            L.bsa_topk_select_noalloc.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i32, i32,
+                                                  i32, vp, vp]
             for name in EXPORTED[1:]:
                 if name != "bsa_topk_workspace_bytes":
                     getattr(L, name).restype = ctypes.c_int
@@ -273,3 +277,23 @@ def bsa_topk_select_sparse_table(scores: torch.Tensor, seq_lens: torch.Tensor,
                _ptr(seq_lens), K, num_init, num_local, _ptr(block_table), MB, _ptr(out_idx),
                _ptr(sparse_bt), _ptr(sparse_ctx), _ptr(workspace), wbytes, _stream(dev)))
     return out_idx, sparse_bt, sparse_ctx
+
+
+def bsa_topk_select_noalloc(scores: torch.Tensor, num_valid_pages: torch.Tensor, K: int,
+                            num_init: int = 1, num_local: int = 1,
+                            out_idx: torch.Tensor | None = None,
+                            M: int | None = None) -> torch.Tensor:
+    """bsa_topk_select without a workspace argument, for callers that cannot
+    allocate device memory: the library's own fixed device array serves as
+    scratch (see include/bsa_topk.h).  Same results as bsa_topk_select."""
+    T, H, M, ts, hs = _score_view(scores, M)
+    dt = _score_dtype(scores)
+    _dev_i32(num_valid_pages, "num_valid_pages")
+    if out_idx is None:
+        out_idx = torch.empty((T, H, K), dtype=torch.int32, device=scores.device)
+    _dev_i32(out_idx, "out_idx")
+    _check("bsa_topk_select_noalloc",
+           lib().bsa_topk_select_noalloc(_ptr(scores), dt, T, H, M, ts, hs, _ptr(num_valid_pages),
+                                         K, num_init, num_local, _ptr(out_idx),
+                                         _stream(scores.device)))
+    return out_idx

@@ -216,6 +216,7 @@ const char* bsa_status_string(int status) {
         case BSA_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
         case BSA_ERR_ROWS: return "T != num_reqs * decode_query_len";
         case BSA_ERR_ALIGN: return "scores pointer not aligned to its element size";
+        case BSA_ERR_CAPACITY: return "request needs more scratch than the built-in array holds";
         default: break;
     }
     if (status > 0) return cudaGetErrorString((cudaError_t)status);

@@ -57,6 +57,7 @@ extern "C" {
 #define BSA_ERR_WORKSPACE (-5) /* workspace missing, too small or misaligned    */
 #define BSA_ERR_ROWS (-6)      /* T != num_reqs * decode_query_len              */
 #define BSA_ERR_ALIGN (-7)     /* scores pointer not aligned to its element size */
+#define BSA_ERR_CAPACITY (-8)  /* request needs more than the built-in scratch  */
 
 /* ---- constants ---------------------------------------------------------- */
 #define BSA_PAGE_SIZE 128              /* tokens per sparse block ([47502] PAGE_SIZE) */
@@ -184,6 +185,25 @@ int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_
                                  int64_t max_blocks, int32_t* out_idx, int32_t* sparse_bt,
                                  int32_t* sparse_ctx, void* workspace, size_t workspace_bytes,
                                  void* stream);
+
+/* Size of the device scratch array behind bsa_topk_select_noalloc. */
+#define BSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* bsa_topk_select for callers that cannot allocate device memory (no
+ * counterpart on the pages: it exists for deployment, not for the method).
+ * Same arguments, results and errors as bsa_topk_select, without the
+ * workspace: when the launch policy needs one (few long rows), the library
+ * uses a file-scope device array of BSA_NOALLOC_SCRATCH_BYTES (16 MiB) that
+ * every GPU loading the library holds until the process exits.  Allocates
+ * nothing.  Returns BSA_ERR_CAPACITY, before launching anything, when
+ * bsa_topk_workspace_bytes(T, H, M, K, dtype) exceeds that size.  The first
+ * call on a device looks the array's address up (cudaGetSymbolAddress), so it
+ * should come before any stream capture.  All calls on a device share the
+ * array: calls that overlap on the GPU race. */
+int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_t T, int64_t H, int64_t M,
+                            int64_t token_stride, int64_t head_stride,
+                            const int32_t* num_valid_pages, int32_t K, int32_t num_init,
+                            int32_t num_local, int32_t* out_idx, void* stream);
 
 /* The selector's launch policy ([55235] _decode_topk_launch_policy, redone
  * for sm_103a) for `rows` = T*H rows of capacity M on a GPU with `num_sms`

@@ -44,7 +44,7 @@ def test_library_is_built_for_sm103a(bsa):
 
 def test_status_strings(bsa):
     L = bsa.lib()
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         s = L.bsa_status_string(code).decode()
         assert s and s != "unknown status"
 
