@@ -1383,29 +1383,34 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
             }
         };
         if (nsteps > 0) edge_step(0, 0);
-        // interior steps 1 .. i_last hold chunks <= nchunk - 2 only; a rolling
-        // window of 2 steps (4 chunks per lane) stays in flight
+        // interior steps 1 .. i_last hold chunks <= nchunk - 2 only; the next
+        // step's two chunks are loaded while the current one is reduced
         const int i_last = nsteps >= 2 ? (nchunk - 5) / 4 : 0;
-        {
-            uint32_t w[2][2][8];
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-                if (1 + u <= i_last) {
-                    const uintptr_t ad = c0 + ((uintptr_t)(4 * (1 + u) + 2 * s) << 5);
-                    ld32(ad, w[u][0]);
-                    ld32(ad + 32, w[u][1]);
-                }
-            for (int ib = 1; ib <= i_last; ib += 2) {
+        if (i_last >= 1) {
+            uint32_t w0[8], w1[8];
+            uintptr_t ad = c0 + ((uintptr_t)(4 + 2 * s) << 5);
+            ld32(ad, w0);
+            ld32(ad + 32, w1);
+            for (int i = 1; i <= i_last; i += 2) {
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const int i = ib + u;
-                    if (i <= i_last) {
-                        take(w[u][0], 2 * i, 2 * u);
-                        take(w[u][1], 2 * i + 1, 2 * u + 1);
-                        if (i + 2 <= i_last) {
-                            const uintptr_t ad = c0 + ((uintptr_t)(4 * (i + 2) + 2 * s) << 5);
-                            ld32(ad, w[u][0]);
-                            ld32(ad + 32, w[u][1]);
+                    const int ii = i + u;
+                    if (ii <= i_last) {
+                        uint32_t n0[8], n1[8];
+                        const bool more = ii < i_last;
+                        if (more) {
+                            ad += 128;
+                            ld32(ad, n0);
+                            ld32(ad + 32, n1);
+                        }
+                        take(w0, 2 * ii, 2 * u);
+                        take(w1, 2 * ii + 1, 2 * u + 1);
+                        if (more) {
+#pragma unroll
+                            for (int x = 0; x < 8; ++x) {
+                                w0[x] = n0[x];
+                                w1[x] = n1[x];
+                            }
                         }
                     }
                 }
