@@ -320,8 +320,8 @@ def run_ours(args):
         "hbm_frac_of_peak": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
-                     "kernel": "select_kernel (fused sparse-table epilogue)"
-                     if args.path == "fused" else "select_kernel",
+                     "kernel": "pair_select_kernel (fused sparse-table epilogue)"
+                     if args.path == "fused" else "pair_select_kernel",
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
                      "traffic_note": None if traffic is None else traffic.get("note")},
