@@ -123,7 +123,7 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
         const int gsmem = kPairWarps * (int)(dtype == BSA_DTYPE_BF16
                                                  ? sizeof(PairSmem<uint32_t>)
                                                  : sizeof(PairSmem<unsigned long long>));
-        int ctas = 5;  // the kernel's register bound: 5 CTAs of 4 warps per SM
+        int ctas = kPairCtas;  // the kernel's register bound
         while (ctas > 1 && ctas * (gsmem + 1024) > 228 * 1024) --ctas;
         const int64_t items = (rows + kPairRows - 1) / kPairRows;
         int64_t grid = (items + kPairWarps - 1) / kPairWarps;

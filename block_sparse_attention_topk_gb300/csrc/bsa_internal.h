@@ -56,25 +56,30 @@ constexpr int kPairMaxChunks = 66;   // 32-byte chunks per row (2 KB + alignment
 constexpr int kPairStepsPad = 40;    // >= ceil(kPairMaxChunks / 2), multiple of 8
 constexpr int kPairCand = 32;        // candidate capacity per row (one 2-lane sort)
 constexpr int kPairWarps = 4;        // warps per CTA
+constexpr int kPairCtas = 5;         // CTAs per SM the kernel's register bound allows
 
 struct PairRowDesc {
     unsigned long long c0;       // first 32-byte chunk of the non-forced range
     unsigned long long row_ptr;  // address of element 0 of the row
     int32_t base_id, lo, hi, theta;
-    int32_t fast, nchunk;
+    int32_t nchunk, pad;
 };
 
 template <typename CK>
 struct PairSmem {
-    // chunk maxima (raw signed; fp32 keeps the top 16 bits), lane-major:
-    // chunk k = s + 2 i of row p at vmax[p][s][i]
-    int16_t vmax[kPairRows][2][kPairStepsPad];
+    union {
+        // chunk maxima (signed keys; fp32 keeps the top 16 bits), lane-major:
+        // chunk k = 4 i + 2 s + c of row p at vmax[p][s][2 i + c]; live from
+        // pass 1 until the queue is built
+        int16_t vmax[kPairRows][2][kPairStepsPad];
+        // one 32-byte chunk per lane while candidates are collected
+        uint32_t scratch[32][8];
+    } a;
     union {
         uint16_t queue[kPairRows * kPairMaxChunks];  // (row << 8 | chunk) work items
         int32_t sorted[kPairRows][kGroupMaxK];      // selected ids, ascending
     } q;
     CK cand[kPairRows][kPairCand];                  // candidate composite keys
-    uint32_t scratch[32][8];                        // one 32-byte chunk per lane
     int32_t ccount[kPairRows];
     int32_t ovf[kPairRows];
     PairRowDesc desc[kPairRows];

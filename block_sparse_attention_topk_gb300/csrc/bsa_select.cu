@@ -334,36 +334,50 @@ __device__ void write_outputs(const KernelParams& P, int64_t row, int n, int lo,
 
 // Row geometry shared by both paths: causal bound, forced ranges, how many
 // non-forced ids to select.
+// rows < 2^31 (checked on the host), so t, h and req fit 32 bits; the causal
+// length is at most seq_lens[req] <= INT32_MAX.
 struct RowInfo {
-    int64_t t, h, req, causal_len;
+    int32_t t, h, req, causal_len;
     int v, lo, hi, n, kp;
     bool all, need;
 };
 
+// Fused mode of a kernel instantiation: read from the arguments at run time,
+// or fixed at compile time (plain select / fused select + table).
+constexpr int kFusedRuntime = 0, kFusedNo = 1, kFusedYes = 2;
+
+template <int FM>
+__device__ __forceinline__ bool is_fused(const SelectArgs& a) {
+    if constexpr (FM == kFusedRuntime) return a.fused;
+    else return FM == kFusedYes;
+}
+
 // The per-row metadata word: num_valid_pages[t] (select) or seq_lens[req]
 // (fused).  Split from row_info so the group path can load it one item early.
+template <int FM = kFusedRuntime>
 __device__ __forceinline__ int32_t row_meta(const SelectArgs& a, int64_t row) {
     // rows < 2^31 (checked on the host): 32-bit division is exact
     const uint32_t t32 = (uint32_t)row / (uint32_t)a.H;
-    if (a.fused) return __ldg(a.seq_lens + t32 / (uint32_t)a.dql);
+    if (is_fused<FM>(a)) return __ldg(a.seq_lens + t32 / (uint32_t)a.dql);
     return __ldg(a.num_valid_pages + t32);
 }
 
+template <int FM = kFusedRuntime>
 __device__ __forceinline__ RowInfo row_info_from(const SelectArgs& a, int64_t row, int32_t meta) {
     RowInfo r;
     const uint32_t t32 = (uint32_t)row / (uint32_t)a.H;
-    r.t = t32;
-    r.h = row - r.t * a.H;
+    r.t = (int32_t)t32;
+    r.h = (int32_t)((uint32_t)row - t32 * (uint32_t)a.H);
     int64_t pages;
     r.causal_len = 0;
     r.req = 0;
-    if (a.fused) {
+    if (is_fused<FM>(a)) {
         const uint32_t req32 = t32 / (uint32_t)a.dql;
-        r.req = req32;
-        const int64_t lq = r.t - r.req * a.dql;
+        r.req = (int32_t)req32;
+        const int32_t lq = (int32_t)(t32 - req32 * (uint32_t)a.dql);
         const int64_t pos = (int64_t)meta - a.dql + lq;
-        r.causal_len = pos + 1 > 0 ? pos + 1 : 0;
-        pages = (r.causal_len + kPageSize - 1) >> kLogPageSize;
+        r.causal_len = (int32_t)(pos + 1 > 0 ? pos + 1 : 0);
+        pages = ((int64_t)r.causal_len + kPageSize - 1) >> kLogPageSize;
     } else {
         pages = meta;
     }
@@ -813,17 +827,18 @@ __device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,
 // (two 16-byte stores) and their part of ctx.  Every lane of the warp calls
 // this (ctx is summed with shuffles inside each row's lanes); `write` masks
 // the stores.
-template <int LANES>
+template <int LANES, int FM = kFusedRuntime>
 __device__ void group_write_outputs(const KernelParams& P, int64_t row, const RowInfo& r,
                                     bool all, const int32_t* sorted, int q, bool write) {
     const SelectArgs& a = P.a;
     const int K = a.K;
+    const bool fused = is_fused<FM>(a);
     int ctx = 0;
     if (write) {
         int32_t* out = a.out_idx != nullptr ? a.out_idx + row * K : nullptr;
         const int width = K * kPagesPerBlock;
-        int32_t* bt = a.fused ? a.sparse_bt + row * (int64_t)width : nullptr;
-        const int32_t* table = a.fused ? a.block_table + r.req * a.max_blocks : nullptr;
+        int32_t* bt = fused ? a.sparse_bt + row * (int64_t)width : nullptr;
+        const int32_t* table = fused ? a.block_table + (int64_t)r.req * a.max_blocks : nullptr;
         const bool vec_ok = ((reinterpret_cast<uintptr_t>(bt)) & 15) == 0;
         // lane q owns the contiguous slots [q * per, q * per + per); 8 at a
         // time: ids first, then all table gathers in flight together, then
@@ -882,7 +897,7 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
             }
         }
     }
-    if (!a.fused) return;
+    if (!fused) return;
 #pragma unroll
     for (int m = 1; m < LANES; m <<= 1) ctx += __shfl_xor_sync(kFull, ctx, m);
     if (write && q == 0) a.sparse_ctx[row] = ctx;
@@ -1172,8 +1187,16 @@ __global__ void __launch_bounds__(kThreads, 3) group_select_kernel(const KernelP
 // Same algorithm as the group path with half the lanes per row, so that the
 // fixed per-row steps (threshold search, sorts, outputs) cover 16 rows per
 // warp instruction, and with 32-byte chunks (one 256-bit load per lane, a
-// row's pair reads 64 contiguous bytes per instruction).  Representatives
-// stay packed: bf16 keeps 16 per lane in 8 registers updated with max.s16x2.
+// row's pair reads 64 contiguous bytes per instruction).
+//
+// Elements become signed order-preserving keys as they are loaded: a
+// negative value has its low 15 (bf16) or 31 (fp32) bits flipped, after which
+// signed integer order is totalOrder.  Maxima, representatives and the
+// threshold therefore work for rows of any sign.  Representatives stay
+// packed: bf16 keeps 16 per lane in 8 registers updated with max.s16x2.
+//
+// A row whose candidates overflow the 32-entry list is redone by the whole
+// warp on the warp path (no candidate limit) before the warp moves on.
 // ===========================================================================
 
 __device__ __forceinline__ void ld32(uintptr_t addr, uint32_t (&w)[8]) {
@@ -1181,6 +1204,29 @@ __device__ __forceinline__ void ld32(uintptr_t addr, uint32_t (&w)[8]) {
         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
           "=r"(w[7])
         : "l"(addr));
+}
+
+// Signed order-preserving key of one raw element (sign-extended to int32).
+template <bool BF16>
+__device__ __forceinline__ int32_t key_of_raw(int32_t raw) {
+    if constexpr (BF16) return raw ^ ((raw >> 15) & 0x7FFF);
+    else return raw ^ ((raw >> 31) & 0x7FFFFFFF);
+}
+
+// The same on a whole 32-byte chunk, in place (bf16: two keys per word).
+template <bool BF16>
+__device__ __forceinline__ void chunk_to_keys(uint32_t (&w)[8]) {
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+        if constexpr (BF16) {
+            // 0xFFFF in each half whose sign bit is set (prmt sign-replicate)
+            uint32_t sg;
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sg) : "r"(w[x]), "r"(0u), "n"(0xBB99));
+            w[x] ^= sg & 0x7FFF7FFFu;
+        } else {
+            w[x] ^= (uint32_t)((int32_t)w[x] >> 31) & 0x7FFFFFFFu;
+        }
+    }
 }
 
 template <bool BF16>
@@ -1199,7 +1245,8 @@ __device__ __forceinline__ void chunk_set(uint32_t (&w)[8], int e, int32_t raw) 
     }
 }
 
-// Chunk k of a row's non-forced range, with ids outside [lo, hi) masked.
+// Chunk k of a row's non-forced range as keys, with ids outside [lo, hi) set
+// to the smallest key (0x8000 / 0x80000000).
 template <bool BF16>
 __device__ __forceinline__ void pair_load_edge(const KernelParams& P, int k, uintptr_t c0,
                                                int base_id, int lo, int hi,
@@ -1210,6 +1257,7 @@ __device__ __forceinline__ void pair_load_edge(const KernelParams& P, int k, uin
     const uintptr_t addr = c0 + ((uintptr_t)k << 5);
     if (addr >= P.buf_lo && addr + 32 <= P.buf_hi) {
         ld32(addr, w);
+        chunk_to_keys<BF16>(w);
 #pragma unroll
         for (int e = 0; e < CE; ++e) {
             const int id = base_id + k * CE + e;
@@ -1221,7 +1269,8 @@ __device__ __forceinline__ void pair_load_edge(const KernelParams& P, int k, uin
 #pragma unroll
         for (int e = 0; e < CE; ++e) {
             const int id = base_id + k * CE + e;
-            if (id >= lo && id < hi) chunk_set<BF16>(w, e, E::load_one(row_ptr + (int64_t)id * S));
+            if (id >= lo && id < hi)
+                chunk_set<BF16>(w, e, key_of_raw<BF16>(E::load_one(row_ptr + (int64_t)id * S)));
         }
     }
 }
@@ -1281,16 +1330,20 @@ __device__ __forceinline__ void lane_sort16_desc(T (&x)[16]) {
     }
 }
 
-template <bool BF16, bool SMALLK>
-__global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const KernelParams P) {
+template <bool BF16, bool SMALLK, int FM>
+__global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel(const KernelParams P) {
     using E = Elem<BF16>;
     using CK = typename std::conditional<BF16, uint32_t, unsigned long long>::type;
     using G = PairSmem<CK>;
     constexpr int S = E::kBytes;
     constexpr int CE = 32 / S;                 // elements per 32-byte chunk
-    constexpr int kTop = BF16 ? 14 : 30;
+    // theta is searched in offset binary (key + 2^15 / 2^31), top bit first;
+    // bits below kLow stay 0, which only lowers the bound
+    constexpr int kTop = BF16 ? 15 : 31;
     constexpr int kLow = BF16 ? 3 : 19;
+    constexpr uint32_t kFlip = BF16 ? 0x8000u : 0x80000000u;  // signed key -> unsigned key
     constexpr uint32_t kLowMax = BF16 ? 0xFFFFu : 0xFFFFFFFFu;
+    constexpr int32_t kKeyMin = BF16 ? -32768 : INT32_MIN;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -1303,16 +1356,16 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
 
     int64_t it = (int64_t)blockIdx.x * kPairWarps + warp;
     int32_t meta = 0;
-    if (it < nitems && it * kPairRows + p < P.rows) meta = row_meta(a, it * kPairRows + p);
+    if (it < nitems && it * kPairRows + p < P.rows) meta = row_meta<FM>(a, it * kPairRows + p);
     for (; it < nitems; it += stride) {
         const int64_t row = it * kPairRows + p;
         const bool active = row < P.rows;
         const int64_t nrow = (it + stride) * kPairRows + p;
         const bool nactive = it + stride < nitems && nrow < P.rows;
-        const int32_t nmeta = nactive ? row_meta(a, nrow) : 0;
+        const int32_t nmeta = nactive ? row_meta<FM>(a, nrow) : 0;
         RowInfo r{};
         r.all = true;
-        if (active) r = row_info_from(a, row, meta);
+        if (active) r = row_info_from<FM>(a, row, meta);
         meta = nmeta;
         const bool need = active && r.need;
 
@@ -1322,7 +1375,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
         int nchunk = 0, base_id = 0;
         if (need) {
             row_ptr = reinterpret_cast<const char*>(a.scores) +
-                      (r.t * a.token_stride + r.h * a.head_stride) * S;
+                      ((int64_t)r.t * a.token_stride + (int64_t)r.h * a.head_stride) * S;
             const uintptr_t a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * S;
             const uintptr_t a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * S;
             c0 = a_lo & ~(uintptr_t)31;
@@ -1346,7 +1399,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
         uint32_t rp[8];   // bf16: packed pairs; fp32 uses rq
         int32_t rq[16];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) rp[x] = 0x80008000u;
+        for (int x = 0; x < 8; ++x) rp[x] = E::kMaskWord;
 #pragma unroll
         for (int x = 0; x < 16; ++x) rq[x] = INT32_MIN;
         auto take = [&](const uint32_t (&w)[8], int j, int cls) {
@@ -1367,7 +1420,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
                 }
                 vm = max(max(m4[0], m4[1]), max(m4[2], m4[3])) >> 16;
             }
-            sm.vmax[p][s][j] = (int16_t)vm;
+            sm.a.vmax[p][s][j] = (int16_t)vm;
         };
         const int nsteps = need ? (nchunk + 3) >> 2 : 0;
         // step 0 and the last step hold the row's edge chunks: masked loads
@@ -1403,7 +1456,9 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
                             ld32(ad, n0);
                             ld32(ad + 32, n1);
                         }
+                        chunk_to_keys<BF16>(w0);
                         take(w0, 2 * ii, 2 * u);
+                        chunk_to_keys<BF16>(w1);
                         take(w1, 2 * ii + 1, 2 * u + 1);
                         if (more) {
 #pragma unroll
@@ -1418,7 +1473,8 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
         }
         if (nsteps >= 2) edge_step(nsteps - 1, 2);
 
-        // ---- theta: the K'-th largest of the row's 32 representatives ----
+        // ---- theta: a lower bound on the K'-th largest of the row's 32
+        // representatives (distinct elements), on a grid of 2^kLow ----
         int32_t rep[16];
         if constexpr (BF16) {
 #pragma unroll
@@ -1430,24 +1486,22 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
 #pragma unroll
             for (int x = 0; x < 16; ++x) rep[x] = rq[x];
         }
-        int c0n = 0;
-#pragma unroll
-        for (int x = 0; x < 16; ++x) c0n += rep[x] >= 0 ? 1 : 0;
-        c0n += __shfl_xor_sync(kFull, c0n, 1);
-        const bool fast = need && c0n >= r.kp;
-        int32_t theta = 0;
+        uint32_t tu = 0;
         for (int bit = kTop; bit >= kLow; --bit) {
-            const int32_t tt = theta | (1 << bit);
+            const uint32_t cand = tu | (1u << bit);
+            const int32_t tt = BF16 ? (int32_t)cand - 0x8000 : (int32_t)(cand ^ 0x80000000u);
             int c = 0;
 #pragma unroll
             for (int x = 0; x < 16; ++x) c += rep[x] >= tt ? 1 : 0;
             c += __shfl_xor_sync(kFull, c, 1);
-            if (c >= r.kp) theta = tt;
+            if (c >= r.kp) tu = cand;
         }
-        const bool ovf0 = need && !fast && (r.hi - r.lo) > kPairCand;
+        // fewer than K' representatives in the row: tu == 0, every element
+        // of [lo, hi) is a candidate
+        const int32_t theta = BF16 ? (int32_t)tu - 0x8000 : (int32_t)(tu ^ 0x80000000u);
         if (s == 0) {
             sm.ccount[p] = 0;
-            sm.ovf[p] = ovf0 ? 1 : 0;
+            sm.ovf[p] = 0;
             PairRowDesc d;
             d.c0 = c0;
             d.row_ptr = reinterpret_cast<uintptr_t>(row_ptr);
@@ -1455,25 +1509,25 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
             d.lo = r.lo;
             d.hi = r.hi;
             d.theta = theta;
-            d.fast = fast ? 1 : 0;
             d.nchunk = nchunk;
+            d.pad = 0;
             sm.desc[p] = d;
         }
         const int32_t th16 = BF16 ? theta : (theta >> 16);
 
         // ---- queue the chunks that can hold candidates ----
         // lane-local entry j holds chunk 4 (j >> 1) + 2 s + (j & 1)
-        const int my_n = (need && !ovf0) ? 2 * nsteps : 0;
+        const int my_n = need ? 2 * nsteps : 0;
         unsigned long long hot = 0;
         for (int i0 = 0; i0 < my_n; i0 += 8) {
-            const uint4 pk = *reinterpret_cast<const uint4*>(&sm.vmax[p][s][i0]);
+            const uint4 pk = *reinterpret_cast<const uint4*>(&sm.a.vmax[p][s][i0]);
             const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int j = i0 + u;
                 const int k = 4 * (j >> 1) + 2 * s + (j & 1);
                 const int32_t vm = (int32_t)(int16_t)(uint16_t)(wv[u >> 1] >> ((u & 1) * 16));
-                if (j < my_n && k < nchunk && (!fast || vm >= th16)) hot |= 1ull << j;
+                if (j < my_n && k < nchunk && vm >= th16) hot |= 1ull << j;
             }
         }
         int qtotal;
@@ -1484,13 +1538,14 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
             sm.q.queue[qpos++] = (uint16_t)((p << 8) | (4 * (j >> 1) + 2 * s + (j & 1)));
         }
         const int qn = qtotal;
-        __syncwarp();
+        __syncwarp();   // vmax is dead from here on; its space holds the scratch
 
         // ---- candidates from the queued chunks, 32 at a time ----
         // Every chunk is loaded whole (it lies inside the score buffer unless
-        // the row's edges cross the buffer's ends, which the descriptor flags);
-        // ids outside [lo, hi) are cut by a range mask; elements >= theta are
-        // found with packed compares and emitted through a per-lane scratch.
+        // the row's edges cross the buffer's ends, which the edge loader
+        // handles); ids outside [lo, hi) are cut by a range mask; keys >=
+        // theta are found with packed compares and emitted through a per-lane
+        // scratch.
         for (int base = 0; base < qn; base += 32) {
             const int e = base + lane;
             if (e < qn) {
@@ -1500,18 +1555,20 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
                 const PairRowDesc d = sm.desc[pp];
                 uint32_t w[8];
                 const uintptr_t addr = (uintptr_t)d.c0 + ((uintptr_t)k << 5);
-                if (addr >= P.buf_lo && addr + 32 <= P.buf_hi)
+                if (addr >= P.buf_lo && addr + 32 <= P.buf_hi) {
                     ld32(addr, w);
-                else
+                    chunk_to_keys<BF16>(w);
+                } else {
                     pair_load_edge<BF16>(P, k, (uintptr_t)d.c0, d.base_id, d.lo, d.hi,
                                          reinterpret_cast<const char*>(d.row_ptr), w);
+                }
                 const int first_id = d.base_id + k * CE;
                 const int lo_e = min(max(d.lo - first_id, 0), CE);
                 const int hi_e = min(max(d.hi - first_id, 0), CE);
                 uint32_t m = ((1u << hi_e) - 1u) & ~((1u << lo_e) - 1u);
-                if (d.fast) {
+                if (d.theta != kKeyMin) {
                     if constexpr (BF16) {
-                        // per half: 1 if raw >= theta (signed), gathered into 16 bits
+                        // per half: 1 if key >= theta (signed), gathered into 16 bits
                         const uint32_t t2 = ((uint32_t)(d.theta - 1) & 0xFFFFu) * 0x10001u;
                         uint32_t b[8];
 #pragma unroll
@@ -1536,18 +1593,18 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
                 if (nc) {
                     int pos = atomicAdd(&sm.ccount[pp], nc);
                     if (pos + nc <= kPairCand) {
-                        uint32_t* scr = sm.scratch[lane];
+                        uint32_t* scr = sm.a.scratch[lane];
 #pragma unroll
                         for (int x = 0; x < 8; ++x) scr[x] = w[x];
                         while (m) {
                             const int x = __ffs(m) - 1;
                             m &= m - 1;
-                            int32_t raw;
+                            uint32_t ukey;
                             if constexpr (BF16)
-                                raw = reinterpret_cast<const int16_t*>(scr)[x];
+                                ukey = ((uint32_t)reinterpret_cast<const uint16_t*>(scr)[x]) ^ kFlip;
                             else
-                                raw = (int32_t)scr[x];
-                            sm.cand[pp][pos++] = make_ck<CK>(E::key(raw), first_id + x);
+                                ukey = scr[x] ^ kFlip;
+                            sm.cand[pp][pos++] = make_ck<CK>(ukey, first_id + x);
                         }
                     } else {
                         sm.ovf[pp] = 1;
@@ -1594,7 +1651,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
         __syncwarp();
 
         // ---- outputs ----
-        group_write_outputs<2>(P, row, r, r.all, sm.q.sorted[p], s, active && (!need || !ovf));
+        group_write_outputs<2, FM>(P, row, r, r.all, sm.q.sorted[p], s, active && (!need || !ovf));
 
         // ---- rows whose candidates overflowed: the whole warp redoes them ----
         unsigned fb = __ballot_sync(kFull, s == 0 && need && ovf);
@@ -1612,10 +1669,11 @@ __global__ void __launch_bounds__(kPairWarps * 32, 5) pair_select_kernel(const K
     }
 }
 
-template <bool BF16>
-cudaError_t launch_pair(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
+template <bool BF16, int FM>
+cudaError_t launch_pair_fm(const KernelParams& P, const bsa_launch_policy_t& pol,
+                           cudaStream_t st) {
     const bool small = P.a.K - P.a.num_init - P.a.num_local <= 16;
-    auto kern = small ? pair_select_kernel<BF16, true> : pair_select_kernel<BF16, false>;
+    auto kern = small ? pair_select_kernel<BF16, true, FM> : pair_select_kernel<BF16, false, FM>;
     if (pol.smem_bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              pol.smem_bytes);
@@ -1623,6 +1681,12 @@ cudaError_t launch_pair(const KernelParams& P, const bsa_launch_policy_t& pol, c
     }
     kern<<<pol.grid, kPairWarps * 32, pol.smem_bytes, st>>>(P);
     return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_pair(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
+    return P.a.fused ? launch_pair_fm<BF16, kFusedYes>(P, pol, st)
+                     : launch_pair_fm<BF16, kFusedNo>(P, pol, st);
 }
 
 template <bool BF16, int R>

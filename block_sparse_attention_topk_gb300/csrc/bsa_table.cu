@@ -12,9 +12,14 @@
 // table; ids outside [0, cdiv(causal_len, 128)) and -1 are ignored; padded
 // rows give an empty context.
 //
-// Both kernels are tiny integer passes bound by memory latency; the table
-// builder gives one warp to each (token, head) row and deduplicates and sorts
-// the row's ids in shared memory by counting ranks (K <= 1024 ids).
+// Both kernels are tiny integer passes bound by memory latency.  For topk up
+// to 32 the table builder gives each (token, head) row a segment of 16 or 32
+// lanes, one id per lane: the block-table gather is issued as soon as the id
+// is known, and overlaps a segmented bitonic sort of (id, lane) that brings
+// duplicates together; kept ids are compacted through shared memory and each
+// lane writes one 32-byte slot of the row.  Larger topk gives one warp to a
+// row and deduplicates and sorts the ids in shared memory by counting ranks
+// (K <= 1024 ids).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -129,6 +134,104 @@ sparse_table_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t 
     }
 }
 
+// topk <= 32: G lanes per row (G = 16 for K <= 16, else 32), 32 / G rows per
+// warp.  VEC: the output table is 16-byte aligned, so each slot is written
+// with two 16-byte stores.
+constexpr int kSegWarps = 8;
+
+template <int G, bool VEC>
+__global__ void __launch_bounds__(kSegWarps * 32)
+sparse_table_seg_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t H, int32_t K,
+                        const int32_t* __restrict__ block_table, int64_t max_blocks,
+                        const int32_t* __restrict__ seq_lens, int32_t dql,
+                        int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx) {
+    constexpr int R = 32 / G;                  // rows per warp
+    constexpr int32_t kNone = 0x7FFFFFFF;      // sorts after every (id << 5 | lane)
+    __shared__ int32_t s_blk[kSegWarps][32];
+    __shared__ int32_t s_phys[kSegWarps][32];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int g = lane & (G - 1);              // lane within the row's segment
+    const int seg = lane - g;                  // first lane of the segment
+    const int width = K * kPagesPerBlock;
+    for (int64_t base = ((int64_t)blockIdx.x * kSegWarps + warp) * R; base < rows;
+         base += (int64_t)gridDim.x * kSegWarps * R) {
+        const int64_t row = base + lane / G;
+        const bool active = row < rows;
+        int64_t causal_len = 0;
+        int32_t key = kNone;
+        int32_t phys = 0;
+        if (active) {
+            const int64_t t = row / H;
+            const int64_t req = t / dql;
+            const int64_t pos = (int64_t)__ldg(seq_lens + req) - dql + (t - req * dql);
+            causal_len = pos + 1 > 0 ? pos + 1 : 0;
+            const int64_t nblk = (causal_len + kPageSize - 1) >> kLogPageSize;
+            const int64_t limit = nblk < max_blocks ? nblk : max_blocks;
+            if (g < K) {
+                const int32_t x = __ldg(topk_idx + row * K + g);
+                if (x >= 0 && x < limit) {
+                    key = (x << 5) | lane;
+                    phys = __ldg(block_table + req * max_blocks + x);
+                }
+            }
+        }
+        // ascending bitonic sort of the segment's keys; equal ids end up
+        // adjacent, ordered by lane
+#pragma unroll
+        for (int k = 2; k <= G; k <<= 1) {
+#pragma unroll
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const int32_t other = __shfl_xor_sync(kFull, key, j);
+                const bool take_min = ((g & j) == 0) == ((g & k) == 0 || k == G);
+                key = take_min ? min(key, other) : max(key, other);
+            }
+        }
+        const int32_t prev = __shfl_up_sync(kFull, key, 1);
+        const bool keep = key != kNone && (g == 0 || (prev >> 5) != (key >> 5));
+        // the gathered entry travels from the lane that loaded it
+        const int32_t got = __shfl_sync(kFull, phys, key & 31);
+        const unsigned segmask = G == 32 ? kFull : (0xFFFFu << seg);
+        const unsigned kept = __ballot_sync(kFull, keep) & segmask;
+        const int n = __popc(kept);
+        if (keep) {
+            const int rank = __popc(kept & ((1u << lane) - 1u));
+            s_blk[warp][seg + rank] = key >> 5;
+            s_phys[warp][seg + rank] = got;
+        }
+        __syncwarp();
+        int32_t contrib = 0;
+        if (active && g < K) {
+            int32_t v[8];
+            if (g < n) {
+                const int32_t b = s_blk[warp][lane];
+                const int32_t ph = s_phys[warp][lane];
+                const int64_t first = (int64_t)b * kPageSize;
+#pragma unroll
+                for (int pg = 0; pg < 8; ++pg)
+                    v[pg] = first + pg * kSubPage < causal_len ? ph * kPagesPerBlock + pg : 0;
+                const int64_t rem = causal_len - first;
+                contrib = (int32_t)(rem < kPageSize ? rem : kPageSize);
+            } else {
+#pragma unroll
+                for (int pg = 0; pg < 8; ++pg) v[pg] = 0;
+            }
+            int32_t* dst = sparse_bt + row * (int64_t)width + g * kPagesPerBlock;
+            if constexpr (VEC) {
+                reinterpret_cast<int4*>(dst)[0] = make_int4(v[0], v[1], v[2], v[3]);
+                reinterpret_cast<int4*>(dst)[1] = make_int4(v[4], v[5], v[6], v[7]);
+            } else {
+#pragma unroll
+                for (int pg = 0; pg < 8; ++pg) dst[pg] = v[pg];
+            }
+        }
+#pragma unroll
+        for (int off = G >> 1; off > 0; off >>= 1) contrib += __shfl_xor_sync(kFull, contrib, off);
+        if (active && g == 0) sparse_ctx[row] = contrib;
+        __syncwarp();
+    }
+}
+
 int grid_for(int64_t work, int per_block, int max_blocks_per_sm) {
     int64_t g = (work + per_block - 1) / per_block;
     const int64_t cap = (int64_t)device_sm_count() * max_blocks_per_sm;
@@ -162,6 +265,18 @@ cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, 
                                             int32_t* sparse_ctx, cudaStream_t stream) {
     const int64_t rows = T * H;
     if (rows == 0) return cudaSuccess;
+    if (K <= 32) {
+        const bool vec = (reinterpret_cast<uintptr_t>(sparse_bt) & 15) == 0;
+        const int per_block = kSegWarps * (K <= 16 ? 2 : 1);
+        const int grid = grid_for(rows, per_block, 8);
+        auto kern = K <= 16 ? (vec ? sparse_table_seg_kernel<16, true>
+                                   : sparse_table_seg_kernel<16, false>)
+                            : (vec ? sparse_table_seg_kernel<32, true>
+                                   : sparse_table_seg_kernel<32, false>);
+        kern<<<grid, kSegWarps * 32, 0, stream>>>(topk_idx, rows, H, K, block_table, max_blocks,
+                                                  seq_lens, dql, sparse_bt, sparse_ctx);
+        return cudaGetLastError();
+    }
     const size_t smem = (size_t)kTableWarps * 3 * K * sizeof(int32_t);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(sparse_table_kernel,

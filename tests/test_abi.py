@@ -117,7 +117,7 @@ def test_policy_capacity_and_grid(bsa):
     assert p["grid"] == 152 * 4
     g = _policy(bsa, 10**6, 1024, 16, BF)
     assert g["path"] == bsa.BSA_PATH_PAIR and g["grid"] == 152 * 5
-    # the warp fallback's buffer fits in a group warp's shared memory
+    # the overflow fallback's buffer fits in a pair warp's shared memory
     assert g["cand_capacity"] * 8 <= g["smem_bytes"] // g["warps_per_cta"]
     assert _policy(bsa, 10, 74, 16, BF)["grid"] == 1
 

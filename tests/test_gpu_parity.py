@@ -203,6 +203,50 @@ def test_select_adversarial_rows(cuda_device, bf16, M):
         _assert_equal(got, want, f"adversarial bf16={bf16} M={M} K={K}")
 
 
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("want_idx", [True, False])
+def test_fused_adversarial_rows(cuda_device, bf16, want_idx):
+    """The fused call on rows that overflow any fixed candidate list (ties,
+    NaN runs) or hold only negative scores: overflowing rows are finished by
+    the fix-up launch, which also writes their table and ctx."""
+    M = 500
+    rng = np.random.default_rng(11)
+    rows = [_adversarial_row(k, M, rng, bf16) for k in ADVERSARIAL] * 3
+    T = len(rows)
+    scores = torch.stack(rows).view(T, 1, M)
+    seq = np.full(T, M * 128, dtype=np.int32)
+    seq[len(ADVERSARIAL):2 * len(ADVERSARIAL)] -= 777        # partial last block
+    seq[2 * len(ADVERSARIAL):] = rng.integers(2000, M * 128, len(ADVERSARIAL))
+    table = synth.random_block_table(T, M, seed=5)
+    want_idx_np, want_bt, want_ctx = oracle.topk_select_sparse_table(
+        scores, seq, 1, 16, 1, 2, table.numpy())
+    dev = cuda_device
+    idx, bt, ctx = bsa.bsa_topk_select_sparse_table(
+        scores.to(dev), torch.from_numpy(seq).to(dev), 1, 16, 1, 2, table.to(dev),
+        want_idx=want_idx)
+    torch.cuda.synchronize()
+    if want_idx:
+        _assert_equal(idx.cpu().numpy(), want_idx_np, "fused adversarial idx")
+    _assert_equal(bt.cpu().numpy(), want_bt, "fused adversarial table")
+    _assert_equal(ctx.cpu().numpy(), want_ctx, "fused adversarial ctx")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_select_all_negative_long_rows(cuda_device, dtype):
+    """Long-context rows whose scores are all negative, with one planted
+    block that is the least negative: the threshold works in key space for
+    rows of any sign."""
+    w = synth.long_decode(seed=21, B=96, H=2, M=1024 if dtype == torch.bfloat16 else 512,
+                          K=16, dtype=dtype)
+    nvp = _nvp_for(w)
+    w.scores.copy_(-(w.scores.float().abs() + 0.25).to(dtype))
+    synth.fill_tail(w.scores, torch.from_numpy(nvp), float("-inf"))
+    synth.plant(w.scores, torch.from_numpy(nvp), w.plant_u, -0.01)
+    want = oracle.topk_select(w.scores, nvp, w.K, w.num_init, w.num_local)
+    got = _gpu_select(w.scores, nvp, w.K, w.num_init, w.num_local, cuda_device)
+    _assert_equal(got, want, f"all-negative rows {dtype}")
+
+
 # ---------------------------------------------------------------- layouts
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -296,7 +340,8 @@ def test_sparse_table_worked_example(cuda_device):
         assert list(bt.cpu().numpy()[r, 0]) == pref + [0] * (ex["row_width"] - len(pref))
 
 
-@pytest.mark.parametrize("H,K,dql", [(1, 16, 4), (2, 16, 1), (3, 7, 3), (1, 64, 2), (2, 300, 1)])
+@pytest.mark.parametrize("H,K,dql", [(1, 16, 4), (2, 16, 1), (3, 7, 3), (1, 64, 2), (2, 300, 1),
+                                     (2, 32, 2), (1, 13, 1), (4, 1, 1), (3, 17, 2), (1, 33, 1)])
 def test_sparse_table_random_ids(cuda_device, H, K, dql):
     """Arbitrary ids: -1, out-of-range, beyond the block table, duplicates."""
     g = torch.Generator().manual_seed(K * 31 + H)
@@ -315,6 +360,30 @@ def test_sparse_table_random_ids(cuda_device, H, K, dql):
     torch.cuda.synchronize()
     _assert_equal(bt.cpu().numpy(), want_bt, "sparse table")
     _assert_equal(ctx.cpu().numpy(), want_ctx, "sparse ctx")
+
+
+@pytest.mark.parametrize("K", [16, 32])
+def test_sparse_table_unaligned_output_and_many_rows(cuda_device, K):
+    """An output table that starts 4 bytes past a 16-byte boundary takes the
+    scalar-store form; 12000 rows span many grid strides."""
+    g = torch.Generator().manual_seed(500 + K)
+    B, H, dql, MB = 3000, 2, 2, 64
+    seq = torch.randint(0, 8200, (B,), generator=g, dtype=torch.int32)
+    T = B * dql
+    idx = torch.randint(-2, 70, (T, H, K), generator=g, dtype=torch.int32)
+    idx[:, :, 3::5] = idx[:, :, ::5][:, :, :idx[:, :, 3::5].shape[2]]
+    table = synth.random_block_table(B, MB, seed=K + 1)
+    want_bt, want_ctx = oracle.build_sparse_block_table(idx.numpy(), table.numpy(), seq.numpy(), dql)
+    n = T * H * K * 8
+    flat = torch.full((n + 1,), -7, dtype=torch.int32, device=cuda_device)
+    bt = flat[1:].view(T, H, K * 8)
+    assert bt.data_ptr() % 16 == 4
+    _, ctx = bsa.bsa_build_sparse_block_table(idx.to(cuda_device), table.to(cuda_device),
+                                              seq.to(cuda_device), dql, sparse_bt=bt)
+    torch.cuda.synchronize()
+    _assert_equal(bt.cpu().numpy(), want_bt, "sparse table (unaligned)")
+    _assert_equal(ctx.cpu().numpy(), want_ctx, "sparse ctx")
+    assert int(flat[0].item()) == -7
 
 
 @pytest.mark.parametrize("variant", ["as_given", "dql1_h2", "fp32_small_table", "no_idx"])
