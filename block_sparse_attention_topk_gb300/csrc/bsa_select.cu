@@ -1422,6 +1422,33 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
             }
             sm.a.vmax[p][s][j] = (int16_t)vm;
         };
+        // Step 0 splits each chunk finer, into 8 subsets spread over the
+        // four classes, so that a short row (a few chunks) still has at least
+        // K' representatives and a tight theta.
+        auto take_first = [&](const uint32_t (&w)[8], int c) {
+            int32_t vm;
+            if constexpr (BF16) {
+                const uint32_t a0 = max_s16x2(w[0], w[4]), a1 = max_s16x2(w[2], w[6]);
+                const uint32_t b0 = max_s16x2(w[1], w[5]), b1 = max_s16x2(w[3], w[7]);
+                rp[2 * c] = max_s16x2(rp[2 * c], a0);
+                rp[2 * c + 1] = max_s16x2(rp[2 * c + 1], b0);
+                rp[2 * c + 4] = max_s16x2(rp[2 * c + 4], a1);
+                rp[2 * c + 5] = max_s16x2(rp[2 * c + 5], b1);
+                const uint32_t mm = max_s16x2(max_s16x2(a0, a1), max_s16x2(b0, b1));
+                vm = max(E::pack_lo(mm), E::pack_hi(mm));
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    rq[c * 4 + jj] = max(rq[c * 4 + jj], (int32_t)w[jj]);
+                    rq[(c + 2) * 4 + jj] = max(rq[(c + 2) * 4 + jj], (int32_t)w[jj + 4]);
+                }
+                int32_t m = (int32_t)w[0];
+#pragma unroll
+                for (int jj = 1; jj < 8; ++jj) m = max(m, (int32_t)w[jj]);
+                vm = m >> 16;
+            }
+            sm.a.vmax[p][s][c] = (int16_t)vm;
+        };
         const int nsteps = need ? (nchunk + 3) >> 2 : 0;
         // step 0 and the last step hold the row's edge chunks: masked loads
         auto edge_step = [&](int i, int cls0) {
@@ -1431,7 +1458,10 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                 if (k < nchunk) {
                     uint32_t w[8];
                     pair_load_edge<BF16>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
-                    take(w, 2 * i + c, cls0 + c);
+                    if (i == 0)
+                        take_first(w, c);
+                    else
+                        take(w, 2 * i + c, cls0 + c);
                 }
             }
         };
