@@ -1275,6 +1275,24 @@ __device__ __forceinline__ void pair_load_edge(const KernelParams& P, int k, uin
     }
 }
 
+// One bit per int16 half of NW packed words: bit e set when half e >= t
+// (signed), for t > -32768.  max.s16x2(x, t - 1) differs from t - 1 iff x >= t.
+template <int NW>
+__device__ __forceinline__ uint32_t ge_bits16(const uint32_t (&w)[NW], int32_t t) {
+    const uint32_t t2 = ((uint32_t)(t - 1) & 0xFFFFu) * 0x10001u;
+    uint32_t b[NW];
+#pragma unroll
+    for (int x = 0; x < NW; ++x) b[x] = min_u16x2(max_s16x2(w[x], t2) ^ t2, 0x00010001u);
+    uint32_t bits = 0;
+#pragma unroll
+    for (int x = 0; x < NW; x += 2) {
+        // bytes: halves 2x, 2x+1, 2x+2, 2x+3 as 0/1, folded into 4 bits
+        const uint32_t v4 = __byte_perm(b[x], b[x + 1], 0x6420);
+        bits |= ((v4 * 0x01020408u) >> 24) << (2 * x);
+    }
+    return bits;
+}
+
 // Bitonic sort, descending, of the 32 values a lane pair holds: lane s keeps
 // positions 16 s .. 16 s + 15 in x[0..15].  Every lane of the warp calls it.
 template <typename T>
@@ -1337,10 +1355,6 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
     using G = PairSmem<CK>;
     constexpr int S = E::kBytes;
     constexpr int CE = 32 / S;                 // elements per 32-byte chunk
-    // theta is searched in offset binary (key + 2^15 / 2^31), top bit first;
-    // bits below kLow stay 0, which only lowers the bound
-    constexpr int kTop = BF16 ? 15 : 31;
-    constexpr int kLow = BF16 ? 3 : 19;
     constexpr uint32_t kFlip = BF16 ? 0x8000u : 0x80000000u;  // signed key -> unsigned key
     constexpr uint32_t kLowMax = BF16 ? 0xFFFFu : 0xFFFFFFFFu;
     constexpr int32_t kKeyMin = BF16 ? -32768 : INT32_MIN;
@@ -1503,8 +1517,8 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         }
         if (nsteps >= 2) edge_step(nsteps - 1, 2);
 
-        // ---- theta: a lower bound on the K'-th largest of the row's 32
-        // representatives (distinct elements), on a grid of 2^kLow ----
+        // ---- theta: the K'-th largest of the row's 32 representatives (distinct
+        // elements), a lower bound on the K'-th best score ----
         int32_t rep[16];
         if constexpr (BF16) {
 #pragma unroll
@@ -1516,19 +1530,15 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
 #pragma unroll
             for (int x = 0; x < 16; ++x) rep[x] = rq[x];
         }
-        uint32_t tu = 0;
-        for (int bit = kTop; bit >= kLow; --bit) {
-            const uint32_t cand = tu | (1u << bit);
-            const int32_t tt = BF16 ? (int32_t)cand - 0x8000 : (int32_t)(cand ^ 0x80000000u);
-            int c = 0;
-#pragma unroll
-            for (int x = 0; x < 16; ++x) c += rep[x] >= tt ? 1 : 0;
-            c += __shfl_xor_sync(kFull, c, 1);
-            if (c >= r.kp) tu = cand;
-        }
-        // fewer than K' representatives in the row: tu == 0, every element
-        // of [lo, hi) is a candidate
-        const int32_t theta = BF16 ? (int32_t)tu - 0x8000 : (int32_t)(tu ^ 0x80000000u);
+        // bitonic sort of the pair's 32 representatives; the K'-th largest is
+        // position K' - 1 (lane 0 holds positions 0..15).  A row with fewer
+        // than K' representatives gets the smallest key: every element of
+        // [lo, hi) is then a candidate.
+        pair_sort32_desc<int32_t>(rep, s);
+        const int want = max(r.kp - 1, 0);
+        const int32_t mine = pick(rep, want & 15);
+        const int32_t other = __shfl_xor_sync(kFull, mine, 1);
+        const int32_t theta = ((want < 16) == (s == 0)) ? mine : other;
         if (s == 0) {
             sm.ccount[p] = 0;
             sm.ovf[p] = 0;
@@ -1546,20 +1556,17 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         const int32_t th16 = BF16 ? theta : (theta >> 16);
 
         // ---- queue the chunks that can hold candidates ----
-        // lane-local entry j holds chunk 4 (j >> 1) + 2 s + (j & 1)
-        const int my_n = need ? 2 * nsteps : 0;
+        // lane-local entry j holds chunk 4 (j >> 1) + 2 s + (j & 1); the
+        // entries below jmax exist.  Eight chunk maxima per packed compare.
+        const int jmax = need ? 2 * (nchunk >> 2) + min(max((nchunk & 3) - 2 * s, 0), 2) : 0;
         unsigned long long hot = 0;
-        for (int i0 = 0; i0 < my_n; i0 += 8) {
+        for (int i0 = 0; i0 < jmax; i0 += 8) {
             const uint4 pk = *reinterpret_cast<const uint4*>(&sm.a.vmax[p][s][i0]);
             const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = i0 + u;
-                const int k = 4 * (j >> 1) + 2 * s + (j & 1);
-                const int32_t vm = (int32_t)(int16_t)(uint16_t)(wv[u >> 1] >> ((u & 1) * 16));
-                if (j < my_n && k < nchunk && vm >= th16) hot |= 1ull << j;
-            }
+            const uint32_t bits = th16 == -32768 ? 0xFFu : ge_bits16<4>(wv, th16);
+            hot |= (unsigned long long)bits << i0;
         }
+        hot &= (1ull << jmax) - 1ull;
         int qtotal;
         int qpos = warp_excl_scan(__popcll(hot), lane, qtotal);
         while (hot) {
@@ -1598,20 +1605,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                 uint32_t m = ((1u << hi_e) - 1u) & ~((1u << lo_e) - 1u);
                 if (d.theta != kKeyMin) {
                     if constexpr (BF16) {
-                        // per half: 1 if key >= theta (signed), gathered into 16 bits
-                        const uint32_t t2 = ((uint32_t)(d.theta - 1) & 0xFFFFu) * 0x10001u;
-                        uint32_t b[8];
-#pragma unroll
-                        for (int x = 0; x < 8; ++x)
-                            b[x] = min_u16x2(max_s16x2(w[x], t2) ^ t2, 0x00010001u);
-                        uint32_t bits = 0;
-#pragma unroll
-                        for (int x = 0; x < 8; x += 2) {
-                            // bytes: element 2x, 2x+1, 2x+2, 2x+3 as 0/1
-                            const uint32_t v4 = __byte_perm(b[x], b[x + 1], 0x6420);
-                            bits |= ((v4 * 0x01020408u) >> 24) << (2 * x);
-                        }
-                        m &= bits;
+                        m &= ge_bits16<8>(w, d.theta);
                     } else {
                         uint32_t bits = 0;
 #pragma unroll
