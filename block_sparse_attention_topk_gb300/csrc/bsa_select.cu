@@ -1484,35 +1484,31 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         // step's two chunks are loaded while the current one is reduced
         const int i_last = nsteps >= 2 ? (nchunk - 5) / 4 : 0;
         if (i_last >= 1) {
-            uint32_t w0[8], w1[8];
+            // ping-pong between buffers A and B: odd steps in A, even in B
+            uint32_t a0[8], a1[8], b0[8], b1[8];
             uintptr_t ad = c0 + ((uintptr_t)(4 + 2 * s) << 5);
-            ld32(ad, w0);
-            ld32(ad + 32, w1);
+            ld32(ad, a0);
+            ld32(ad + 32, a1);
             for (int i = 1; i <= i_last; i += 2) {
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int ii = i + u;
-                    if (ii <= i_last) {
-                        uint32_t n0[8], n1[8];
-                        const bool more = ii < i_last;
-                        if (more) {
-                            ad += 128;
-                            ld32(ad, n0);
-                            ld32(ad + 32, n1);
-                        }
-                        chunk_to_keys<BF16>(w0);
-                        take(w0, 2 * ii, 2 * u);
-                        chunk_to_keys<BF16>(w1);
-                        take(w1, 2 * ii + 1, 2 * u + 1);
-                        if (more) {
-#pragma unroll
-                            for (int x = 0; x < 8; ++x) {
-                                w0[x] = n0[x];
-                                w1[x] = n1[x];
-                            }
-                        }
-                    }
+                if (i < i_last) {
+                    ld32(ad + 128, b0);
+                    ld32(ad + 160, b1);
                 }
+                chunk_to_keys<BF16>(a0);
+                take(a0, 2 * i, 0);
+                chunk_to_keys<BF16>(a1);
+                take(a1, 2 * i + 1, 1);
+                if (i < i_last) {
+                    if (i + 1 < i_last) {
+                        ld32(ad + 256, a0);
+                        ld32(ad + 288, a1);
+                    }
+                    chunk_to_keys<BF16>(b0);
+                    take(b0, 2 * i + 2, 2);
+                    chunk_to_keys<BF16>(b1);
+                    take(b1, 2 * i + 3, 3);
+                }
+                ad += 256;
             }
         }
         if (nsteps >= 2) edge_step(nsteps - 1, 2);
@@ -1594,10 +1590,12 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                 const uintptr_t addr = (uintptr_t)d.c0 + ((uintptr_t)k << 5);
                 if (addr >= P.buf_lo && addr + 32 <= P.buf_hi) {
                     ld32(addr, w);
-                    chunk_to_keys<BF16>(w);
+                    // against theta >= 0, raw signed order is key order
+                    if (d.theta < 0) chunk_to_keys<BF16>(w);
                 } else {
                     pair_load_edge<BF16>(P, k, (uintptr_t)d.c0, d.base_id, d.lo, d.hi,
                                          reinterpret_cast<const char*>(d.row_ptr), w);
+                    if (d.theta >= 0) chunk_to_keys<BF16>(w);  // back to raw bits
                 }
                 const int first_id = d.base_id + k * CE;
                 const int lo_e = min(max(d.lo - first_id, 0), CE);
