@@ -1348,6 +1348,31 @@ __device__ __forceinline__ void lane_sort16_desc(T (&x)[16]) {
     }
 }
 
+// The 16 largest of the 32 values a lane pair holds, descending, in lane 0's
+// x[0..15] (lane 1's registers end up unspecified).  Each lane sorts its 16;
+// lane 0 then keeps max(a[r], b[15 - r]) of its list a and the partner's list
+// b, a bitonic sequence holding the top 16, and merges it.
+template <typename T>
+__device__ __forceinline__ void pair_top16_desc(T (&x)[16]) {
+    lane_sort16_desc<T>(x);
+    T y[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) y[r] = shfl_xor_any(x[15 - r], 1);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) x[r] = x[r] > y[r] ? x[r] : y[r];
+#pragma unroll
+    for (int j = 8; j > 0; j >>= 1) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            if ((r & j) == 0) {
+                const T a = x[r], b = x[r | j];
+                x[r] = a > b ? a : b;
+                x[r | j] = a > b ? b : a;
+            }
+        }
+    }
+}
+
 template <bool BF16, bool SMALLK, int FM>
 __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel(const KernelParams P) {
     using E = Elem<BF16>;
@@ -1530,11 +1555,18 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         // position K' - 1 (lane 0 holds positions 0..15).  A row with fewer
         // than K' representatives gets the smallest key: every element of
         // [lo, hi) is then a candidate.
-        pair_sort32_desc<int32_t>(rep, s);
         const int want = max(r.kp - 1, 0);
-        const int32_t mine = pick(rep, want & 15);
-        const int32_t other = __shfl_xor_sync(kFull, mine, 1);
-        const int32_t theta = ((want < 16) == (s == 0)) ? mine : other;
+        int32_t theta;
+        if constexpr (SMALLK) {
+            // K' <= 16: the top 16 suffice, in lane 0
+            pair_top16_desc<int32_t>(rep);
+            theta = __shfl_sync(kFull, pick(rep, want), lane & ~1);
+        } else {
+            pair_sort32_desc<int32_t>(rep, s);
+            const int32_t mine = pick(rep, want & 15);
+            const int32_t other = __shfl_xor_sync(kFull, mine, 1);
+            theta = ((want < 16) == (s == 0)) ? mine : other;
+        }
         if (s == 0) {
             sm.ccount[p] = 0;
             sm.ovf[p] = 0;
@@ -1646,7 +1678,10 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
             const int pos = s * 16 + u;
             x[u] = (sel_ok && pos < cn) ? sm.cand[p][pos] : (CK)0;
         }
-        pair_sort32_desc<CK>(x, s);
+        if constexpr (SMALLK)
+            pair_top16_desc<CK>(x);
+        else
+            pair_sort32_desc<CK>(x, s);
         __syncwarp();
         if constexpr (SMALLK) {
             // K' <= 16: the kept positions are lane 0's registers
