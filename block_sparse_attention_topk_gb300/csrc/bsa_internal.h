@@ -62,7 +62,8 @@ struct PairRowDesc {
     unsigned long long c0;       // first 32-byte chunk of the non-forced range
     unsigned long long row_ptr;  // address of element 0 of the row
     int32_t base_id, lo, hi, theta;
-    int32_t nchunk, pad;
+    int32_t nchunk;
+    int32_t inside;              // every chunk of the range lies inside the score buffer
 };
 
 template <typename CK>
@@ -101,7 +102,19 @@ struct SelectArgs {
     int32_t* sparse_bt;
     int32_t* sparse_ctx;
     bool fused;
+    // x / H and x / dql for x < 2^31 as (umulhi(x, mul) + x) >> shift
+    uint32_t h_mul, h_shift, dql_mul, dql_shift;
 };
+
+// Multiplier and shift that divide every x < 2^31 by d >= 1 exactly as
+// (umulhi(x, mul) + x) >> shift (round-up reciprocal, Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994).
+inline void div_magic(uint32_t d, uint32_t* mul, uint32_t* shift) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    *mul = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+    *shift = l;
+}
 
 // Workspace carve-up for the split path (all offsets 256-byte aligned).
 struct SplitWorkspace {

@@ -354,25 +354,30 @@ __device__ __forceinline__ bool is_fused(const SelectArgs& a) {
 
 // The per-row metadata word: num_valid_pages[t] (select) or seq_lens[req]
 // (fused).  Split from row_info so the group path can load it one item early.
+// x / d for x < 2^31 with the host's multiplier (see div_magic).
+__device__ __forceinline__ uint32_t div_u31(uint32_t x, uint32_t mul, uint32_t shift) {
+    return (__umulhi(x, mul) + x) >> shift;
+}
+
 template <int FM = kFusedRuntime>
 __device__ __forceinline__ int32_t row_meta(const SelectArgs& a, int64_t row) {
-    // rows < 2^31 (checked on the host): 32-bit division is exact
-    const uint32_t t32 = (uint32_t)row / (uint32_t)a.H;
-    if (is_fused<FM>(a)) return __ldg(a.seq_lens + t32 / (uint32_t)a.dql);
+    // rows < 2^31 (checked on the host)
+    const uint32_t t32 = div_u31((uint32_t)row, a.h_mul, a.h_shift);
+    if (is_fused<FM>(a)) return __ldg(a.seq_lens + div_u31(t32, a.dql_mul, a.dql_shift));
     return __ldg(a.num_valid_pages + t32);
 }
 
 template <int FM = kFusedRuntime>
 __device__ __forceinline__ RowInfo row_info_from(const SelectArgs& a, int64_t row, int32_t meta) {
     RowInfo r;
-    const uint32_t t32 = (uint32_t)row / (uint32_t)a.H;
+    const uint32_t t32 = div_u31((uint32_t)row, a.h_mul, a.h_shift);
     r.t = (int32_t)t32;
     r.h = (int32_t)((uint32_t)row - t32 * (uint32_t)a.H);
     int64_t pages;
     r.causal_len = 0;
     r.req = 0;
     if (is_fused<FM>(a)) {
-        const uint32_t req32 = t32 / (uint32_t)a.dql;
+        const uint32_t req32 = div_u31(t32, a.dql_mul, a.dql_shift);
         r.req = (int32_t)req32;
         const int32_t lq = (int32_t)(t32 - req32 * (uint32_t)a.dql);
         const int64_t pos = (int64_t)meta - a.dql + lq;
@@ -1293,6 +1298,20 @@ __device__ __forceinline__ uint32_t ge_bits16(const uint32_t (&w)[NW], int32_t t
     return bits;
 }
 
+// ge_bits16<8> with the bits in another order: bit x (x < 8) is element 2x
+// and bit 8 + x is element 2x + 1 of the chunk; shifts and adds replace the
+// byte gathers.
+__device__ __forceinline__ uint32_t ge_bits16_perm(const uint32_t (&w)[8], int32_t t) {
+    const uint32_t t2 = ((uint32_t)(t - 1) & 0xFFFFu) * 0x10001u;
+    uint32_t c = 0;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) c += min_u16x2(max_s16x2(w[x], t2) ^ t2, 0x00010001u) << x;
+    return (c & 0xFFu) | ((c >> 8) & 0xFF00u);
+}
+
+// Element of a bf16 chunk named by bit b of ge_bits16_perm.
+__device__ __forceinline__ int perm_elem(int b) { return ((b & 7) << 1) | (b >> 3); }
+
 // Bitonic sort, descending, of the 32 values a lane pair holds: lane s keeps
 // positions 16 s .. 16 s + 15 in x[0..15].  Every lane of the warp calls it.
 template <typename T>
@@ -1578,7 +1597,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
             d.hi = r.hi;
             d.theta = theta;
             d.nchunk = nchunk;
-            d.pad = 0;
+            d.inside = (c0 >= P.buf_lo && c0 + ((uintptr_t)nchunk << 5) <= P.buf_hi) ? 1 : 0;
             sm.desc[p] = d;
         }
         const int32_t th16 = BF16 ? theta : (theta >> 16);
@@ -1620,7 +1639,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                 const PairRowDesc d = sm.desc[pp];
                 uint32_t w[8];
                 const uintptr_t addr = (uintptr_t)d.c0 + ((uintptr_t)k << 5);
-                if (addr >= P.buf_lo && addr + 32 <= P.buf_hi) {
+                if (d.inside || (addr >= P.buf_lo && addr + 32 <= P.buf_hi)) {
                     ld32(addr, w);
                     // against theta >= 0, raw signed order is key order
                     if (d.theta < 0) chunk_to_keys<BF16>(w);
@@ -1630,12 +1649,23 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                     if (d.theta >= 0) chunk_to_keys<BF16>(w);  // back to raw bits
                 }
                 const int first_id = d.base_id + k * CE;
-                const int lo_e = min(max(d.lo - first_id, 0), CE);
-                const int hi_e = min(max(d.hi - first_id, 0), CE);
-                uint32_t m = ((1u << hi_e) - 1u) & ~((1u << lo_e) - 1u);
+                // bf16 masks use the ge_bits16_perm order
+                uint32_t m = BF16 ? 0xFFFFu : 0xFFu;
+                if (k == 0 || k == d.nchunk - 1) {
+                    // an edge chunk: cut ids outside [lo, hi)
+                    const int lo_e = min(max(d.lo - first_id, 0), CE);
+                    const int hi_e = min(max(d.hi - first_id, 0), CE);
+                    if constexpr (BF16) {
+                        auto range = [](int a, int b) { return ((1u << b) - 1u) & ~((1u << a) - 1u); };
+                        m = range((lo_e + 1) >> 1, (hi_e + 1) >> 1) |
+                            (range(lo_e >> 1, hi_e >> 1) << 8);
+                    } else {
+                        m = ((1u << hi_e) - 1u) & ~((1u << lo_e) - 1u);
+                    }
+                }
                 if (d.theta != kKeyMin) {
                     if constexpr (BF16) {
-                        m &= ge_bits16<8>(w, d.theta);
+                        m &= ge_bits16_perm(w, d.theta);
                     } else {
                         uint32_t bits = 0;
 #pragma unroll
@@ -1651,8 +1681,9 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
 #pragma unroll
                         for (int x = 0; x < 8; ++x) scr[x] = w[x];
                         while (m) {
-                            const int x = __ffs(m) - 1;
+                            const int b = __ffs(m) - 1;
                             m &= m - 1;
+                            const int x = BF16 ? perm_elem(b) : b;
                             uint32_t ukey;
                             if constexpr (BF16)
                                 ukey = ((uint32_t)reinterpret_cast<const uint16_t*>(scr)[x]) ^ kFlip;
@@ -1803,6 +1834,8 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
                           const SplitWorkspace& ws, cudaStream_t stream) {
     KernelParams P;
     P.a = a;
+    div_magic((uint32_t)(a.H > 0 ? a.H : 1), &P.a.h_mul, &P.a.h_shift);
+    div_magic((uint32_t)(a.dql > 0 ? a.dql : 1), &P.a.dql_mul, &P.a.dql_shift);
     P.ws = Split{ws.keys, ws.ids, ws.counts, ws.tickets};
     P.chunks_per_row = pol.chunks_per_row;
     P.cap = pol.cand_capacity;
