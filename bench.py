@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--requests", type=int, default=131072)
     p.add_argument("--topk", type=int, default=16)
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-chunks", type=int, default=8)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true")
@@ -301,7 +302,7 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, table, device, stream, rows)
+        e2e = run_e2e(args, w, table, device, stream, rows, expect=(out_idx, sparse_ctx))
         e2e["value"] = sum_over_ranks(e2e["value"], world) if world > 1 else e2e["value"]
 
     result = {
@@ -341,10 +342,13 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, table, device, stream, rows):
+def run_e2e(args, w, table, device, stream, rows, expect=None):
     """Host buffers in, host buffers out, through the same C-ABI call: the
     timed region holds the H2D copies of scores, seq_lens and block table,
-    the fused call, and the D2H copies of ids, table and ctx."""
+    the fused call, and the D2H copies of ids, table and ctx.  The step is
+    pipelined over request chunks on three streams (upload, compute,
+    download), so a chunk's outputs come back while later inputs still go
+    up; one step finishes before the next begins."""
     import block_sparse_attention_topk_gb300 as bsa
     K, I, L = w.K, w.num_init, w.num_local
     h_scores = w.scores.cpu().pin_memory()
@@ -359,16 +363,38 @@ def run_e2e(args, w, table, device, stream, rows):
     d_idx = torch.empty((w.T, w.H, K), dtype=torch.int32, device=device)
     d_bt = torch.empty((w.T, w.H, K * 8), dtype=torch.int32, device=device)
     d_ctx = torch.empty((w.T, w.H), dtype=torch.int32, device=device)
+    C = max(1, min(args.e2e_chunks, w.B))
+    bounds = [(w.B * c // C, w.B * (c + 1) // C) for c in range(C)]
+    up, comp, down = (torch.cuda.Stream(device) for _ in range(3))
 
     def one():
-        d_scores.copy_(h_scores, non_blocking=True)
-        d_seq.copy_(h_seq, non_blocking=True)
-        d_table.copy_(h_table, non_blocking=True)
-        bsa.bsa_topk_select_sparse_table(d_scores, d_seq, w.dql, K, I, L, d_table,
-                                         out_idx=d_idx, sparse_bt=d_bt, sparse_ctx=d_ctx)
-        h_idx.copy_(d_idx, non_blocking=True)
-        h_bt.copy_(d_bt, non_blocking=True)
-        h_ctx.copy_(d_ctx, non_blocking=True)
+        start = torch.cuda.Event()
+        start.record(stream)
+        for st in (up, comp, down):
+            st.wait_event(start)
+        for r0, r1 in bounds:
+            t0, t1 = r0 * w.dql, r1 * w.dql
+            with torch.cuda.stream(up):
+                d_scores[t0:t1].copy_(h_scores[t0:t1], non_blocking=True)
+                d_seq[r0:r1].copy_(h_seq[r0:r1], non_blocking=True)
+                d_table[r0:r1].copy_(h_table[r0:r1], non_blocking=True)
+                e_up = torch.cuda.Event()
+                e_up.record(up)
+            comp.wait_event(e_up)
+            with torch.cuda.stream(comp):
+                bsa.bsa_topk_select_sparse_table(d_scores[t0:t1], d_seq[r0:r1], w.dql, K, I, L,
+                                                 d_table[r0:r1], out_idx=d_idx[t0:t1],
+                                                 sparse_bt=d_bt[t0:t1], sparse_ctx=d_ctx[t0:t1])
+                e_c = torch.cuda.Event()
+                e_c.record(comp)
+            down.wait_event(e_c)
+            with torch.cuda.stream(down):
+                h_idx[t0:t1].copy_(d_idx[t0:t1], non_blocking=True)
+                h_bt[t0:t1].copy_(d_bt[t0:t1], non_blocking=True)
+                h_ctx[t0:t1].copy_(d_ctx[t0:t1], non_blocking=True)
+        e_d = torch.cuda.Event()
+        e_d.record(down)
+        stream.wait_event(e_d)
 
     for _ in range(2):
         one()
@@ -380,11 +406,15 @@ def run_e2e(args, w, table, device, stream, rows):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.e2e_steps
+    if expect is not None:
+        # the pipelined step returns what the device-resident step computed
+        if not (torch.equal(h_idx, expect[0].cpu()) and torch.equal(h_ctx, expect[1].cpu())):
+            raise RuntimeError("end-to-end outputs differ from the device-resident run")
     h2d = h_scores.numel() * h_scores.element_size() + h_seq.numel() * 4 + h_table.numel() * 4
     d2h = (h_idx.numel() + h_bt.numel() + h_ctx.numel()) * 4
     return {"value": rows / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": args.e2e_steps}
+            "steps": args.e2e_steps, "chunks": C, "kernel_launches_per_step": C}
 
 
 def config_latencies(device):
