@@ -820,6 +820,13 @@ __device__ __forceinline__ T pick(const T (&x)[N], int idx) {
     return v;
 }
 
+// One 256-bit store of eight int32 (a full 32-byte sector); p 32-byte aligned.
+__device__ __forceinline__ void st_v8(int32_t* p, const int32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,
                                              const int32_t* sorted) {
     if (all || j < r.lo) return j;
@@ -829,7 +836,7 @@ __device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,
 
 // Outputs of one row by its LANES lanes: lane q owns a contiguous run of
 // output slots (= blocks): it writes their ids, their 8 table entries each
-// (two 16-byte stores) and their part of ctx.  Every lane of the warp calls
+// (one 32-byte store) and their part of ctx.  Every lane of the warp calls
 // this (ctx is summed with shuffles inside each row's lanes); `write` masks
 // the stores.
 template <int LANES, int FM = kFusedRuntime>
@@ -844,7 +851,7 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
         const int width = K * kPagesPerBlock;
         int32_t* bt = fused ? a.sparse_bt + row * (int64_t)width : nullptr;
         const int32_t* table = fused ? a.block_table + (int64_t)r.req * a.max_blocks : nullptr;
-        const bool vec_ok = ((reinterpret_cast<uintptr_t>(bt)) & 15) == 0;
+        const bool vec_ok = ((reinterpret_cast<uintptr_t>(bt)) & 31) == 0;  // 32-byte slots
         // lane q owns the contiguous slots [q * per, q * per + per); 8 at a
         // time: ids first, then all table gathers in flight together, then
         // the stores
@@ -893,8 +900,7 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
                 }
                 int32_t* dst = bt + 8 * j;
                 if (vec_ok) {
-                    reinterpret_cast<int4*>(dst)[0] = make_int4(v[0], v[1], v[2], v[3]);
-                    reinterpret_cast<int4*>(dst)[1] = make_int4(v[4], v[5], v[6], v[7]);
+                    st_v8(dst, v);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) dst[e] = v[e];

@@ -419,6 +419,33 @@ def test_fused_select_sparse_table(cuda_device, variant):
     _assert_equal(c2.cpu().numpy(), want_ctx, "unfused ctx")
 
 
+@pytest.mark.parametrize("offset_words", [1, 4])
+def test_fused_table_output_off_32_byte_boundary(cuda_device, offset_words):
+    """The fused call writes 32-byte table slots with one 256-bit store when
+    the table is 32-byte aligned; tables 4 or 16 bytes past a boundary take
+    the element-wise path and give the same result."""
+    w = synth.fused_table(B=96, dql=2, H=2, M=300)
+    table = w.block_table
+    nvp = _prep(w)
+    want_idx, want_bt, want_ctx = oracle.topk_select_sparse_table(
+        w.scores, w.seq_lens.numpy(), w.dql, w.K, w.num_init, w.num_local, table.numpy())
+    dev = cuda_device
+    T, H, K = w.T, w.H, w.K
+    flat = torch.full((T * H * K * 8 + 8,), -9, dtype=torch.int32, device=dev)
+    bt = flat[offset_words:offset_words + T * H * K * 8].view(T, H, K * 8)
+    assert bt.data_ptr() % 32 == 4 * offset_words
+    idx, bt_out, ctx = bsa.bsa_topk_select_sparse_table(
+        w.scores.to(dev), w.seq_lens.to(dev), w.dql, K, w.num_init, w.num_local, table.to(dev),
+        sparse_bt=bt)
+    torch.cuda.synchronize()
+    assert bt_out.data_ptr() == bt.data_ptr()
+    _assert_equal(idx.cpu().numpy(), want_idx, "fused idx (offset table)")
+    _assert_equal(bt.cpu().numpy(), want_bt, "fused table (offset)")
+    _assert_equal(ctx.cpu().numpy(), want_ctx, "fused ctx (offset table)")
+    assert int(flat[0].item()) == -9 and int(flat[-1].item()) == -9
+    del nvp
+
+
 def test_fused_long_rows_split(cuda_device):
     """Fused path on few long rows (split + merge + table epilogue)."""
     w = synth.fused_table(B=8, dql=2, H=2, M=8192, max_len=8192 * 128)
