@@ -834,9 +834,10 @@ __device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,
     return r.hi + (j - r.lo - r.kp);
 }
 
-// Outputs of one row by its LANES lanes: lane q owns a contiguous run of
-// output slots (= blocks): it writes their ids, their 8 table entries each
-// (one 32-byte store) and their part of ctx.  Every lane of the warp calls
+// Outputs of one row by its LANES lanes: lane q owns the output slots (=
+// blocks) q, q + LANES, q + 2 LANES, ..., so that at each step the row's lanes
+// write adjacent 32-byte table slots; it writes their ids, their 8 table
+// entries each (one 32-byte store) and their part of ctx.  Every lane of the warp calls
 // this (ctx is summed with shuffles inside each row's lanes); `write` masks
 // the stores.
 template <int LANES, int FM = kFusedRuntime>
@@ -852,19 +853,16 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
         int32_t* bt = fused ? a.sparse_bt + row * (int64_t)width : nullptr;
         const int32_t* table = fused ? a.block_table + (int64_t)r.req * a.max_blocks : nullptr;
         const bool vec_ok = ((reinterpret_cast<uintptr_t>(bt)) & 31) == 0;  // 32-byte slots
-        // lane q owns the contiguous slots [q * per, q * per + per); 8 at a
-        // time: ids first, then all table gathers in flight together, then
-        // the stores
+        // 8 slots at a time: ids first, then all table gathers in flight
+        // together, then the stores
         const int per = (K + LANES - 1) / LANES;
-        const int jbeg = q * per;
-        const int jend = min(K, jbeg + per);
-        for (int j0 = jbeg; j0 < jend; j0 += 8) {
+        for (int u0 = 0; u0 < per; u0 += 8) {
             int32_t bs[8], phys[8];
             bool okb[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int j = j0 + u;
-                bs[u] = (j < jend && j < r.n) ? group_sel(j, r, all, sorted) : -1;
+                const int j = q + LANES * (u0 + u);
+                bs[u] = (j < K && j < r.n) ? group_sel(j, r, all, sorted) : -1;
                 okb[u] = bt != nullptr && bs[u] >= 0 && bs[u] < a.max_blocks;
                 phys[u] = 0;
             }
@@ -872,25 +870,19 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
             for (int u = 0; u < 8; ++u)
                 if (okb[u]) phys[u] = __ldg(table + bs[u]);
             if (out != nullptr) {
-                const bool ovec = j0 + 8 <= jend &&
-                                  ((reinterpret_cast<uintptr_t>(out + j0)) & 15) == 0;
-                if (ovec) {
-                    reinterpret_cast<int4*>(out + j0)[0] = make_int4(bs[0], bs[1], bs[2], bs[3]);
-                    reinterpret_cast<int4*>(out + j0)[1] = make_int4(bs[4], bs[5], bs[6], bs[7]);
-                } else {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (j0 + u < jend) out[j0 + u] = bs[u];
+                for (int u = 0; u < 8; ++u) {
+                    const int j = q + LANES * (u0 + u);
+                    if (j < K) out[j] = bs[u];
                 }
             }
             if (bt == nullptr) continue;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int j = j0 + u;
-                if (j >= jend) break;
+                const int j = q + LANES * (u0 + u);
+                if (j >= K) break;
                 int v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                 if (okb[u]) {
-                    // tokens of this block inside the causal prefix (b < v <= pages, so >= 1)
                     const int rem = (int)min(r.causal_len - (int64_t)bs[u] * kPageSize,
                                              (int64_t)kPageSize);
                     const int32_t phys8 = phys[u] * kPagesPerBlock;
