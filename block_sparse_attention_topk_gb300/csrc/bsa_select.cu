@@ -1261,10 +1261,20 @@ __device__ __forceinline__ void pair_load_edge(const KernelParams& P, int k, uin
     if (addr >= P.buf_lo && addr + 32 <= P.buf_hi) {
         ld32(addr, w);
         chunk_to_keys<BF16>(w);
+        const int d0 = base_id + k * CE - lo;   // first id of the chunk, relative to lo
+        const uint32_t span = (uint32_t)(hi - lo);
+        if (d0 < 0 || (uint32_t)(d0 + CE) > span) {
+            // element e is kept iff 0 <= d0 + e < hi - lo; one mask word per word
 #pragma unroll
-        for (int e = 0; e < CE; ++e) {
-            const int id = base_id + k * CE + e;
-            if (id < lo || id >= hi) chunk_set<BF16>(w, e, (int32_t)E::kMaskWord);
+            for (int x = 0; x < 8; ++x) {
+                if constexpr (BF16) {
+                    const uint32_t keep = ((uint32_t)(d0 + 2 * x) < span ? 0x0000FFFFu : 0u) |
+                                          ((uint32_t)(d0 + 2 * x + 1) < span ? 0xFFFF0000u : 0u);
+                    w[x] = (w[x] & keep) | (E::kMaskWord & ~keep);
+                } else {
+                    if ((uint32_t)(d0 + x) >= span) w[x] = E::kMaskWord;
+                }
+            }
         }
     } else {
 #pragma unroll
@@ -1614,10 +1624,20 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         hot &= (1ull << jmax) - 1ull;
         int qtotal;
         int qpos = warp_excl_scan(__popcll(hot), lane, qtotal);
-        while (hot) {
-            const int j = __ffsll((long long)hot) - 1;
-            hot &= hot - 1;
-            sm.q.queue[qpos++] = (uint16_t)((p << 8) | (4 * (j >> 1) + 2 * s + (j & 1)));
+        // entry (p << 8 | k), k = 4 (j >> 1) + 2 s + (j & 1) = 2 j - (j & 1) + 2 s;
+        // entries j >= 32 exist only for rows of more than 64 chunks
+        const int ebase = (p << 8) | (2 * s);
+        uint32_t hlo = (uint32_t)hot;
+        while (hlo) {
+            const int j = __ffs(hlo) - 1;
+            hlo &= hlo - 1;
+            sm.q.queue[qpos++] = (uint16_t)(ebase + 2 * j - (j & 1));
+        }
+        uint32_t hhi = (uint32_t)(hot >> 32);
+        while (hhi) {
+            const int j = 32 + __ffs(hhi) - 1;
+            hhi &= hhi - 1;
+            sm.q.queue[qpos++] = (uint16_t)(ebase + 2 * j - (j & 1));
         }
         const int qn = qtotal;
         __syncwarp();   // vmax is dead from here on; its space holds the scratch
