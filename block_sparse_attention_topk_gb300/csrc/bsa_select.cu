@@ -1722,10 +1722,20 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         const int cn = min(sm.ccount[p], kPairCand);
         const bool sel_ok = need && !ovf;
         CK x[16];
+        {
+            // this lane's 16 list positions with vector loads, then the mask
+            const uint4* src = reinterpret_cast<const uint4*>(&sm.cand[p][s * 16]);
+            constexpr int kPer = 16 / sizeof(CK);   // composite keys per 16 bytes
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int pos = s * 16 + u;
-            x[u] = (sel_ok && pos < cn) ? sm.cand[p][pos] : (CK)0;
+            for (int v = 0; v < 16 / kPer; ++v) {
+                const uint4 q4 = src[v];
+                const CK* e = reinterpret_cast<const CK*>(&q4);
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) x[v * kPer + t] = e[t];
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (!(sel_ok && s * 16 + u < cn)) x[u] = (CK)0;
         }
         if constexpr (SMALLK)
             pair_top16_desc<CK>(x);
@@ -1739,9 +1749,13 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
             for (int u = 0; u < 16; ++u) y[u] = (s == 0 && u < r.kp) ? ck_low(x[u]) : 0u;
             lane_sort16_desc<uint32_t>(y);
             if (sel_ok && s == 0) {
+                // positions >= K' are never read
+                int4* dst = reinterpret_cast<int4*>(sm.q.sorted[p]);
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (u < r.kp) sm.q.sorted[p][u] = (int32_t)(kLowMax - y[u]);
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_int4((int32_t)(kLowMax - y[4 * v]), (int32_t)(kLowMax - y[4 * v + 1]),
+                                       (int32_t)(kLowMax - y[4 * v + 2]),
+                                       (int32_t)(kLowMax - y[4 * v + 3]));
             }
         } else {
             uint32_t y[16];

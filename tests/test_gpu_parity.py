@@ -138,6 +138,30 @@ def test_select_boundary_sweep(cuda_device, dtype, K, IL):
     _assert_equal(got, want, f"sweep dtype={dtype} K={K} I={I} L={L}")
 
 
+@pytest.mark.parametrize("dtype,M", [(torch.bfloat16, 74), (torch.bfloat16, 600),
+                                     (torch.bfloat16, 1024), (torch.float32, 300),
+                                     (torch.float32, 512)])
+@pytest.mark.parametrize("K,I,L", [(17, 1, 0), (18, 1, 0), (20, 1, 2), (24, 2, 3), (32, 1, 2),
+                                   (32, 0, 0), (5, 1, 2)])
+def test_select_pair_path_topk_sweep(cuda_device, dtype, M, K, I, L):
+    """The pair path (topk <= 32, rows <= 2 KB) on both sides of K' = 16,
+    where the top-16 merges give way to full 32-entry sorts, over row lengths
+    from a handful of blocks to the capacity, with NaN / Inf / zero / tie
+    specials."""
+    assert bsa.bsa_select_policy(10**5, M, K, 0 if dtype == torch.bfloat16 else 1)["path"] == \
+        bsa.BSA_PATH_PAIR
+    rows = 96
+    rng = np.random.default_rng(K * 100 + M)
+    nvp = rng.integers(0, M + 40, rows).astype(np.int32)
+    nvp[:8] = [0, 1, K - 1, K, K + 1, M, M - 1, 2 * K]
+    scores = synth.normal_scores((rows, 2, M), dtype, seed=K * 13 + M)
+    synth.inject_specials(scores, seed=K + M, frac_each=0.02, frac_ties=0.05)
+    synth.fill_tail(scores, torch.from_numpy(np.minimum(nvp, M)), float("-inf"))
+    want = oracle.topk_select(scores, nvp, K, I, L)
+    got = _gpu_select(scores, nvp, K, I, L, cuda_device)
+    _assert_equal(got, want, f"pair sweep dtype={dtype} M={M} K={K} I={I} L={L}")
+
+
 @pytest.mark.parametrize("M", [16, 74, 128, 129, 256, 257, 512, 513, 1024])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_select_capacity_boundaries(cuda_device, M, dtype):
