@@ -69,10 +69,11 @@ struct PairRowDesc {
 template <typename CK>
 struct PairSmem {
     union {
-        // chunk maxima (signed keys; fp32 keeps the top 16 bits), lane-major:
-        // chunk k = 4 i + 2 s + c of row p at vmax[p][s][2 i + c]; live from
+        // chunk maxima (signed keys; fp32 keeps the top 16 bits): the two
+        // chunks 4 i + 2 s + c (c = 0, 1) a lane takes at step i share one
+        // word, vmax2[i][lane] = max(c = 0) | max(c = 1) << 16; live from
         // pass 1 until the queue is built
-        int16_t vmax[kPairRows][2][kPairStepsPad];
+        uint32_t vmax2[kPairStepsPad / 2][32];
         // one 32-byte chunk per lane while candidates are collected
         uint32_t scratch[32][8];
     } a;

@@ -1459,16 +1459,16 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
 
         // ---- pass 1: chunk maxima and representatives ----
         // Step i covers chunks 4i .. 4i+3 (one 128-byte line of the row): lane
-        // s takes chunks 4i + 2s and 4i + 2s + 1.  Chunk maxima go to
-        // vmax[p][s][2i + c]; representatives: 4 classes (by step and chunk
-        // parity) x 4 disjoint element subsets.
+        // s takes chunks 4i + 2s and 4i + 2s + 1.  The step's two chunk maxima
+        // go to vmax2[i][lane] in one store; representatives: 4 classes (by
+        // step and chunk parity) x 4 disjoint element subsets.
         uint32_t rp[8];   // bf16: packed pairs; fp32 uses rq
         int32_t rq[16];
 #pragma unroll
         for (int x = 0; x < 8; ++x) rp[x] = E::kMaskWord;
 #pragma unroll
         for (int x = 0; x < 16; ++x) rq[x] = INT32_MIN;
-        auto take = [&](const uint32_t (&w)[8], int j, int cls) {
+        auto take = [&](const uint32_t (&w)[8], int cls) -> int32_t {
             int32_t vm;
             if constexpr (BF16) {
                 const uint32_t pa = max_s16x2(max_s16x2(w[0], w[2]), max_s16x2(w[4], w[6]));
@@ -1486,12 +1486,15 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                 }
                 vm = max(max(m4[0], m4[1]), max(m4[2], m4[3])) >> 16;
             }
-            sm.a.vmax[p][s][j] = (int16_t)vm;
+            return vm;
+        };
+        auto store_vmax = [&](int i, int32_t v0, int32_t v1) {
+            sm.a.vmax2[i][lane] = ((uint32_t)v0 & 0xFFFFu) | ((uint32_t)v1 << 16);
         };
         // Step 0 splits each chunk finer, into 8 subsets spread over the
         // four classes, so that a short row (a few chunks) still has at least
         // K' representatives and a tight theta.
-        auto take_first = [&](const uint32_t (&w)[8], int c) {
+        auto take_first = [&](const uint32_t (&w)[8], int c) -> int32_t {
             int32_t vm;
             if constexpr (BF16) {
                 const uint32_t a0 = max_s16x2(w[0], w[4]), a1 = max_s16x2(w[2], w[6]);
@@ -1513,23 +1516,22 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                 for (int jj = 1; jj < 8; ++jj) m = max(m, (int32_t)w[jj]);
                 vm = m >> 16;
             }
-            sm.a.vmax[p][s][c] = (int16_t)vm;
+            return vm;
         };
         const int nsteps = need ? (nchunk + 3) >> 2 : 0;
         // step 0 and the last step hold the row's edge chunks: masked loads
         auto edge_step = [&](int i, int cls0) {
+            int32_t vm[2] = {-32768, -32768};
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int k = 4 * i + 2 * s + c;
                 if (k < nchunk) {
                     uint32_t w[8];
                     pair_load_edge<BF16>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
-                    if (i == 0)
-                        take_first(w, c);
-                    else
-                        take(w, 2 * i + c, cls0 + c);
+                    vm[c] = i == 0 ? take_first(w, c) : take(w, cls0 + c);
                 }
             }
+            store_vmax(i, vm[0], vm[1]);
         };
         if (nsteps > 0) edge_step(0, 0);
         // interior steps 1 .. i_last hold chunks <= nchunk - 2 only; the next
@@ -1547,18 +1549,18 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                     ld32(ad + 160, b1);
                 }
                 chunk_to_keys<BF16>(a0);
-                take(a0, 2 * i, 0);
+                const int32_t va0 = take(a0, 0);
                 chunk_to_keys<BF16>(a1);
-                take(a1, 2 * i + 1, 1);
+                store_vmax(i, va0, take(a1, 1));
                 if (i < i_last) {
                     if (i + 1 < i_last) {
                         ld32(ad + 256, a0);
                         ld32(ad + 288, a1);
                     }
                     chunk_to_keys<BF16>(b0);
-                    take(b0, 2 * i + 2, 2);
+                    const int32_t vb0 = take(b0, 2);
                     chunk_to_keys<BF16>(b1);
-                    take(b1, 2 * i + 3, 3);
+                    store_vmax(i + 1, vb0, take(b1, 3));
                 }
                 ad += 256;
             }
@@ -1616,8 +1618,8 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         const int jmax = need ? 2 * (nchunk >> 2) + min(max((nchunk & 3) - 2 * s, 0), 2) : 0;
         unsigned long long hot = 0;
         for (int i0 = 0; i0 < jmax; i0 += 8) {
-            const uint4 pk = *reinterpret_cast<const uint4*>(&sm.a.vmax[p][s][i0]);
-            const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
+            const uint32_t wv[4] = {sm.a.vmax2[i0 / 2][lane], sm.a.vmax2[i0 / 2 + 1][lane],
+                                    sm.a.vmax2[i0 / 2 + 2][lane], sm.a.vmax2[i0 / 2 + 3][lane]};
             const uint32_t bits = th16 == -32768 ? 0xFFu : ge_bits16<4>(wv, th16);
             hot |= (unsigned long long)bits << i0;
         }
