@@ -107,6 +107,15 @@ struct SelectArgs {
     uint32_t h_mul, h_shift, dql_mul, dql_shift;
 };
 
+#ifdef __CUDACC__
+// One 256-bit store of eight int32 (a full 32-byte sector); p 32-byte aligned.
+__device__ __forceinline__ void st_v8(int32_t* p, const int32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+#endif
+
 // Multiplier and shift that divide every x < 2^31 by d >= 1 exactly as
 // (umulhi(x, mul) + x) >> shift (round-up reciprocal, Granlund and
 // Montgomery, "Division by invariant integers using multiplication", 1994).

@@ -13,41 +13,37 @@
 // ("Support speculative decode with AITER sparse PA", 实现拆解 items 1 and 3)
 // and of the EMIT_SPARSE_TABLE flag in PR #55235.
 //
-// How (a design for this GPU, not the pages' Triton/ROCm kernels):
-//  * One warp owns one work item: a whole row, or one chunk of a long row
-//    when there are too few rows to fill 152 SMs (split path).  The causal
-//    prefix is streamed with 16-byte vector loads (lane l loads vectors l,
-//    l+32, ...; a warp instruction moves 512 contiguous bytes); forced blocks
-//    and ids outside the row's range are replaced at load time by the bit
-//    pattern 0x8000 (bf16) / 0x80000000 (fp32), the most negative signed
-//    integer.
-//  * Threshold estimate.  On the raw bits read as signed integers, any two
-//    non-negative floats compare like the floats (+NaN above +Inf above
-//    finite), and every negative float or masked slot compares below them.
-//    Each lane keeps R representatives (maxima of its elements; bf16 pairs
-//    are maxed with one packed max.s16x2).  If at least K' representatives
-//    are >= 0, the K'-th largest of them, theta, is a lower bound on the K'-th
-//    best score of the chunk: K' distinct elements reach it.  Only elements
-//    >= theta can be selected, and for N(0,1)-like scores that is ~K' to 2K'
-//    elements.  When the estimate does not exist (few lanes with data, mostly
-//    negative scores) the chunk falls back to taking every valid element as
-//    a candidate, filtered in the order-preserving key space instead.
-//  * Candidates (order-preserving key, id) are appended in ascending id order
-//    to a per-warp shared-memory buffer.  When it would overflow, and at the
-//    end, an exact warp select keeps the K' best: a bit-by-bit search for the
-//    K'-th largest key (warp-reduced counts), then ties at that key resolved
-//    by buffer order, which is id order.  Later elements have higher ids, so
-//    after a compaction only keys strictly above the K'-th kept key can still
-//    enter; the raw-space threshold is raised accordingly.
-//  * Split rows: each chunk's warp writes its <= K' candidates to the
-//    caller's workspace and takes a ticket with atomicAdd; the warp that draws
-//    the last ticket merges the chunks' lists (chunk order = id order) with
-//    the same buffer logic, writes the output, and sets the ticket back to 0.
-//    The host also clears the tickets before every launch, so graph replays
-//    and workspaces reused across layouts start from zero (PR #55235:
-//    counters reset under graph replay).  Nothing ever waits on another warp.
-//  * Output: slots [0, n) = init ids, the K' selected ids, the local ids --
-//    ascending by construction -- then -1.
+// How (a design for this GPU, not the pages' Triton/ROCm kernels).  Three
+// kernels share one method:
+//  * Threshold.  Representatives (maxima of disjoint element subsets) give a
+//    lower bound theta on the K'-th best non-forced score: K' distinct
+//    elements reach the K'-th largest representative.  Only elements >= theta
+//    can be selected; for N(0,1)-like scores that is about K' to 1.5 K'.
+//    Forced blocks (init [0, I), local [v - L, v)) and ids outside the causal
+//    prefix are masked out of the search and emitted directly.
+//  * Candidates are composite keys (order-preserving key, then the inverted
+//    id): unique, and larger means a better (score, lower id) pair.  An exact
+//    select keeps the K' largest; the output lists init ids, the selected ids
+//    and local ids in ascending order, then -1.
+//  * pair_select_kernel (default for topk <= 32 and rows <= 2 KB): 2 lanes per
+//    row, 16 rows per warp, 32-byte chunks; elements become signed
+//    order-preserving keys as they are loaded (IEEE totalOrder for any sign);
+//    chunk maxima select the hot chunks, which are reloaded (L2 hits) and
+//    filtered; bitonic networks across the lane pair sort representatives and
+//    candidates.  Rows whose candidates overflow are redone by the warp path.
+//  * group_select_kernel: the same with 4 lanes per row, 8 rows per warp
+//    (selectable for testing).
+//  * select_kernel (warp path): one warp per row, or per chunk of a long row
+//    when there are too few rows to fill the GPU (split path).  Candidates
+//    are appended in id order to a per-warp shared buffer compacted by an
+//    exact warp select (bit search over the key, ties by buffer order).  A
+//    split row's chunks write their lists to the caller's workspace and take a
+//    ticket with atomicAdd; the last arriver merges, writes the output and
+//    resets the ticket, and the host clears the tickets before every launch
+//    (PR #55235: counters reset under graph replay).  Nothing waits on another
+//    warp.
+//  * The fused variant of every kernel gathers block_table[req, b] for the
+//    selected blocks and writes their page-16 entries and ctx in the same pass.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -818,13 +814,6 @@ __device__ __forceinline__ T pick(const T (&x)[N], int idx) {
 #pragma unroll
     for (int r = 1; r < N; ++r) v = idx == r ? x[r] : v;
     return v;
-}
-
-// One 256-bit store of eight int32 (a full 32-byte sector); p 32-byte aligned.
-__device__ __forceinline__ void st_v8(int32_t* p, const int32_t (&v)[8]) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
-                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-                 : "memory");
 }
 
 __device__ __forceinline__ int32_t group_sel(int j, const RowInfo& r, bool all,

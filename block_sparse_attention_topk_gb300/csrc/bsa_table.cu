@@ -135,8 +135,8 @@ sparse_table_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t 
 }
 
 // topk <= 32: G lanes per row (G = 16 for K <= 16, else 32), 32 / G rows per
-// warp.  VEC: the output table is 16-byte aligned, so each slot is written
-// with two 16-byte stores.
+// warp.  VEC: the output table is 32-byte aligned, so each slot is written
+// with one 256-bit store.
 constexpr int kSegWarps = 8;
 
 template <int G, bool VEC>
@@ -218,8 +218,7 @@ sparse_table_seg_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int6
             }
             int32_t* dst = sparse_bt + row * (int64_t)width + g * kPagesPerBlock;
             if constexpr (VEC) {
-                reinterpret_cast<int4*>(dst)[0] = make_int4(v[0], v[1], v[2], v[3]);
-                reinterpret_cast<int4*>(dst)[1] = make_int4(v[4], v[5], v[6], v[7]);
+                st_v8(dst, v);
             } else {
 #pragma unroll
                 for (int pg = 0; pg < 8; ++pg) dst[pg] = v[pg];
@@ -266,7 +265,7 @@ cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, 
     const int64_t rows = T * H;
     if (rows == 0) return cudaSuccess;
     if (K <= 32) {
-        const bool vec = (reinterpret_cast<uintptr_t>(sparse_bt) & 15) == 0;
+        const bool vec = (reinterpret_cast<uintptr_t>(sparse_bt) & 31) == 0;
         const int per_block = kSegWarps * (K <= 16 ? 2 : 1);
         const int grid = grid_for(rows, per_block, 8);
         auto kern = K <= 16 ? (vec ? sparse_table_seg_kernel<16, true>

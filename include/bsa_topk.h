@@ -209,6 +209,11 @@ int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_t T, int64_
  * for sm_103a) for `rows` = T*H rows of capacity M on a GPU with `num_sms`
  * SMs.  Host-only, deterministic, launches nothing; exported so the 74 /
  * 128 / 129 and other capacity boundaries can be tested without a GPU.
+ * Paths: BSA_PATH_PAIR when K <= 32 and a row holds at most 2 KB (M * element
+ * size <= 2048); otherwise BSA_PATH_ROW, or BSA_PATH_SPLIT when a row needs
+ * more than one pass and the rows alone cannot fill the GPU.  The environment
+ * variable BSA_SELECT_PATH=row|group|pair, read once per process, forces a
+ * path for testing (BSA_PATH_GROUP is reachable only that way).
  * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_TOPK, BSA_ERR_DTYPE. */
 int bsa_select_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
                       bsa_launch_policy_t* policy);

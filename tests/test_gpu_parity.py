@@ -387,9 +387,10 @@ def test_sparse_table_random_ids(cuda_device, H, K, dql):
 
 
 @pytest.mark.parametrize("K", [16, 32])
-def test_sparse_table_unaligned_output_and_many_rows(cuda_device, K):
-    """An output table that starts 4 bytes past a 16-byte boundary takes the
-    scalar-store form; 12000 rows span many grid strides."""
+@pytest.mark.parametrize("offset_words", [1, 4])
+def test_sparse_table_unaligned_output_and_many_rows(cuda_device, K, offset_words):
+    """An output table that starts 4 or 16 bytes past a 32-byte boundary takes
+    the element-wise store form; 12000 rows span many grid strides."""
     g = torch.Generator().manual_seed(500 + K)
     B, H, dql, MB = 3000, 2, 2, 64
     seq = torch.randint(0, 8200, (B,), generator=g, dtype=torch.int32)
@@ -399,15 +400,15 @@ def test_sparse_table_unaligned_output_and_many_rows(cuda_device, K):
     table = synth.random_block_table(B, MB, seed=K + 1)
     want_bt, want_ctx = oracle.build_sparse_block_table(idx.numpy(), table.numpy(), seq.numpy(), dql)
     n = T * H * K * 8
-    flat = torch.full((n + 1,), -7, dtype=torch.int32, device=cuda_device)
-    bt = flat[1:].view(T, H, K * 8)
-    assert bt.data_ptr() % 16 == 4
+    flat = torch.full((n + 8,), -7, dtype=torch.int32, device=cuda_device)
+    bt = flat[offset_words:offset_words + n].view(T, H, K * 8)
+    assert bt.data_ptr() % 32 == 4 * offset_words
     _, ctx = bsa.bsa_build_sparse_block_table(idx.to(cuda_device), table.to(cuda_device),
                                               seq.to(cuda_device), dql, sparse_bt=bt)
     torch.cuda.synchronize()
     _assert_equal(bt.cpu().numpy(), want_bt, "sparse table (unaligned)")
     _assert_equal(ctx.cpu().numpy(), want_ctx, "sparse ctx")
-    assert int(flat[0].item()) == -7
+    assert int(flat[0].item()) == -7 and int(flat[-1].item()) == -7
 
 
 @pytest.mark.parametrize("variant", ["as_given", "dql1_h2", "fp32_small_table", "no_idx"])
