@@ -69,6 +69,16 @@ __device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
     asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+__device__ __forceinline__ uint32_t min_s16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.s16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 r;
@@ -1309,6 +1319,94 @@ __device__ __forceinline__ uint32_t ge_bits16_perm(const uint32_t (&w)[8], int32
 // Element of a bf16 chunk named by bit b of ge_bits16_perm.
 __device__ __forceinline__ int perm_elem(int b) { return ((b & 7) << 1) | (b >> 3); }
 
+// Sorting 16 sixteen-bit values packed two per word: value r sits in word
+// r & 7, low half for r < 8 and high half for r >= 8.  One max/min of two
+// words compares the two columns at once.  SG selects signed or unsigned
+// order.
+template <bool SG>
+__device__ __forceinline__ uint32_t hmax(uint32_t a, uint32_t b) {
+    return SG ? max_s16x2(a, b) : max_u16x2(a, b);
+}
+template <bool SG>
+__device__ __forceinline__ uint32_t hmin(uint32_t a, uint32_t b) {
+    return SG ? min_s16x2(a, b) : min_u16x2(a, b);
+}
+
+// Each 16-bit half of every word: low half <- max of the two, high <- min.
+template <bool SG>
+__device__ __forceinline__ uint32_t hsplit(uint32_t t) {
+    const uint32_t sw = __byte_perm(t, 0, 0x1032);
+    return __byte_perm(hmax<SG>(t, sw), hmin<SG>(t, sw), 0x7610);
+}
+
+// Descending half-cleaners j = 4, 2, 1 on both columns: each column, bitonic
+// on entry, leaves sorted.
+template <bool SG>
+__device__ __forceinline__ void hclean8_desc(uint32_t (&w)[8]) {
+#pragma unroll
+    for (int j = 4; j > 0; j >>= 1) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            if ((r & j) == 0) {
+                const uint32_t a = w[r], b = w[r | j];
+                w[r] = hmax<SG>(a, b);
+                w[r | j] = hmin<SG>(a, b);
+            }
+        }
+    }
+}
+
+// The 16 packed values sorted descending (positions 0..7 in the low halves).
+template <bool SG>
+__device__ __forceinline__ void packed_sort16_desc(uint32_t (&w)[8]) {
+    // each column (8 values) by a bitonic network on whole words
+#pragma unroll
+    for (int k = 2; k <= 8; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                if ((r & j) == 0) {
+                    const bool desc = (r & k) == 0 || k == 8;
+                    const uint32_t a = w[r], b = w[r | j];
+                    const uint32_t mx = hmax<SG>(a, b), mn = hmin<SG>(a, b);
+                    w[r] = desc ? mx : mn;
+                    w[r | j] = desc ? mn : mx;
+                }
+            }
+        }
+    }
+    // merge the sorted columns A (low) and B (high): max(A[i], B[7 - i]) are
+    // the top 8 as a bitonic sequence, the minima the bottom 8
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = __byte_perm(w[i], w[7 - i], 0x7610);
+        const uint32_t b = __byte_perm(w[7 - i], w[i], 0x7610);
+        w[i] = hsplit<SG>(a);
+        w[7 - i] = hsplit<SG>(b);
+    }
+    hclean8_desc<SG>(w);
+}
+
+// The 16 largest of the 32 packed values a lane pair holds, sorted
+// descending, in both lanes' registers (the packed form of pair_top16_desc).
+template <bool SG>
+__device__ __forceinline__ void packed_pair_top16_desc(uint32_t (&w)[8]) {
+    packed_sort16_desc<SG>(w);
+    // c[r] = max(a[r], b[15 - r]): for word i, the partner's word 7 - i with
+    // its halves swapped
+    uint32_t y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __shfl_xor_sync(0xffffffffu, w[7 - i], 1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = hmax<SG>(w[i], __byte_perm(y[i], 0, 0x1032));
+    // c is bitonic: half-cleaner j = 8 (low vs high half of each word), then
+    // j = 4, 2, 1 within the columns
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = hsplit<SG>(w[i]);
+    hclean8_desc<SG>(w);
+}
+
 // Bitonic sort, descending, of the 32 values a lane pair holds: lane s keeps
 // positions 16 s .. 16 s + 15 in x[0..15].  Every lane of the warp calls it.
 template <typename T>
@@ -1558,32 +1656,38 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
 
         // ---- theta: the K'-th largest of the row's 32 representatives (distinct
         // elements), a lower bound on the K'-th best score ----
-        int32_t rep[16];
-        if constexpr (BF16) {
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                rep[2 * x] = E::pack_lo(rp[x]);
-                rep[2 * x + 1] = E::pack_hi(rp[x]);
-            }
-        } else {
-#pragma unroll
-            for (int x = 0; x < 16; ++x) rep[x] = rq[x];
-        }
         // bitonic sort of the pair's 32 representatives; the K'-th largest is
-        // position K' - 1 (lane 0 holds positions 0..15).  A row with fewer
-        // than K' representatives gets the smallest key: every element of
-        // [lo, hi) is then a candidate.
+        // position K' - 1.  A row with fewer than K' representatives gets the
+        // smallest key: every element of [lo, hi) is then a candidate.
         const int want = max(r.kp - 1, 0);
         int32_t theta;
-        if constexpr (SMALLK) {
-            // K' <= 16: the top 16 suffice, in lane 0
-            pair_top16_desc<int32_t>(rep);
-            theta = __shfl_sync(kFull, pick(rep, want), lane & ~1);
+        if constexpr (SMALLK && BF16) {
+            // K' <= 16: the top 16 suffice; bf16 representatives stay packed
+            packed_pair_top16_desc<true>(rp);
+            const uint32_t wv = pick(rp, want & 7);
+            theta = (int32_t)(int16_t)(uint16_t)(want < 8 ? wv : (wv >> 16));
         } else {
-            pair_sort32_desc<int32_t>(rep, s);
-            const int32_t mine = pick(rep, want & 15);
-            const int32_t other = __shfl_xor_sync(kFull, mine, 1);
-            theta = ((want < 16) == (s == 0)) ? mine : other;
+            int32_t rep[16];
+            if constexpr (BF16) {
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    rep[2 * x] = E::pack_lo(rp[x]);
+                    rep[2 * x + 1] = E::pack_hi(rp[x]);
+                }
+            } else {
+#pragma unroll
+                for (int x = 0; x < 16; ++x) rep[x] = rq[x];
+            }
+            if constexpr (SMALLK) {
+                // K' <= 16: the top 16 suffice, in lane 0
+                pair_top16_desc<int32_t>(rep);
+                theta = __shfl_sync(kFull, pick(rep, want), lane & ~1);
+            } else {
+                pair_sort32_desc<int32_t>(rep, s);
+                const int32_t mine = pick(rep, want & 15);
+                const int32_t other = __shfl_xor_sync(kFull, mine, 1);
+                theta = ((want < 16) == (s == 0)) ? mine : other;
+            }
         }
         if (s == 0) {
             sm.ccount[p] = 0;
@@ -1734,19 +1838,31 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
             pair_sort32_desc<CK>(x, s);
         __syncwarp();
         if constexpr (SMALLK) {
-            // K' <= 16: the kept positions are lane 0's registers
-            uint32_t y[16];
+            // K' <= 16: the kept positions are lane 0's registers.  Their ids
+            // (< 2^16 on this path) are sorted as 0xFFFF - id, two per word.
+            uint32_t yp[8];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) y[u] = (s == 0 && u < r.kp) ? ck_low(x[u]) : 0u;
-            lane_sort16_desc<uint32_t>(y);
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t lo = (s == 0 && u < r.kp)
+                                        ? 0xFFFFu - (uint32_t)(kLowMax - ck_low(x[u])) : 0u;
+                const uint32_t hi = (s == 0 && u + 8 < r.kp)
+                                        ? 0xFFFFu - (uint32_t)(kLowMax - ck_low(x[u + 8])) : 0u;
+                yp[u] = lo | (hi << 16);
+            }
+            packed_sort16_desc<false>(yp);
             if (sel_ok && s == 0) {
-                // positions >= K' are never read
+                // id = 0xFFFF - value = the value's complement; positions >= K'
+                // are never read
                 int4* dst = reinterpret_cast<int4*>(sm.q.sorted[p]);
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_int4((int32_t)(kLowMax - y[4 * v]), (int32_t)(kLowMax - y[4 * v + 1]),
-                                       (int32_t)(kLowMax - y[4 * v + 2]),
-                                       (int32_t)(kLowMax - y[4 * v + 3]));
+                for (int v = 0; v < 2; ++v) {
+                    dst[v] = make_int4((int32_t)(~yp[4 * v] & 0xFFFFu), (int32_t)(~yp[4 * v + 1] & 0xFFFFu),
+                                       (int32_t)(~yp[4 * v + 2] & 0xFFFFu),
+                                       (int32_t)(~yp[4 * v + 3] & 0xFFFFu));
+                    dst[v + 2] = make_int4((int32_t)(~yp[4 * v] >> 16), (int32_t)(~yp[4 * v + 1] >> 16),
+                                           (int32_t)(~yp[4 * v + 2] >> 16),
+                                           (int32_t)(~yp[4 * v + 3] >> 16));
+                }
             }
         } else {
             uint32_t y[16];
