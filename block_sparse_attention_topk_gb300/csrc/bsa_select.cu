@@ -1215,16 +1215,21 @@ __device__ __forceinline__ int32_t key_of_raw(int32_t raw) {
     else return raw ^ ((raw >> 31) & 0x7FFFFFFF);
 }
 
+// 0xFFFF in each 16-bit half of x whose sign bit is set (prmt with the
+// sign-replicate selector).
+__device__ __forceinline__ uint32_t sign_mask16(uint32_t x) {
+    uint32_t m;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(m) : "r"(x), "r"(0u), "n"(0xBB99));
+    return m;
+}
+
 // The same on a whole 32-byte chunk, in place (bf16: two keys per word).
 template <bool BF16>
 __device__ __forceinline__ void chunk_to_keys(uint32_t (&w)[8]) {
 #pragma unroll
     for (int x = 0; x < 8; ++x) {
         if constexpr (BF16) {
-            // 0xFFFF in each half whose sign bit is set (prmt sign-replicate)
-            uint32_t sg;
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sg) : "r"(w[x]), "r"(0u), "n"(0xBB99));
-            w[x] ^= sg & 0x7FFF7FFFu;
+            w[x] ^= sign_mask16(w[x]) & 0x7FFF7FFFu;
         } else {
             w[x] ^= (uint32_t)((int32_t)w[x] >> 31) & 0x7FFFFFFFu;
         }
@@ -1575,6 +1580,33 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
             }
             return vm;
         };
+        // The same on raw bits (interior chunks, bf16): a subset's largest key
+        // is its raw signed maximum when that is non-negative, else the key of
+        // its raw signed minimum (a negative value's magnitude grows with its
+        // raw integer, so the most negative raw value is the largest float),
+        // with the low 15 bits flipped.
+        auto take_raw = [&](const uint32_t (&w)[8], int cls) -> int32_t {
+            if constexpr (BF16) {
+                const uint32_t ax = max_s16x2(max_s16x2(w[0], w[2]), max_s16x2(w[4], w[6]));
+                const uint32_t an = min_s16x2(min_s16x2(w[0], w[2]), min_s16x2(w[4], w[6]));
+                const uint32_t bx = max_s16x2(max_s16x2(w[1], w[3]), max_s16x2(w[5], w[7]));
+                const uint32_t bn = min_s16x2(min_s16x2(w[1], w[3]), min_s16x2(w[5], w[7]));
+                // 0xFFFF in each half whose raw maximum is negative
+                const uint32_t ma = sign_mask16(ax), mb = sign_mask16(bx);
+                const uint32_t pa = (ax & ~ma) | ((an ^ 0x7FFF7FFFu) & ma);
+                const uint32_t pb = (bx & ~mb) | ((bn ^ 0x7FFF7FFFu) & mb);
+                rp[cls * 2] = max_s16x2(rp[cls * 2], pa);
+                rp[cls * 2 + 1] = max_s16x2(rp[cls * 2 + 1], pb);
+                const uint32_t mm = max_s16x2(pa, pb);
+                return max(E::pack_lo(mm), E::pack_hi(mm));
+            } else {
+                uint32_t k[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) k[x] = w[x];
+                chunk_to_keys<BF16>(k);
+                return take(k, cls);
+            }
+        };
         auto store_vmax = [&](int i, int32_t v0, int32_t v1) {
             sm.a.vmax2[i][lane] = ((uint32_t)v0 & 0xFFFFu) | ((uint32_t)v1 << 16);
         };
@@ -1635,19 +1667,15 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
                     ld32(ad + 128, b0);
                     ld32(ad + 160, b1);
                 }
-                chunk_to_keys<BF16>(a0);
-                const int32_t va0 = take(a0, 0);
-                chunk_to_keys<BF16>(a1);
-                store_vmax(i, va0, take(a1, 1));
+                const int32_t va0 = take_raw(a0, 0);
+                store_vmax(i, va0, take_raw(a1, 1));
                 if (i < i_last) {
                     if (i + 1 < i_last) {
                         ld32(ad + 256, a0);
                         ld32(ad + 288, a1);
                     }
-                    chunk_to_keys<BF16>(b0);
-                    const int32_t vb0 = take(b0, 2);
-                    chunk_to_keys<BF16>(b1);
-                    store_vmax(i + 1, vb0, take(b1, 3));
+                    const int32_t vb0 = take_raw(b0, 2);
+                    store_vmax(i + 1, vb0, take_raw(b1, 3));
                 }
                 ad += 256;
             }
