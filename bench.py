@@ -432,6 +432,9 @@ def config_latencies(device):
         "long_decode_k64": synth.long_decode(device=device, K=64),
         "mixed_prefill_decode": synth.mixed_prefill_decode(device=device),
         "fused_table": synth.fused_table(device=device),
+        # full capacity (1M-token contexts, 4096..8192 blocks): the split path
+        "capacity_8192_split": synth.long_decode(device=device, B=64, H=2, M=8192, K=16,
+                                                 min_len=524288, max_len=1048576),
     }
     for name, w in cases.items():
         if w.seq_lens is not None:

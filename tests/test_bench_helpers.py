@@ -1,0 +1,28 @@
+"""bench.py's algorithmic byte count against a hand-computed example (the
+definition the roofline uses: the non-forced causal prefix of each row when
+the row needs a selection, the id write, the page-count read, and for the
+fused call the block-table gathers, the table and ctx writes)."""
+import os
+import sys
+from types import SimpleNamespace
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_algorithmic_bytes_hand_example():
+    sys.path.insert(0, ROOT)
+    import bench
+    w = SimpleNamespace(K=4, H=2, num_init=1, num_local=1, dtype=torch.bfloat16, M=10, T=3)
+    # page counts 0, 3, 12 -> v = 0, 3, 10; only the last row has v > K
+    b = bench.algorithmic_bytes(w, np.array([0, 3, 12], dtype=np.int32), "fused")
+    # scores: (10 - 2 forced) bf16 x 2 heads = 32 B; ids 3*2*4*4 = 96 B; page counts 3*4 = 12 B
+    assert b["score_read"] == 32
+    assert b["select"] == 32 + 96 + 12
+    # gathers: n = 0 + 3 + 4 ids per head x 2 heads x 4 B = 56 B
+    # table + ctx: 3 tokens x 2 heads x (4*8*4 + 4) = 792 B
+    assert b["fused"] == 140 + 56 + 792
+    assert b["table_builder"] == 96 + 12 + 56 + 792
+    assert b["per_row_fused"] == (140 + 56 + 792) / 6
