@@ -123,12 +123,13 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
         const int gsmem = kPairWarps * (int)(dtype == BSA_DTYPE_BF16
                                                  ? sizeof(PairSmem<uint32_t>)
                                                  : sizeof(PairSmem<unsigned long long>));
-        int ctas = kPairCtas;  // the kernel's register bound
-        while (ctas > 1 && ctas * (gsmem + 1024) > 228 * 1024) --ctas;
+        // One item (16 rows) per warp and no persistent grid: the hardware
+        // hands a finished CTA's slot to the next CTA, which balances items
+        // of unequal length better than a fixed stride over resident warps.
+        // (The kernel still strides, so a capped grid would also be correct.)
         const int64_t items = (rows + kPairRows - 1) / kPairRows;
         int64_t grid = (items + kPairWarps - 1) / kPairWarps;
-        const int64_t grid_cap = (int64_t)num_sms * ctas;
-        if (grid > grid_cap) grid = grid_cap;
+        if (grid > INT32_MAX) grid = INT32_MAX;
         if (grid < 1) grid = 1;
         p->path = BSA_PATH_PAIR;
         p->vecs_per_lane = 4;

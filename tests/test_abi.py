@@ -116,7 +116,8 @@ def test_policy_capacity_and_grid(bsa):
     assert p["smem_bytes"] == p["warps_per_cta"] * p["cand_capacity"] * 8
     assert p["grid"] == 152 * 4
     g = _policy(bsa, 10**6, 1024, 16, BF)
-    assert g["path"] == bsa.BSA_PATH_PAIR and g["grid"] == 152 * 5
+    # pair path: one 16-row item per warp, 4 warps per CTA, no persistent cap
+    assert g["path"] == bsa.BSA_PATH_PAIR and g["grid"] == (10**6 // 16 + 3) // 4
     # the overflow fallback's buffer fits in a pair warp's shared memory
     assert g["cand_capacity"] * 8 <= g["smem_bytes"] // g["warps_per_cta"]
     assert _policy(bsa, 10, 74, 16, BF)["grid"] == 1
