@@ -162,13 +162,12 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
         p->smem_bytes = gsmem;
         return BSA_OK;
     }
+    // One work item per warp; the grid is not capped at the resident CTAs,
+    // so the hardware balances items of unequal length (the kernel strides,
+    // so any grid is correct).
     const int64_t items = rows * chunks;
-    int ctas_per_sm = 4;
-    const int smem_budget = 227 * 1024;
-    while (ctas_per_sm > 1 && ctas_per_sm * smem > smem_budget) --ctas_per_sm;
     int64_t grid = (items + warps - 1) / warps;
-    const int64_t grid_cap = (int64_t)num_sms * ctas_per_sm;
-    if (grid > grid_cap) grid = grid_cap;
+    if (grid > INT32_MAX) grid = INT32_MAX;
     if (grid < 1) grid = 1;
     p->path = chunks > 1 ? BSA_PATH_SPLIT : BSA_PATH_ROW;
     p->vecs_per_lane = nv;

@@ -267,7 +267,8 @@ cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, 
     if (K <= 32) {
         const bool vec = (reinterpret_cast<uintptr_t>(sparse_bt) & 31) == 0;
         const int per_block = kSegWarps * (K <= 16 ? 2 : 1);
-        const int grid = grid_for(rows, per_block, 8);
+        // one row group per warp, grid not capped at the resident CTAs
+        const int grid = grid_for(rows, per_block, 1 << 20);
         auto kern = K <= 16 ? (vec ? sparse_table_seg_kernel<16, true>
                                    : sparse_table_seg_kernel<16, false>)
                             : (vec ? sparse_table_seg_kernel<32, true>

@@ -114,7 +114,7 @@ def test_policy_capacity_and_grid(bsa):
     p = _policy(bsa, 10**6, 1024, 64, BF)
     assert p["cand_capacity"] >= 64 + 32 * 8 and p["cand_capacity"] % 32 == 0
     assert p["smem_bytes"] == p["warps_per_cta"] * p["cand_capacity"] * 8
-    assert p["grid"] == 152 * 4
+    assert p["grid"] == (10**6 + 7) // 8          # one row per warp, 8 warps per CTA
     g = _policy(bsa, 10**6, 1024, 16, BF)
     # pair path: one 16-row item per warp, 4 warps per CTA, no persistent cap
     assert g["path"] == bsa.BSA_PATH_PAIR and g["grid"] == (10**6 // 16 + 3) // 4
