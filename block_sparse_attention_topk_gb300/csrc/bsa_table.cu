@@ -17,9 +17,10 @@
 // lanes, one id per lane: the block-table gather is issued as soon as the id
 // is known, and overlaps a segmented bitonic sort of (id, lane) that brings
 // duplicates together; kept ids are compacted through shared memory and each
-// lane writes one 32-byte slot of the row.  Larger topk gives one warp to a
-// row and deduplicates and sorts the ids in shared memory by counting ranks
-// (K <= 1024 ids).
+// lane writes one 32-byte slot of the row.  For topk up to 64 a warp takes one
+// row with two ids per lane and sorts them the same way.  Larger topk gives
+// one warp to a row and deduplicates and sorts the ids in shared memory by
+// counting ranks (K <= 1024 ids).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -231,6 +232,120 @@ sparse_table_seg_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int6
     }
 }
 
+// 32 < topk <= 64: one warp per row, two ids per lane.  Element e = 2 * lane
+// + h (h = 0, 1) holds id e of the row; the 64 keys (id << 6 | e) are sorted
+// across the warp with a bitonic network whose last stage compares a lane's
+// own two registers.  Ids are below cdiv(seq_len, 128) <= 2^24, so the key
+// does not overflow.
+template <bool VEC>
+__global__ void __launch_bounds__(kSegWarps * 32)
+sparse_table_seg64_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t H,
+                          int32_t K, const int32_t* __restrict__ block_table,
+                          int64_t max_blocks, const int32_t* __restrict__ seq_lens, int32_t dql,
+                          int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx) {
+    constexpr int32_t kNone = 0x7FFFFFFF;      // sorts after every (id << 6 | e)
+    __shared__ int32_t s_in[kSegWarps][64];    // gathered entry by element
+    __shared__ int32_t s_blk[kSegWarps][64];   // kept ids, ascending
+    __shared__ int32_t s_phys[kSegWarps][64];  // their gathered entries
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int width = K * kPagesPerBlock;
+    for (int64_t row = (int64_t)blockIdx.x * kSegWarps + warp; row < rows;
+         row += (int64_t)gridDim.x * kSegWarps) {
+        const int64_t t = row / H;
+        const int64_t req = t / dql;
+        const int64_t pos = (int64_t)__ldg(seq_lens + req) - dql + (t - req * dql);
+        const int64_t causal_len = pos + 1 > 0 ? pos + 1 : 0;
+        const int64_t nblk = (causal_len + kPageSize - 1) >> kLogPageSize;
+        const int64_t limit = nblk < max_blocks ? nblk : max_blocks;
+        const int32_t* table = block_table + req * max_blocks;
+        int32_t key[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int e = 2 * lane + h;
+            key[h] = kNone;
+            int32_t phys = 0;
+            if (e < K) {
+                const int32_t x = __ldg(topk_idx + row * K + e);
+                if (x >= 0 && x < limit) {
+                    key[h] = (x << 6) | e;
+                    phys = __ldg(table + x);
+                }
+            }
+            s_in[warp][e] = phys;
+        }
+        // ascending bitonic sort of the 64 keys; equal ids end up adjacent,
+        // ordered by element
+#pragma unroll
+        for (int k = 2; k <= 64; k <<= 1) {
+            const bool asc = k == 64 || (lane & (k >> 1)) == 0;
+#pragma unroll
+            for (int j = k >> 1; j > 1; j >>= 1) {
+                const bool take_min = ((lane & (j >> 1)) == 0) == asc;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int32_t other = __shfl_xor_sync(kFull, key[h], j >> 1);
+                    key[h] = take_min ? min(key[h], other) : max(key[h], other);
+                }
+            }
+            const int32_t lo = min(key[0], key[1]);
+            const int32_t hi = max(key[0], key[1]);
+            key[0] = asc ? lo : hi;
+            key[1] = asc ? hi : lo;
+        }
+        const int32_t prev1 = __shfl_up_sync(kFull, key[1], 1);
+        const bool keep0 = key[0] != kNone && (lane == 0 || (prev1 >> 6) != (key[0] >> 6));
+        const bool keep1 = key[1] != kNone && (key[0] >> 6) != (key[1] >> 6);
+        const unsigned b0 = __ballot_sync(kFull, keep0);
+        const unsigned b1 = __ballot_sync(kFull, keep1);
+        const int n = __popc(b0) + __popc(b1);
+        __syncwarp();
+        const unsigned below = (1u << lane) - 1u;
+        const int rank0 = __popc(b0 & below) + __popc(b1 & below);
+        if (keep0) {
+            s_blk[warp][rank0] = key[0] >> 6;
+            s_phys[warp][rank0] = s_in[warp][key[0] & 63];
+        }
+        if (keep1) {
+            const int rank1 = rank0 + (keep0 ? 1 : 0);
+            s_blk[warp][rank1] = key[1] >> 6;
+            s_phys[warp][rank1] = s_in[warp][key[1] & 63];
+        }
+        __syncwarp();
+        int32_t contrib = 0;
+        int32_t* out = sparse_bt + row * (int64_t)width;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int j = lane + 32 * u;
+            if (j >= K) continue;
+            int32_t v[8];
+            if (j < n) {
+                const int32_t b = s_blk[warp][j];
+                const int32_t ph = s_phys[warp][j];
+                const int64_t first = (int64_t)b * kPageSize;
+#pragma unroll
+                for (int pg = 0; pg < 8; ++pg)
+                    v[pg] = first + pg * kSubPage < causal_len ? ph * kPagesPerBlock + pg : 0;
+                const int64_t rem = causal_len - first;
+                contrib += (int32_t)(rem < kPageSize ? rem : kPageSize);
+            } else {
+#pragma unroll
+                for (int pg = 0; pg < 8; ++pg) v[pg] = 0;
+            }
+            int32_t* dst = out + j * kPagesPerBlock;
+            if constexpr (VEC) {
+                st_v8(dst, v);
+            } else {
+#pragma unroll
+                for (int pg = 0; pg < 8; ++pg) dst[pg] = v[pg];
+            }
+        }
+        contrib = __reduce_add_sync(kFull, contrib);
+        if (lane == 0) sparse_ctx[row] = contrib;
+        __syncwarp();
+    }
+}
+
 int grid_for(int64_t work, int per_block, int max_blocks_per_sm) {
     int64_t g = (work + per_block - 1) / per_block;
     const int64_t cap = (int64_t)device_sm_count() * max_blocks_per_sm;
@@ -273,6 +388,15 @@ cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, 
                                    : sparse_table_seg_kernel<16, false>)
                             : (vec ? sparse_table_seg_kernel<32, true>
                                    : sparse_table_seg_kernel<32, false>);
+        kern<<<grid, kSegWarps * 32, 0, stream>>>(topk_idx, rows, H, K, block_table, max_blocks,
+                                                  seq_lens, dql, sparse_bt, sparse_ctx);
+        return cudaGetLastError();
+    }
+    if (K <= 64) {
+        const bool vec = (reinterpret_cast<uintptr_t>(sparse_bt) & 31) == 0;
+        // one row per warp, grid not capped at the resident CTAs
+        const int grid = grid_for(rows, kSegWarps, 1 << 20);
+        auto kern = vec ? sparse_table_seg64_kernel<true> : sparse_table_seg64_kernel<false>;
         kern<<<grid, kSegWarps * 32, 0, stream>>>(topk_idx, rows, H, K, block_table, max_blocks,
                                                   seq_lens, dql, sparse_bt, sparse_ctx);
         return cudaGetLastError();

@@ -365,7 +365,8 @@ def test_sparse_table_worked_example(cuda_device):
 
 
 @pytest.mark.parametrize("H,K,dql", [(1, 16, 4), (2, 16, 1), (3, 7, 3), (1, 64, 2), (2, 300, 1),
-                                     (2, 32, 2), (1, 13, 1), (4, 1, 1), (3, 17, 2), (1, 33, 1)])
+                                     (2, 32, 2), (1, 13, 1), (4, 1, 1), (3, 17, 2), (1, 33, 1),
+                                     (2, 47, 3), (3, 63, 1), (1, 65, 2)])
 def test_sparse_table_random_ids(cuda_device, H, K, dql):
     """Arbitrary ids: -1, out-of-range, beyond the block table, duplicates."""
     g = torch.Generator().manual_seed(K * 31 + H)
@@ -386,7 +387,41 @@ def test_sparse_table_random_ids(cuda_device, H, K, dql):
     _assert_equal(ctx.cpu().numpy(), want_ctx, "sparse ctx")
 
 
-@pytest.mark.parametrize("K", [16, 32])
+@pytest.mark.parametrize("K", [33, 48, 64])
+@pytest.mark.parametrize("pattern", ["distinct", "all_same", "descending", "mixed"])
+def test_sparse_table_warp_row_patterns(cuda_device, K, pattern):
+    """Topk between 33 and 64 (one warp per row, two ids per lane): ids all
+    distinct, all one id, in descending order, or distinct with -1 holes and
+    repeats, against the oracle."""
+    g = torch.Generator().manual_seed(900 + K)
+    B, H, dql, MB = 150, 2, 2, 128
+    seq = torch.randint(0, 128 * MB + 300, (B,), generator=g, dtype=torch.int32)
+    seq[::13] = 0
+    T = B * dql
+    rows = T * H
+    if pattern == "distinct":
+        idx = torch.stack([torch.randperm(MB, generator=g)[:K] for _ in range(rows)])
+    elif pattern == "all_same":
+        idx = torch.randint(0, 40, (rows, 1), generator=g).expand(rows, K).clone()
+    elif pattern == "descending":
+        idx = torch.arange(K - 1, -1, -1).expand(rows, K).clone() + torch.randint(
+            0, MB - K, (rows, 1), generator=g)
+    else:
+        idx = torch.stack([torch.randperm(MB, generator=g)[:K] for _ in range(rows)])
+        idx[:, ::7] = -1
+        idx[:, 5::9] = idx[:, 4::9][:, :idx[:, 5::9].shape[1]]
+    idx = idx.to(torch.int32).view(T, H, K)
+    table = synth.random_block_table(B, MB, seed=K + 7)
+    want_bt, want_ctx = oracle.build_sparse_block_table(idx.numpy(), table.numpy(),
+                                                        seq.numpy(), dql)
+    bt, ctx = bsa.bsa_build_sparse_block_table(idx.to(cuda_device), table.to(cuda_device),
+                                               seq.to(cuda_device), dql)
+    torch.cuda.synchronize()
+    _assert_equal(bt.cpu().numpy(), want_bt, f"sparse table {pattern}")
+    _assert_equal(ctx.cpu().numpy(), want_ctx, f"sparse ctx {pattern}")
+
+
+@pytest.mark.parametrize("K", [16, 32, 64])
 @pytest.mark.parametrize("offset_words", [1, 4])
 def test_sparse_table_unaligned_output_and_many_rows(cuda_device, K, offset_words):
     """An output table that starts 4 or 16 bytes past a 32-byte boundary takes
