@@ -206,15 +206,30 @@ def read_peaks():
         return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
-def read_traffic(path_name: str):
-    """DRAM bytes per launch from the committed ncu summary, if it still
-    describes the current kernel source."""
+KERNEL_OF_PATH = {0: "select_kernel", 1: "select_kernel", 2: "group_select_kernel",
+                  3: "pair_select_kernel"}
+
+
+def dominant_kernel(path_id: int, fused: bool) -> str:
+    """Name of the selector kernel the launch policy picked."""
+    name = KERNEL_OF_PATH[path_id]
+    return name + " (fused sparse-table epilogue)" if fused else name
+
+
+def read_traffic(path_name: str, kernel: str = "pair_select_kernel", topk: int = 16,
+                 requests: int = 131072):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on this kernel, topk and request count and still describes the current
+    kernel source."""
     f = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(f) as fh:
             d = json.load(fh)
         ent = d.get(path_name)
         if not ent:
+            return None
+        if (not ent.get("kernel", "").startswith(kernel + "<") or ent.get("topk") != topk
+                or ent.get("requests") != requests):
             return None
         import hashlib
         src = os.path.join(ROOT, "block_sparse_attention_topk_gb300", "csrc", "bsa_select.cu")
@@ -297,7 +312,10 @@ def run_ours(args):
     peak, peak_src = read_peaks()
     dom_bytes = byt["fused"] if args.path == "fused" else byt["select"]
     achieved = dom_bytes / (kern_avg_ms / 1e3) / 1e9
-    traffic = read_traffic(args.path)
+    pol = bsa.bsa_select_policy(rows, w.M, K, bsa.BSA_DTYPE_BF16,
+                                torch.cuda.get_device_properties(device).multi_processor_count)
+    kernel = KERNEL_OF_PATH[pol["path"]]
+    traffic = read_traffic(args.path, kernel, K, w.B)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -321,8 +339,7 @@ def run_ours(args):
         "hbm_frac_of_peak": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
-                     "kernel": "pair_select_kernel (fused sparse-table epilogue)"
-                     if args.path == "fused" else "pair_select_kernel",
+                     "kernel": dominant_kernel(pol["path"], args.path == "fused"),
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
                      "traffic_note": None if traffic is None else traffic.get("note")},

@@ -26,3 +26,23 @@ def test_algorithmic_bytes_hand_example():
     assert b["fused"] == 140 + 56 + 792
     assert b["table_builder"] == 96 + 12 + 56 + 792
     assert b["per_row_fused"] == (140 + 56 + 792) / 6
+
+
+def test_roofline_kernel_and_traffic_follow_the_policy():
+    """The bench names the selector kernel the launch policy picks, and takes
+    committed ncu traffic only for the kernel, topk and request count it was
+    captured on."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import block_sparse_attention_topk_gb300 as bsa
+    rows = 131072 * 2
+    p16 = bsa.bsa_select_policy(rows, 1024, 16, bsa.BSA_DTYPE_BF16, 152)
+    p64 = bsa.bsa_select_policy(rows, 1024, 64, bsa.BSA_DTYPE_BF16, 152)
+    assert bench.KERNEL_OF_PATH[p16["path"]] == "pair_select_kernel"
+    assert bench.KERNEL_OF_PATH[p64["path"]] == "select_kernel"
+    assert bench.dominant_kernel(p64["path"], True).startswith("select_kernel (fused")
+    for path in ("fused", "unfused"):
+        assert bench.read_traffic(path, "pair_select_kernel", 16, 131072) is not None
+        assert bench.read_traffic(path, "select_kernel", 64, 131072) is None
+        assert bench.read_traffic(path, "pair_select_kernel", 32, 131072) is None
+        assert bench.read_traffic(path, "pair_select_kernel", 16, 65536) is None
