@@ -153,6 +153,37 @@ def check_table_full_selection_covers_causal_len(lib=None, seed=3):
             assert (bt[q, 0, npages:] == 0).all()
 
 
+def check_table_input_order_irrelevant(lib=None, seed=21):
+    """The table keeps the valid distinct ids in ascending order ([47984]
+    sections 实现拆解 item 3 and 关键源码片段, under the ascending reading), so
+    reordering a row's ids changes nothing; a row of one repeated id gives
+    the table of that id alone; and each kept block's entries come in
+    ascending block order."""
+    rng = np.random.default_rng(seed)
+    for _ in range(40):
+        K = int(rng.integers(2, 65))
+        nblk = 96
+        seq = int(rng.integers(0, nblk * 128 + 100))
+        table = rng.permutation(1 << 20)[:nblk].astype(np.int32)[None, :]  # distinct
+        row = rng.integers(-2, nblk + 3, size=K).astype(np.int32)
+        rows = [row, row[::-1].copy(), rng.permutation(row)]
+        outs = [oracle.build_sparse_block_table(r[None, None, :], table, [seq], 1, lib=lib)
+                for r in rows]
+        for bt, ctx in outs[1:]:
+            assert (bt == outs[0][0]).all() and (ctx == outs[0][1]).all()
+        bt = outs[0][0][0, 0]
+        block_of = {int(table[0, b]) * 8: b for b in range(nblk)}
+        kept = sorted({int(x) for x in row if 0 <= x < min(-(-seq // 128), nblk)})
+        assert [block_of.get(int(bt[8 * j]), -1) for j in range(len(kept))] == kept
+        b = int(rng.integers(0, nblk))
+        same = np.full((1, 1, K), b, dtype=np.int32)
+        one = np.full((1, 1, K), -1, dtype=np.int32)
+        one[0, 0, 0] = b
+        t1, c1 = oracle.build_sparse_block_table(same, table, [seq], 1, lib=lib)
+        t2, c2 = oracle.build_sparse_block_table(one, table, [seq], 1, lib=lib)
+        assert (t1 == t2).all() and (c1 == c2).all()
+
+
 def _rand_row_bits(rng, v, is_bf16, palette_frac=0.5):
     """Row of bit patterns mixing a small palette (ties, NaN, +-0, +-Inf) and
     random finite values."""
@@ -254,6 +285,7 @@ ALL_CHECKS = [
     check_spec_decode_worked_example,
     check_table_duplicates_ignored,
     check_table_full_selection_covers_causal_len,
+    check_table_input_order_irrelevant,
     check_select_brute_force,
     check_select_lexsort_special_case,
     check_select_short_rows_take_everything,

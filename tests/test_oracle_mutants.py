@@ -55,6 +55,8 @@ MUTANTS = [
     ("table_phys_scale",
      "bt[j * ORACLE_PAGES_PER_BLOCK + p] = phys * ORACLE_PAGES_PER_BLOCK + p;",
      "bt[j * ORACLE_PAGES_PER_BLOCK + p] = phys + p;"),
+    ("table_unsorted",
+     "qsort(blocks, (size_t)n, sizeof(int32_t), int32_ascending);", ""),
     ("table_row_mapping",
      "int64_t local_q = r % dql;", "int64_t local_q = dql - 1 - r % dql;"),
 ]
