@@ -177,13 +177,19 @@ def build_sparse_block_table(topk_idx, block_table, seq_lens, dql: int, lib=None
 
 def topk_select_sparse_table(scores, seq_lens, dql: int, K: int, num_init: int,
                              num_local: int, block_table, token_stride: int | None = None,
-                             head_stride: int | None = None, lib=None):
-    """Returns (out_idx [T,H,K], sparse_bt [T,H,K*8], sparse_ctx [T,H])."""
+                             head_stride: int | None = None, H: int | None = None,
+                             M: int | None = None, lib=None):
+    """Returns (out_idx [T,H,K], sparse_bt [T,H,K*8], sparse_ctx [T,H]).
+    `scores` is a [T, H, M] buffer, or a flat buffer with explicit H, M and
+    strides (a capacity-wide or padded layout)."""
     bits, dtype = _score_bits(scores)
-    T, H, M = bits.shape
+    if H is None:
+        T, H, M = bits.shape
     s = _i32(seq_lens)
     B = s.shape[0]
-    assert T == B * dql
+    T = B * dql
+    if bits.ndim == 3:
+        assert bits.shape[0] == T
     bt = _i32(block_table)
     MB = bt.shape[1]
     if head_stride is None:

@@ -276,6 +276,136 @@ def check_select_ties_lower_id(lib=None):
     assert list(got) == [0, 1, 2, 7]
 
 
+def _fused(flat, seq, dql, K, I, L, table, ts, hs, H, M, lib):
+    """The fused oracle on a flat buffer; an error return counts as a
+    failed pin (a mutant that breaks the call must not pass silently)."""
+    try:
+        return oracle.topk_select_sparse_table(flat, seq, dql, K, I, L, table, token_stride=ts,
+                                               head_stride=hs, H=H, M=M, lib=lib)
+    except ValueError as e:
+        raise AssertionError(f"fused oracle rejected a valid call: {e}")
+
+
+def _fused_layout(rng, B, dql, H, M, is_bf16):
+    """A flat score buffer with a capacity-wide head stride and a padded token
+    stride.  The tiles between M and the head stride hold +NaN (the largest
+    value), so a read past M would change the selection; the buffer has
+    spare room at its end so that a layout mistake reads defined memory."""
+    T = B * dql
+    hs = M + int(rng.integers(0, 10))
+    ts = H * hs + int(rng.integers(0, 6))
+    n = (T + H + 1) * ts + M
+    bits = _rand_row_bits(rng, n, is_bf16, palette_frac=0.3)
+    flat = np.array(bits, dtype=np.uint16 if is_bf16 else np.uint32)
+    nan = 0x7FC0 if is_bf16 else 0x7FC00000
+    for t in range(T):
+        for h in range(H):
+            base = t * ts + h * hs
+            flat[base + M:base + hs] = nan
+    return flat, ts, hs
+
+
+def _seq_lens_mix(rng, B, dql, M):
+    """Padded requests, requests shorter than dql, lengths straddling 128-token
+    boundaries, and contexts longer than the M-block capacity."""
+    out = []
+    for _ in range(B):
+        kind = int(rng.integers(0, 5))
+        if kind == 0:
+            out.append(0)
+        elif kind == 1:
+            out.append(int(rng.integers(1, dql + 1)))
+        elif kind == 2:
+            out.append(128 * int(rng.integers(1, M + 1)) + int(rng.integers(-dql, dql + 1)))
+        elif kind == 3:
+            out.append(int(rng.integers(128 * M, 128 * M + 600)))
+        else:
+            out.append(int(rng.integers(1, 128 * M)))
+    return np.maximum(np.array(out, dtype=np.int64), 0).astype(np.int32)
+
+
+def check_fused_equals_select_then_table(lib=None, trials=60, seed=31):
+    """The fused oracle is, by definition ([55235] 实现拆解: the sparse table is
+    emitted from the selector's result; [47984] 关键源码片段: row = req * dql +
+    local_q), the decode page count, then the selection, then the table.
+    Compared element by element with those three pinned steps called one by
+    one, on query lengths 1-4, 1-3 heads, capacity-wide and padded score
+    layouts, padded and short requests, and block tables narrower than the
+    causal range."""
+    rng = np.random.default_rng(seed)
+    for trial in range(trials):
+        is_bf16 = bool(trial % 2)
+        dql = int(rng.integers(1, 5))
+        H = int(rng.integers(1, 4))
+        B = int(rng.integers(1, 7))
+        M = int(rng.integers(4, 41))
+        I = int(rng.integers(0, 3))
+        L = int(rng.integers(0, 3))
+        K = int(rng.integers(max(1, I + L), max(1, I + L) + 12))
+        flat, ts, hs = _fused_layout(rng, B, dql, H, M, is_bf16)
+        seq = _seq_lens_mix(rng, B, dql, M)
+        MB = int(rng.integers(1, M + 4))
+        table = rng.permutation(1 << 20)[:B * MB].astype(np.int32).reshape(B, MB)
+        T = B * dql
+        idx, bt, ctx = _fused(flat, seq, dql, K, I, L, table, ts, hs, H, M, lib)
+        nvp = oracle.num_valid_pages_decode(seq, dql, lib=lib)
+        idx2 = oracle.topk_select(flat, nvp, K, I, L, token_stride=ts, head_stride=hs, T=T, H=H,
+                                  M=M, lib=lib)
+        bt2, ctx2 = oracle.build_sparse_block_table(idx2, table, seq, dql, lib=lib)
+        ctxt = (trial, dql, H, B, M, K, I, L)
+        assert (idx == idx2).all(), ("ids", ctxt)
+        assert (bt == bt2).all(), ("table", ctxt)
+        assert (ctx == ctx2).all(), ("ctx", ctxt)
+
+
+def check_fused_token_enumeration(lib=None, trials=150, seed=32):
+    """Tiny fused calls against an independent formulation: the causal blocks
+    are found by listing the query's tokens 0 .. pos one by one, the selection
+    by subset enumeration (brute force), and each kept block's table entries
+    and ctx by listing its causal tokens and the page-16 pages they fall in."""
+    rng = np.random.default_rng(seed)
+    for trial in range(trials):
+        is_bf16 = bool(trial % 2)
+        dql = int(rng.integers(1, 5))
+        H = int(rng.integers(1, 4))
+        B = int(rng.integers(1, 4))
+        M = int(rng.integers(1, 9))
+        I = int(rng.integers(0, 3))
+        L = int(rng.integers(0, 3))
+        K = int(rng.integers(max(1, I + L), max(1, I + L) + 6))
+        flat, ts, hs = _fused_layout(rng, B, dql, H, M, is_bf16)
+        seq = _seq_lens_mix(rng, B, dql, M)
+        MB = int(rng.integers(1, M + 3))
+        table = rng.permutation(1 << 20)[:B * MB].astype(np.int32).reshape(B, MB)
+        idx, bt, ctx = _fused(flat, seq, dql, K, I, L, table, ts, hs, H, M, lib)
+        for req in range(B):
+            for q in range(dql):
+                row = req * dql + q
+                last = int(seq[req]) - dql + q          # query position
+                tokens = range(0, last + 1)             # empty when last < 0
+                v = min(M, len({x // 128 for x in tokens}))
+                for h in range(H):
+                    base = row * ts + h * hs
+                    bits = [int(b) for b in flat[base:base + M]]
+                    sols = _pins.brute_force_select(bits, v, K, I, L, is_bf16)
+                    assert len(sols) == 1
+                    sel = sols[0]
+                    want_idx = sel + [-1] * (K - len(sel))
+                    assert list(idx[row, h]) == want_idx, (trial, row, h, list(idx[row, h]),
+                                                           want_idx)
+                    want_bt = [0] * (8 * K)
+                    want_ctx = 0
+                    kept = [b for b in sel if b < MB]
+                    for j, b in enumerate(kept):
+                        mine = [x for x in tokens if x // 128 == b]
+                        want_ctx += len(mine)
+                        for page in sorted({(x - 128 * b) // 16 for x in mine}):
+                            want_bt[8 * j + page] = int(table[req, b]) * 8 + page
+                    assert list(bt[row, h]) == want_bt, (trial, row, h)
+                    assert int(ctx[row, h]) == want_ctx, (trial, row, h, int(ctx[row, h]),
+                                                          want_ctx)
+
+
 ALL_CHECKS = [
     check_total_order_golden,
     check_total_order_exhaustive_bf16,
@@ -291,4 +421,6 @@ ALL_CHECKS = [
     check_select_short_rows_take_everything,
     check_select_forced_blocks,
     check_select_ties_lower_id,
+    check_fused_equals_select_then_table,
+    check_fused_token_enumeration,
 ]

@@ -59,6 +59,19 @@ MUTANTS = [
      "qsort(blocks, (size_t)n, sizeof(int32_t), int32_ascending);", ""),
     ("table_row_mapping",
      "int64_t local_q = r % dql;", "int64_t local_q = dql - 1 - r % dql;"),
+    # mistakes inside the fused composition (select, then table)
+    ("fused_strides_swapped",
+     "T, H, M, token_stride, head_stride, nvp, K,", "T, H, M, head_stride, token_stride, nvp, K,"),
+    ("fused_init_local_swapped",
+     "num_init, num_local, out_idx);", "num_local, num_init, out_idx);"),
+    ("fused_reads_capacity",
+     "T, H, M, token_stride, head_stride, nvp, K,", "T, H, head_stride, token_stride, head_stride, nvp, K,"),
+    ("fused_table_dql_one",
+     "B, MB, seq_lens,\n                                             dql, sparse_bt",
+     "B, MB, seq_lens,\n                                             1, sparse_bt"),
+    ("fused_table_from_page_counts",
+     "rc = oracle_build_sparse_block_table(out_idx, T, H, K, block_table, B, MB, seq_lens,",
+     "rc = oracle_build_sparse_block_table(out_idx, T, H, K, block_table, B, MB, nvp,"),
 ]
 
 
