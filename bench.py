@@ -216,12 +216,19 @@ def dominant_kernel(path_id: int, fused: bool) -> str:
     return name + " (fused sparse-table epilogue)" if fused else name
 
 
+def select_source_sha() -> str:
+    """First 16 hex digits of the sha256 of the selector's CUDA source."""
+    import hashlib
+    src = os.path.join(ROOT, "block_sparse_attention_topk_gb300", "csrc", "bsa_select.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
 def read_traffic(path_name: str, kernel: str = "pair_select_kernel", topk: int = 16,
-                 requests: int = 131072):
+                 requests: int = 131072, traffic_file: str | None = None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on this kernel, topk and request count and still describes the current
     kernel source."""
-    f = os.path.join(ROOT, "profiles", "traffic.json")
+    f = traffic_file or os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(f) as fh:
             d = json.load(fh)
@@ -231,10 +238,7 @@ def read_traffic(path_name: str, kernel: str = "pair_select_kernel", topk: int =
         if (not ent.get("kernel", "").startswith(kernel + "<") or ent.get("topk") != topk
                 or ent.get("requests") != requests):
             return None
-        import hashlib
-        src = os.path.join(ROOT, "block_sparse_attention_topk_gb300", "csrc", "bsa_select.cu")
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if ent.get("source_sha") != h:
+        if ent.get("source_sha") != select_source_sha():
             return None
         return ent
     except (OSError, ValueError):

@@ -88,12 +88,12 @@ def lib() -> ctypes.CDLL:
             L.bsa_topk_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
             L.bsa_topk_workspace_bytes.restype = sz
             L.bsa_topk_select.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i32, i32, i32,
-                                          vp, vp, sz, vp]
+                                          vp, i64, i64, vp, sz, vp]
             L.bsa_build_sparse_block_table.argtypes = [vp, i64, i64, i32, vp, i64, i64, vp, i32,
                                                        vp, vp, vp]
             L.bsa_topk_select_sparse_table.argtypes = [vp, i32, i64, i32, i64, i64, i64, i64, vp,
-                                                       i32, i32, i32, vp, i64, vp, vp, vp, vp, sz,
-                                                       vp]
+                                                       i32, i32, i32, vp, i64, vp, i64, i64, vp,
+                                                       vp, vp, sz, vp]
             L.bsa_select_policy.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(LaunchPolicy)]
             L.bsa_topk_select_noalloc.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i32, i32,
                                                   i32, vp, vp]
@@ -109,6 +109,14 @@ def _check(fn: str, status: int):
         raise BsaError(fn, status, lib().bsa_status_string(status).decode())
 
 
+def _call(fn: str, device: torch.device, *args):
+    """Calls C entry point `fn` with `device` current: the library takes the
+    launch policy's SM count, the workspace size and its scratch address from
+    the current device."""
+    with torch.cuda.device(device):
+        _check(fn, getattr(lib(), fn)(*args))
+
+
 def _stream(device: torch.device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
@@ -117,10 +125,33 @@ def _ptr(t: torch.Tensor | None):
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
-def _dev_i32(t: torch.Tensor, name: str) -> torch.Tensor:
-    if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+def _dev_i32(t: torch.Tensor, name: str, device: torch.device | None = None,
+             shape: tuple | None = None) -> torch.Tensor:
+    """A contiguous int32 CUDA tensor, on `device` and of `shape` when given;
+    raises ValueError before anything is launched otherwise."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 \
+            or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     return t
+
+
+def _out_idx(t: torch.Tensor, T: int, H: int, K: int, device: torch.device):
+    """An int32 [T, H, K] output view whose K slots are contiguous (token-major,
+    or a transpose(0, 1) view of a head-major [H, T, K] buffer); returns its
+    (token, head) element strides."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32:
+        raise ValueError("out_idx must be an int32 CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"out_idx is on {t.device}, expected {device}")
+    if tuple(t.shape) != (T, H, K):
+        raise ValueError(f"out_idx has shape {tuple(t.shape)}, expected {(T, H, K)}")
+    if K > 1 and t.stride(2) != 1:
+        raise ValueError("out_idx must be contiguous along its topk dimension")
+    return t.stride(0), t.stride(1)
 
 
 def _score_dtype(scores: torch.Tensor) -> int:
@@ -131,9 +162,9 @@ def _score_dtype(scores: torch.Tensor) -> int:
     raise ValueError(f"scores must be bfloat16 or float32, not {scores.dtype}")
 
 
-# One workspace per device, grown on demand (the library clears the parts it
-# needs cleared on every call).  Calls that share it must not overlap on the
-# GPU: pass your own workspace for concurrent streams.
+# One workspace per (device, stream), grown on demand (the library clears the
+# parts it needs cleared on every call).  Calls on one stream run in order,
+# so they may share it; calls on different streams get different buffers.
 _ws_cache: dict = {}
 _ws_lock = threading.Lock()
 
@@ -141,7 +172,7 @@ _ws_lock = threading.Lock()
 def _workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
     if nbytes == 0:
         return None
-    key = (device.type, device.index)
+    key = (device.type, device.index, torch.cuda.current_stream(device).cuda_stream)
     with _ws_lock:
         ws = _ws_cache.get(key)
         if ws is None or ws.numel() < nbytes:
@@ -150,8 +181,22 @@ def _workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
         return ws
 
 
-def bsa_topk_workspace_bytes(T: int, H: int, M: int, K: int, dtype: int) -> int:
-    return int(lib().bsa_topk_workspace_bytes(T, H, M, K, dtype))
+def _workspace_arg(workspace: torch.Tensor | None, device: torch.device, need: int):
+    if workspace is None:
+        workspace = _workspace(device, need)
+    elif not workspace.is_cuda or workspace.device != device or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return workspace, nbytes
+
+
+def bsa_topk_workspace_bytes(T: int, H: int, M: int, K: int, dtype: int,
+                             device: torch.device | None = None) -> int:
+    """Workspace bytes for these sizes on `device` (default: the current one)."""
+    if device is None:
+        return int(lib().bsa_topk_workspace_bytes(T, H, M, K, dtype))
+    with torch.cuda.device(device):
+        return int(lib().bsa_topk_workspace_bytes(T, H, M, K, dtype))
 
 
 def bsa_select_policy(rows: int, M: int, K: int, dtype: int, num_sms: int = 152) -> dict:
@@ -163,35 +208,38 @@ def bsa_select_policy(rows: int, M: int, K: int, dtype: int, num_sms: int = 152)
 
 def bsa_num_valid_pages_decode(seq_lens: torch.Tensor, decode_query_len: int,
                                out: torch.Tensor | None = None) -> torch.Tensor:
+    dev = seq_lens.device
     _dev_i32(seq_lens, "seq_lens")
+    if seq_lens.dim() != 1:
+        raise ValueError("seq_lens must be 1-D [num_reqs]")
     T = seq_lens.shape[0] * decode_query_len
     if out is None:
-        out = torch.empty(T, dtype=torch.int32, device=seq_lens.device)
-    _dev_i32(out, "out")
-    _check("bsa_num_valid_pages_decode",
-           lib().bsa_num_valid_pages_decode(_ptr(seq_lens), seq_lens.shape[0], decode_query_len,
-                                            _ptr(out), _stream(seq_lens.device)))
+        out = torch.empty(T, dtype=torch.int32, device=dev)
+    _dev_i32(out, "out", dev, (T,))
+    _call("bsa_num_valid_pages_decode", dev, _ptr(seq_lens), seq_lens.shape[0],
+          decode_query_len, _ptr(out), _stream(dev))
     return out
 
 
 def bsa_num_valid_pages_varlen(cu_seqlens_q: torch.Tensor, prefix_lens: torch.Tensor,
                                total_q: int, out: torch.Tensor | None = None) -> torch.Tensor:
-    _dev_i32(cu_seqlens_q, "cu_seqlens_q")
-    _dev_i32(prefix_lens, "prefix_lens")
+    dev = cu_seqlens_q.device
+    _dev_i32(prefix_lens, "prefix_lens", dev)
+    if prefix_lens.dim() != 1:
+        raise ValueError("prefix_lens must be 1-D [num_seqs]")
+    _dev_i32(cu_seqlens_q, "cu_seqlens_q", dev, (prefix_lens.shape[0] + 1,))
     if out is None:
-        out = torch.empty(total_q, dtype=torch.int32, device=cu_seqlens_q.device)
-    _dev_i32(out, "out")
-    _check("bsa_num_valid_pages_varlen",
-           lib().bsa_num_valid_pages_varlen(_ptr(cu_seqlens_q), _ptr(prefix_lens),
-                                            prefix_lens.shape[0], total_q, _ptr(out),
-                                            _stream(cu_seqlens_q.device)))
+        out = torch.empty(total_q, dtype=torch.int32, device=dev)
+    _dev_i32(out, "out", dev, (total_q,))
+    _call("bsa_num_valid_pages_varlen", dev, _ptr(cu_seqlens_q), _ptr(prefix_lens),
+          prefix_lens.shape[0], total_q, _ptr(out), _stream(dev))
     return out
 
 
 def _score_view(scores: torch.Tensor, M: int | None):
-    if scores.dim() != 3 or not scores.is_cuda:
+    if not isinstance(scores, torch.Tensor) or scores.dim() != 3 or not scores.is_cuda:
         raise ValueError("scores must be a 3-D CUDA tensor [T, H, tiles]")
-    if scores.stride(2) != 1:
+    if scores.shape[2] > 1 and scores.stride(2) != 1:
         raise ValueError("scores must be contiguous along the tile dimension")
     T, H, cap = scores.shape
     M = cap if M is None else int(M)
@@ -204,21 +252,20 @@ def bsa_topk_select(scores: torch.Tensor, num_valid_pages: torch.Tensor, K: int,
                     num_init: int = 1, num_local: int = 1, out_idx: torch.Tensor | None = None,
                     M: int | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """scores [T, H, tiles] (bf16/fp32, tile dim contiguous; M = tiles used,
-    default all), num_valid_pages int32[T] -> out_idx int32 [T, H, K]."""
+    default all), num_valid_pages int32[T] -> out_idx int32 [T, H, K].  A
+    given out_idx may be any [T, H, K] view with contiguous topk slots, e.g.
+    ``buf.transpose(0, 1)`` of a head-major [H, T, K] buffer."""
     T, H, M, ts, hs = _score_view(scores, M)
     dt = _score_dtype(scores)
-    _dev_i32(num_valid_pages, "num_valid_pages")
+    dev = scores.device
+    _dev_i32(num_valid_pages, "num_valid_pages", dev, (T,))
     if out_idx is None:
-        out_idx = torch.empty((T, H, K), dtype=torch.int32, device=scores.device)
-    _dev_i32(out_idx, "out_idx")
-    need = bsa_topk_workspace_bytes(T, H, M, K, dt)
-    if workspace is None:
-        workspace = _workspace(scores.device, need)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check("bsa_topk_select",
-           lib().bsa_topk_select(_ptr(scores), dt, T, H, M, ts, hs, _ptr(num_valid_pages), K,
-                                 num_init, num_local, _ptr(out_idx), _ptr(workspace), wbytes,
-                                 _stream(scores.device)))
+        out_idx = torch.empty((T, H, K), dtype=torch.int32, device=dev)
+    ots, ohs = _out_idx(out_idx, T, H, K, dev)
+    need = bsa_topk_workspace_bytes(T, H, M, K, dt, dev)
+    workspace, wbytes = _workspace_arg(workspace, dev, need)
+    _call("bsa_topk_select", dev, _ptr(scores), dt, T, H, M, ts, hs, _ptr(num_valid_pages), K,
+          num_init, num_local, _ptr(out_idx), ots, ohs, _ptr(workspace), wbytes, _stream(dev))
     return out_idx
 
 
@@ -227,20 +274,28 @@ def bsa_build_sparse_block_table(topk_idx: torch.Tensor, block_table: torch.Tens
                                  sparse_bt: torch.Tensor | None = None,
                                  sparse_ctx: torch.Tensor | None = None):
     """topk_idx int32 [T, H, K] -> (sparse_bt int32 [T, H, K*8], sparse_ctx int32 [T, H])."""
+    dev = topk_idx.device
     _dev_i32(topk_idx, "topk_idx")
-    _dev_i32(block_table, "block_table")
-    _dev_i32(seq_lens, "seq_lens")
+    if topk_idx.dim() != 3:
+        raise ValueError("topk_idx must be [T, H, K]")
     T, H, K = topk_idx.shape
-    B, MB = block_table.shape
+    _dev_i32(seq_lens, "seq_lens", dev)
+    if seq_lens.dim() != 1:
+        raise ValueError("seq_lens must be 1-D [num_reqs]")
+    B = seq_lens.shape[0]
+    _dev_i32(block_table, "block_table", dev)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"block_table has shape {tuple(block_table.shape)}, expected "
+                         f"[{B}, max_blocks]")
+    MB = block_table.shape[1]
     if sparse_bt is None:
-        sparse_bt = torch.empty((T, H, K * PAGES_PER_SPARSE_BLOCK), dtype=torch.int32,
-                                device=topk_idx.device)
+        sparse_bt = torch.empty((T, H, K * PAGES_PER_SPARSE_BLOCK), dtype=torch.int32, device=dev)
+    _dev_i32(sparse_bt, "sparse_bt", dev, (T, H, K * PAGES_PER_SPARSE_BLOCK))
     if sparse_ctx is None:
-        sparse_ctx = torch.empty((T, H), dtype=torch.int32, device=topk_idx.device)
-    _check("bsa_build_sparse_block_table",
-           lib().bsa_build_sparse_block_table(_ptr(topk_idx), T, H, K, _ptr(block_table), B, MB,
-                                              _ptr(seq_lens), decode_query_len, _ptr(sparse_bt),
-                                              _ptr(sparse_ctx), _stream(topk_idx.device)))
+        sparse_ctx = torch.empty((T, H), dtype=torch.int32, device=dev)
+    _dev_i32(sparse_ctx, "sparse_ctx", dev, (T, H))
+    _call("bsa_build_sparse_block_table", dev, _ptr(topk_idx), T, H, K, _ptr(block_table), B,
+          MB, _ptr(seq_lens), decode_query_len, _ptr(sparse_bt), _ptr(sparse_ctx), _stream(dev))
     return sparse_bt, sparse_ctx
 
 
@@ -251,31 +306,39 @@ def bsa_topk_select_sparse_table(scores: torch.Tensor, seq_lens: torch.Tensor,
                                  sparse_bt: torch.Tensor | None = None,
                                  sparse_ctx: torch.Tensor | None = None, M: int | None = None,
                                  workspace: torch.Tensor | None = None):
-    """Fused decode select + sparse table.  Returns (out_idx or None, sparse_bt, sparse_ctx)."""
+    """Fused decode select + sparse table over the first num_reqs *
+    decode_query_len token rows of `scores`.  Returns (out_idx or None,
+    sparse_bt, sparse_ctx); out_idx may be a strided view as for
+    bsa_topk_select."""
     _, H, M, ts, hs = _score_view(scores, M)
     dt = _score_dtype(scores)
-    _dev_i32(seq_lens, "seq_lens")
-    _dev_i32(block_table, "block_table")
-    B, MB = block_table.shape
-    T = seq_lens.shape[0] * decode_query_len
+    dev = scores.device
+    _dev_i32(seq_lens, "seq_lens", dev)
+    if seq_lens.dim() != 1:
+        raise ValueError("seq_lens must be 1-D [num_reqs]")
+    B = seq_lens.shape[0]
+    _dev_i32(block_table, "block_table", dev)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"block_table has shape {tuple(block_table.shape)}, expected "
+                         f"[{B}, max_blocks]")
+    MB = block_table.shape[1]
+    T = B * decode_query_len
     if scores.shape[0] < T:
         raise ValueError(f"scores holds {scores.shape[0]} token rows, need {T}")
-    dev = scores.device
     if want_idx and out_idx is None:
         out_idx = torch.empty((T, H, K), dtype=torch.int32, device=dev)
+    ots, ohs = (H * K, K) if out_idx is None else _out_idx(out_idx, T, H, K, dev)
     if sparse_bt is None:
         sparse_bt = torch.empty((T, H, K * PAGES_PER_SPARSE_BLOCK), dtype=torch.int32, device=dev)
+    _dev_i32(sparse_bt, "sparse_bt", dev, (T, H, K * PAGES_PER_SPARSE_BLOCK))
     if sparse_ctx is None:
         sparse_ctx = torch.empty((T, H), dtype=torch.int32, device=dev)
-    need = bsa_topk_workspace_bytes(T, H, M, K, dt)
-    if workspace is None:
-        workspace = _workspace(dev, need)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check("bsa_topk_select_sparse_table",
-           lib().bsa_topk_select_sparse_table(
-               _ptr(scores), dt, seq_lens.shape[0], decode_query_len, H, M, ts, hs,
-               _ptr(seq_lens), K, num_init, num_local, _ptr(block_table), MB, _ptr(out_idx),
-               _ptr(sparse_bt), _ptr(sparse_ctx), _ptr(workspace), wbytes, _stream(dev)))
+    _dev_i32(sparse_ctx, "sparse_ctx", dev, (T, H))
+    need = bsa_topk_workspace_bytes(T, H, M, K, dt, dev)
+    workspace, wbytes = _workspace_arg(workspace, dev, need)
+    _call("bsa_topk_select_sparse_table", dev, _ptr(scores), dt, B, decode_query_len, H, M, ts,
+          hs, _ptr(seq_lens), K, num_init, num_local, _ptr(block_table), MB, _ptr(out_idx), ots,
+          ohs, _ptr(sparse_bt), _ptr(sparse_ctx), _ptr(workspace), wbytes, _stream(dev))
     return out_idx, sparse_bt, sparse_ctx
 
 
@@ -285,15 +348,15 @@ def bsa_topk_select_noalloc(scores: torch.Tensor, num_valid_pages: torch.Tensor,
                             M: int | None = None) -> torch.Tensor:
     """bsa_topk_select without a workspace argument, for callers that cannot
     allocate device memory: the library's own fixed device array serves as
-    scratch (see include/bsa_topk.h).  Same results as bsa_topk_select."""
+    scratch (see include/bsa_topk.h).  Same results as bsa_topk_select;
+    out_idx is token-major and contiguous."""
     T, H, M, ts, hs = _score_view(scores, M)
     dt = _score_dtype(scores)
-    _dev_i32(num_valid_pages, "num_valid_pages")
+    dev = scores.device
+    _dev_i32(num_valid_pages, "num_valid_pages", dev, (T,))
     if out_idx is None:
-        out_idx = torch.empty((T, H, K), dtype=torch.int32, device=scores.device)
-    _dev_i32(out_idx, "out_idx")
-    _check("bsa_topk_select_noalloc",
-           lib().bsa_topk_select_noalloc(_ptr(scores), dt, T, H, M, ts, hs, _ptr(num_valid_pages),
-                                         K, num_init, num_local, _ptr(out_idx),
-                                         _stream(scores.device)))
+        out_idx = torch.empty((T, H, K), dtype=torch.int32, device=dev)
+    _dev_i32(out_idx, "out_idx", dev, (T, H, K))
+    _call("bsa_topk_select_noalloc", dev, _ptr(scores), dt, T, H, M, ts, hs,
+          _ptr(num_valid_pages), K, num_init, num_local, _ptr(out_idx), _stream(dev))
     return out_idx

@@ -73,6 +73,26 @@ int check_topk_args(int64_t M, int32_t K, int32_t num_init, int32_t num_local) {
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? BSA_OK : (int)e; }
 
+// Rows (t, h) of out_idx start at t * ots + h * ohs and hold K contiguous
+// slots.  Accepted when no two rows can overlap: with the dimensions of more
+// than one entry ordered by stride, the inner stride is at least K and the
+// outer one clears the last inner row.
+int check_out_layout(int64_t T, int64_t H, int32_t K, int64_t ots, int64_t ohs) {
+    if (ots < 0 || ohs < 0) return BSA_ERR_SHAPE;
+    int64_t n[2], st[2];
+    int d = 0;
+    if (T > 1) { n[d] = T; st[d] = ots; ++d; }
+    if (H > 1) { n[d] = H; st[d] = ohs; ++d; }
+    if (d == 1 && st[0] < K) return BSA_ERR_SHAPE;
+    if (d == 2) {
+        const int in = st[0] <= st[1] ? 0 : 1;
+        const int out = 1 - in;
+        if (st[in] < K) return BSA_ERR_SHAPE;
+        if (st[out] < (n[in] - 1) * st[in] + K) return BSA_ERR_SHAPE;
+    }
+    return BSA_OK;
+}
+
 // BSA_SELECT_PATH=row|group|pair overrides the policy's choice among the
 // paths that can serve a call (for benchmarking); -1 when unset.
 int forced_path() {
@@ -266,13 +286,16 @@ int bsa_num_valid_pages_varlen(const int32_t* cu_seqlens_q, const int32_t* prefi
 int bsa_topk_select(const void* scores, int32_t dtype, int64_t T, int64_t H, int64_t M,
                     int64_t token_stride, int64_t head_stride, const int32_t* num_valid_pages,
                     int32_t K, int32_t num_init, int32_t num_local, int32_t* out_idx,
-                    void* workspace, size_t workspace_bytes, void* stream) {
+                    int64_t out_token_stride, int64_t out_head_stride, void* workspace,
+                    size_t workspace_bytes, void* stream) {
     if (dtype != BSA_DTYPE_BF16 && dtype != BSA_DTYPE_FP32) return BSA_ERR_DTYPE;
     if (T < 0 || H < 0 || M < 1 || M > BSA_MAX_K_TILES) return BSA_ERR_SHAPE;
     int rc = check_topk_args(M, K, num_init, num_local);
     if (rc != BSA_OK) return rc;
     if (head_stride < M || token_stride < (H > 0 ? (H - 1) * head_stride + M : M))
         return BSA_ERR_SHAPE;
+    rc = check_out_layout(T, H, K, out_token_stride, out_head_stride);
+    if (rc != BSA_OK) return rc;
     if (T == 0 || H == 0) return BSA_OK;
     if (scores == nullptr || num_valid_pages == nullptr || out_idx == nullptr) return BSA_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(scores) % elem_bytes(dtype)) != 0) return BSA_ERR_ALIGN;
@@ -290,6 +313,8 @@ int bsa_topk_select(const void* scores, int32_t dtype, int64_t T, int64_t H, int
     a.num_init = num_init;
     a.num_local = num_local;
     a.out_idx = out_idx;
+    a.out_ts = out_token_stride;
+    a.out_hs = out_head_stride;
     a.fused = false;
     return run_select(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
@@ -318,9 +343,10 @@ int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_
                                  int64_t token_stride, int64_t head_stride,
                                  const int32_t* seq_lens, int32_t K, int32_t num_init,
                                  int32_t num_local, const int32_t* block_table,
-                                 int64_t max_blocks, int32_t* out_idx, int32_t* sparse_bt,
-                                 int32_t* sparse_ctx, void* workspace, size_t workspace_bytes,
-                                 void* stream) {
+                                 int64_t max_blocks, int32_t* out_idx,
+                                 int64_t out_token_stride, int64_t out_head_stride,
+                                 int32_t* sparse_bt, int32_t* sparse_ctx, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
     if (dtype != BSA_DTYPE_BF16 && dtype != BSA_DTYPE_FP32) return BSA_ERR_DTYPE;
     if (num_reqs < 0 || decode_query_len < 1 || H < 0 || M < 1 || M > BSA_MAX_K_TILES ||
         max_blocks < 0)
@@ -330,6 +356,10 @@ int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_
     if (head_stride < M || token_stride < (H > 0 ? (H - 1) * head_stride + M : M))
         return BSA_ERR_SHAPE;
     const int64_t T = num_reqs * decode_query_len;
+    if (out_idx != nullptr) {
+        rc = check_out_layout(T, H, K, out_token_stride, out_head_stride);
+        if (rc != BSA_OK) return rc;
+    }
     if (T == 0 || H == 0) return BSA_OK;
     if (scores == nullptr || seq_lens == nullptr || sparse_bt == nullptr ||
         sparse_ctx == nullptr || (max_blocks > 0 && block_table == nullptr))
@@ -349,6 +379,8 @@ int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_
     a.num_init = num_init;
     a.num_local = num_local;
     a.out_idx = out_idx;
+    a.out_ts = out_token_stride;
+    a.out_hs = out_head_stride;
     a.block_table = block_table;
     a.max_blocks = max_blocks;
     a.sparse_bt = sparse_bt;

@@ -98,6 +98,7 @@ struct SelectArgs {
     int32_t dql;
     int32_t K, num_init, num_local;
     int32_t* out_idx;                 // may be null in fused mode
+    int64_t out_ts, out_hs;           // element strides of out_idx rows (token, head)
     const int32_t* block_table;       // fused mode
     int64_t max_blocks;
     int32_t* sparse_bt;

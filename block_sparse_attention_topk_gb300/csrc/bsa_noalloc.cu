@@ -11,11 +11,12 @@
 // fixed file-scope device array and forwards to bsa_topk_select.
 //
 // The array's device address is looked up once per device (with that device
-// current) on the first call made on it; that first call should therefore
-// come before any stream capture.  Every later call on the device reuses the
-// same array, so calls that overlap on the GPU (other streams, other host
-// threads) race on it.  The merge tickets the split path needs at zero are
-// cleared by bsa_topk_select on every call; nothing else must start at zero.
+// current) by the first call made on it, whether or not that call needs
+// scratch; that first call should therefore come before any stream capture.
+// Every later call on the device reuses the same array, so calls that overlap
+// on the GPU (other streams, other host threads) race on it.  The merge
+// tickets the split path needs at zero are cleared by bsa_topk_select on every
+// call; nothing else must start at zero.
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -61,12 +62,13 @@ extern "C" int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_
                                        void* stream) {
     const size_t need = bsa_topk_workspace_bytes(T, H, M, K, dtype);
     if (need > kScratchBytes) return BSA_ERR_CAPACITY;
+    // Looked up on every call (a cached read after the first), so that the
+    // lookup never waits for the first call that needs scratch.
     void* ws = nullptr;
-    if (need > 0) {
-        const cudaError_t e = scratch_address(&ws);
-        if (e != cudaSuccess) return (int)e;
-    }
+    const cudaError_t e = scratch_address(&ws);
+    if (e != cudaSuccess) return (int)e;
+    // token-major [T, H, K] output
     return bsa_topk_select(scores, dtype, T, H, M, token_stride, head_stride, num_valid_pages,
-                           K, num_init, num_local, out_idx, ws, need > 0 ? kScratchBytes : 0,
-                           stream);
+                           K, num_init, num_local, out_idx, H * (int64_t)K, (int64_t)K, ws,
+                           need > 0 ? kScratchBytes : 0, stream);
 }

@@ -1,8 +1,9 @@
 // bsa_select.cu -- the top-k block selector (plain and fused with the sparse
 // block table) for GB300 / sm_103a.
 //
-// What it computes (vLLM PR #47502 report, "Using sparse_topk_select from MSA
-// instead of triton kernels", sections 实现拆解 and 关键源码片段, indexer_msa.py):
+// What it computes (vLLM PR #47502 report, "[Minimax-M3] Using
+// tok_sparse_select from MSA instead of triton kernels", sections 实现拆解 and
+// 关键源码片段, indexer_msa.py):
 // for every row (token t, index head h) of the unified token-major score
 // buffer, the top-K block ids among the causal prefix b < v = min(M,
 // num_valid_pages[t]), with the init blocks [0, I) and the local blocks
@@ -299,13 +300,13 @@ __device__ __forceinline__ int32_t selected_id(int j, int lo, int hi, int kp, bo
     return hi + (j - lo - kp);
 }
 
-__device__ void write_outputs(const KernelParams& P, int64_t row, int n, int lo, int hi, int kp,
-                              bool all, const int32_t* buf_ids, int64_t causal_len,
-                              int64_t req, int lane) {
+__device__ void write_outputs(const KernelParams& P, int64_t row, int64_t t, int64_t h, int n,
+                              int lo, int hi, int kp, bool all, const int32_t* buf_ids,
+                              int64_t causal_len, int64_t req, int lane) {
     const SelectArgs& a = P.a;
     const int K = a.K;
     if (a.out_idx != nullptr) {
-        int32_t* out = a.out_idx + row * K;
+        int32_t* out = a.out_idx + t * a.out_ts + h * a.out_hs;
         for (int s = lane; s < K; s += 32)
             out[s] = s < n ? selected_id(s, lo, hi, kp, all, buf_ids) : -1;
     }
@@ -423,7 +424,8 @@ __device__ void warp_item(const KernelParams& P, int64_t row, int chunk, uint32_
         const bool all = ri.all, need = ri.need;
 
         if (!need) {
-            if (chunk == 0) write_outputs(P, row, n, lo, hi, kp, all, s_ids, causal_len, req, lane);
+            if (chunk == 0)
+                write_outputs(P, row, t, h, n, lo, hi, kp, all, s_ids, causal_len, req, lane);
             return;
         }
 
@@ -611,7 +613,7 @@ __device__ void warp_item(const KernelParams& P, int64_t row, int chunk, uint32_
             if (b.n > kp) buf_compact<E::kKeyBits, E::kKeyMax>(b, kp, lane);
         }
         __syncwarp();
-        write_outputs(P, row, n, lo, hi, kp, false, b.ids, causal_len, req, lane);
+        write_outputs(P, row, t, h, n, lo, hi, kp, false, b.ids, causal_len, req, lane);
         __syncwarp();
     }
 }
@@ -847,7 +849,9 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
     const bool fused = is_fused<FM>(a);
     int ctx = 0;
     if (write) {
-        int32_t* out = a.out_idx != nullptr ? a.out_idx + row * K : nullptr;
+        int32_t* out = a.out_idx != nullptr
+                           ? a.out_idx + (int64_t)r.t * a.out_ts + (int64_t)r.h * a.out_hs
+                           : nullptr;
         const int width = K * kPagesPerBlock;
         int32_t* bt = fused ? a.sparse_bt + row * (int64_t)width : nullptr;
         const int32_t* table = fused ? a.block_table + (int64_t)r.req * a.max_blocks : nullptr;

@@ -1,9 +1,11 @@
 // bsa_table.cu -- causal page counts and the page-16 sparse block table.
 //
-// Causal page count: vLLM PR #47502 report ("Using sparse_topk_select from MSA
-// instead of triton kernels"), section 关键源码片段, indexer_msa.py metadata
-// field "per-token causal page count cdiv(seq_pos+1, PAGE_SIZE)" with
-// PAGE_SIZE = 128, and the batch-wide topk_cu_seqlens_q / topk_prefix_lens.
+// Causal page count: vLLM PR #47502 report ("[Minimax-M3] Using
+// tok_sparse_select from MSA instead of triton kernels"), section 关键源码片段,
+// indexer_msa.py metadata: each token row gets the number of 128-token pages
+// that cover its positions 0 .. pos, i.e. ceil((pos + 1) / 128); varlen rows
+// take their positions from the batch-wide topk_cu_seqlens_q and
+// topk_prefix_lens.
 // Decode row mapping and the sparse table: vLLM PR #47984 report ("Support
 // speculative decode with AITER sparse PA"), sections 实现拆解 items 1-3 and
 // 关键源码片段: row = req*dql + local_q, query position

@@ -27,7 +27,9 @@
  *  - Pointers named in the signature are DEVICE pointers owned by the caller
  *    (except where a parameter says "host"); the library allocates nothing.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
- *    Calls are asynchronous on that stream and can be captured in a CUDA graph.
+ *    Calls are asynchronous on that stream.  Every call except
+ *    bsa_topk_select_noalloc (see its own note) can be captured in a CUDA
+ *    graph.
  *  - Outputs are written in full; callers need not clear them first.
  *  - Return value: BSA_OK (0) on success; a negative BSA_ERR_* when the host
  *    rejects the arguments (nothing is launched); a positive cudaError_t when
@@ -90,8 +92,9 @@ typedef struct bsa_launch_policy {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* bsa_status_string(int status);
 
-/* Causal page count of decode rows ([47502] metadata field comment
- * "cdiv(seq_pos+1, PAGE_SIZE)"; row mapping of [47984]):
+/* Causal page count of decode rows ([47502] 关键源码片段, indexer_msa.py
+ * metadata: the number of 128-token pages that cover positions 0 .. pos;
+ * row mapping of [47984]):
  *   row = req * decode_query_len + local_q,
  *   pos = seq_lens[req] - decode_query_len + local_q,
  *   num_valid_pages[row] = pos >= 0 ? cdiv(pos + 1, 128) : 0.
@@ -129,8 +132,14 @@ size_t bsa_topk_workspace_bytes(int64_t T, int64_t H, int64_t M, int32_t K, int3
  *   Row (t, h) selects n = min(K, v_t) block ids: the init blocks
  *   [0, min(num_init, v_t)), the local blocks [max(v_t - num_local, 0), v_t),
  *   and the best remaining ids by (totalOrder of the score descending, id
- *   ascending).  out_idx: int32[T, H, K] token-major; slots [0, n) hold the
- *   selected ids in ascending order, slots [n, K) hold -1.
+ *   ascending).  out_idx: int32, row (t, h) at out_idx + t * out_token_stride
+ *   + h * out_head_stride with its K slots contiguous; slots [0, n) hold the
+ *   selected ids in ascending order, slots [n, K) hold -1.  The token-major
+ *   [T, H, K] buffer of [47502] (实现拆解 item 4) has strides (H*K, K); a
+ *   head-major [H, T, K] buffer, the layout the Triton consumers of the
+ *   vLLM PR #49149 report keep (实现拆解 items 1-2, transpose(0, 1)), has
+ *   (K, T*K).  Layouts in which two rows could overlap are rejected
+ *   (BSA_ERR_SHAPE).
  *   workspace: device memory of at least bsa_topk_workspace_bytes(...) bytes,
  *   256-byte aligned, any contents.  When it is needed the call first clears
  *   the merge tickets with one cudaMemsetAsync on `stream` (captured as a
@@ -143,7 +152,8 @@ size_t bsa_topk_workspace_bytes(int64_t T, int64_t H, int64_t M, int32_t K, int3
 int bsa_topk_select(const void* scores, int32_t dtype, int64_t T, int64_t H, int64_t M,
                     int64_t token_stride, int64_t head_stride, const int32_t* num_valid_pages,
                     int32_t K, int32_t num_init, int32_t num_local, int32_t* out_idx,
-                    void* workspace, size_t workspace_bytes, void* stream);
+                    int64_t out_token_stride, int64_t out_head_stride, void* workspace,
+                    size_t workspace_bytes, void* stream);
 
 /* Page-16 sparse block table ([47984] minimax_m3_build_sparse_block_table_decode
  * and the hardened _build_sparse_block_table kernels).
@@ -172,7 +182,9 @@ int bsa_build_sparse_block_table(const int32_t* topk_idx, int64_t T, int64_t H, 
  * rows, computes the causal page count from seq_lens, runs the selection of
  * bsa_topk_select, and writes the sparse table of
  * bsa_build_sparse_block_table for the selected ids without a round trip of
- * the ids through memory.  out_idx may be NULL (ids not wanted).  Results are
+ * the ids through memory.  out_idx may be NULL (ids not wanted); when given, its
+ * layout follows out_token_stride / out_head_stride as for bsa_topk_select
+ * (the sparse table and ctx are always token-major).  Results are
  * identical to bsa_num_valid_pages_decode + bsa_topk_select +
  * bsa_build_sparse_block_table.  Workspace rules as for bsa_topk_select
  * (size from bsa_topk_workspace_bytes(T, H, M, K, dtype)).
@@ -182,9 +194,10 @@ int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_
                                  int64_t token_stride, int64_t head_stride,
                                  const int32_t* seq_lens, int32_t K, int32_t num_init,
                                  int32_t num_local, const int32_t* block_table,
-                                 int64_t max_blocks, int32_t* out_idx, int32_t* sparse_bt,
-                                 int32_t* sparse_ctx, void* workspace, size_t workspace_bytes,
-                                 void* stream);
+                                 int64_t max_blocks, int32_t* out_idx,
+                                 int64_t out_token_stride, int64_t out_head_stride,
+                                 int32_t* sparse_bt, int32_t* sparse_ctx, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* Size of the device scratch array behind bsa_topk_select_noalloc. */
 #define BSA_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -197,9 +210,10 @@ int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_
  * every GPU loading the library holds until the process exits.  Allocates
  * nothing.  Returns BSA_ERR_CAPACITY, before launching anything, when
  * bsa_topk_workspace_bytes(T, H, M, K, dtype) exceeds that size.  The first
- * call on a device looks the array's address up (cudaGetSymbolAddress), so it
- * should come before any stream capture.  All calls on a device share the
- * array: calls that overlap on the GPU race. */
+ * call on a device, whether or not it needs scratch, looks the array's
+ * address up (cudaGetSymbolAddress), so it should come before any stream
+ * capture.  All calls on a device share the array: calls that overlap on the
+ * GPU race.  out_idx is token-major int32[T, H, K]. */
 int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_t T, int64_t H, int64_t M,
                             int64_t token_stride, int64_t head_stride,
                             const int32_t* num_valid_pages, int32_t K, int32_t num_init,

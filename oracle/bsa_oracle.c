@@ -10,12 +10,12 @@
  * Everything here is the plain definition written out, in the order the
  * pages state it, with library sorts (qsort) as the only building block:
  *
- *  - causal page bound: "vLLM PR #47502 report" (Using sparse_topk_select
- *    from MSA instead of triton kernels), section 关键源码片段, indexer_msa.py:
- *    the metadata field comment "per-token causal page count
- *    cdiv(seq_pos+1, PAGE_SIZE)" with PAGE_SIZE = 128, and the module
- *    docstring (each row bounded by its causal page count, init/local blocks
- *    force-included, unwritten tail pre-filled with -inf).
+ *  - causal page bound: "vLLM PR #47502 report" ([Minimax-M3] Using
+ *    tok_sparse_select from MSA instead of triton kernels), section
+ *    关键源码片段, indexer_msa.py: the metadata holds, per token row, the
+ *    number of 128-token pages covering positions 0 .. pos, and the module
+ *    docstring bounds each row by that count, always keeps the init and local
+ *    blocks, and fills the unwritten tail with -inf.
  *  - total order incl. NaN, +-Inf, +-0 and ties: "vLLM PR #55235 report"
  *    ([ROCm][Perf] Tune MiniMax-M3 decode top-k for short contexts), sections
  *    执行摘要 and 评论区精华 (independent CPU total-order reference).  The

@@ -185,17 +185,22 @@ def long_decode(seed: int = 1003, device="cpu", B: int = 128, H: int = 2, M: int
 
 def mixed_prefill_decode(seed: int = 1004, device="cpu", num_decode: int = 32,
                          prefill_lens=(8192, 8192), H: int = 4, M: int = 128, K: int = 16,
-                         dtype=torch.float32) -> Workload:
+                         dtype=torch.float32, prefill_prefix=None,
+                         decode_max_prefix: int = 16383) -> Workload:
     """Unified buffer: 32 decode tokens (one per request, context before the
     token uniform in [0, 16383]) followed by two 8192-token prefills from
-    position 0; 4 index heads, 128-tile capacity, topk 16, fp32 N(0,1)."""
+    position 0; 4 index heads, 128-tile capacity, topk 16, fp32 N(0,1).
+    `prefill_prefix` gives each prefill chunk the context that precedes it
+    (default none), and `decode_max_prefix` the largest decode context, so
+    the same layout also describes long-context batches at a large capacity."""
     g = generator(seed, device)
-    dec_prefix = _uniform_int(0, 16383, num_decode, g, device)
+    dec_prefix = _uniform_int(0, decode_max_prefix, num_decode, g, device)
     qlens = [1] * num_decode + list(prefill_lens)
     cu = torch.tensor([0] + list(torch.tensor(qlens).cumsum(0).tolist()), dtype=torch.int32,
                       device=device)
-    prefix = torch.cat([dec_prefix, torch.zeros(len(prefill_lens), dtype=torch.int64,
-                                                device=device)]).to(torch.int32)
+    pre = [0] * len(prefill_lens) if prefill_prefix is None else list(prefill_prefix)
+    prefix = torch.cat([dec_prefix, torch.tensor(pre, dtype=torch.int64,
+                                                 device=device)]).to(torch.int32)
     T = int(cu[-1])
     sc = normal_scores((T, H, M), dtype, seed + 17, device)
     return Workload("mixed_prefill_decode", dtype, T, H, M, K, 1, 1, sc, cu_seqlens_q=cu,

@@ -137,27 +137,112 @@ def test_host_argument_checks_launch_nothing(bsa):
     L = bsa.lib()
     nul = ctypes.c_void_p(0)
     sel = L.bsa_topk_select
+    tm = (4, 4)   # token-major output strides for H = 1, K = 4
     # K out of range, K < init + local, unknown dtype, bad sizes, null pointers
-    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 0, 0, 0, nul, nul, 0, nul) == -3
-    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 33, 0, 0, nul, nul, 0, nul) == -3
-    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 2, 2, 1, nul, nul, 0, nul) == -3
-    assert sel(nul, 9, 4, 1, 32, 32, 32, nul, 4, 1, 1, nul, nul, 0, nul) == -4
-    assert sel(nul, 0, 4, 1, 0, 32, 32, nul, 4, 1, 1, nul, nul, 0, nul) == -2
-    assert sel(nul, 0, 4, 2, 32, 40, 32, nul, 4, 1, 1, nul, nul, 0, nul) == -2
-    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 4, 1, 1, nul, nul, 0, nul) == -1
+    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 0, 0, 0, nul, *tm, nul, 0, nul) == -3
+    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 33, 0, 0, nul, *tm, nul, 0, nul) == -3
+    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 2, 2, 1, nul, *tm, nul, 0, nul) == -3
+    assert sel(nul, 9, 4, 1, 32, 32, 32, nul, 4, 1, 1, nul, *tm, nul, 0, nul) == -4
+    assert sel(nul, 0, 4, 1, 0, 32, 32, nul, 4, 1, 1, nul, *tm, nul, 0, nul) == -2
+    assert sel(nul, 0, 4, 2, 32, 40, 32, nul, 4, 1, 1, nul, *tm, nul, 0, nul) == -2
+    assert sel(nul, 0, 4, 1, 32, 32, 32, nul, 4, 1, 1, nul, *tm, nul, 0, nul) == -1
     assert sel(ctypes.c_void_p(0x1001), 0, 4, 1, 32, 32, 32, ctypes.c_void_p(0x2000), 4, 1, 1,
-               ctypes.c_void_p(0x3000), nul, 0, nul) == -7
+               ctypes.c_void_p(0x3000), *tm, nul, 0, nul) == -7
     # empty batches are a no-op
-    assert sel(nul, 0, 0, 1, 32, 32, 32, nul, 4, 1, 1, nul, nul, 0, nul) == 0
+    assert sel(nul, 0, 0, 1, 32, 32, 32, nul, 4, 1, 1, nul, *tm, nul, 0, nul) == 0
     tbl = L.bsa_build_sparse_block_table
     assert tbl(nul, 5, 1, 4, nul, 2, 3, nul, 2, nul, nul, nul) == -6
     assert tbl(nul, 4, 1, 0, nul, 2, 3, nul, 2, nul, nul, nul) == -3
     assert tbl(nul, 4, 1, 4, nul, 2, 3, nul, 2, nul, nul, nul) == -1
     fused = L.bsa_topk_select_sparse_table
-    assert fused(nul, 0, 4, 0, 1, 32, 32, 32, nul, 4, 1, 1, nul, 3, nul, nul, nul, nul, 0,
+    assert fused(nul, 0, 4, 0, 1, 32, 32, 32, nul, 4, 1, 1, nul, 3, nul, *tm, nul, nul, nul, 0,
                  nul) == -2
-    assert fused(nul, 0, 4, 1, 1, 32, 32, 32, nul, 40, 1, 1, nul, 3, nul, nul, nul, nul, 0,
+    assert fused(nul, 0, 4, 1, 1, 32, 32, 32, nul, 40, 1, 1, nul, 3, nul, *tm, nul, nul, nul, 0,
                  nul) == -3
     assert L.bsa_num_valid_pages_decode(nul, 4, 0, nul, nul) == -2
     assert L.bsa_num_valid_pages_decode(nul, 4, 1, nul, nul) == -1
     assert L.bsa_num_valid_pages_varlen(nul, nul, 2, -1, nul, nul) == -2
+
+
+@pytest.mark.parametrize("T,H,K,ots,ohs,ok", [
+    (5, 3, 4, 12, 4, True),      # token-major [T, H, K]
+    (5, 3, 4, 4, 20, True),      # head-major [H, T, K] seen through transpose(0, 1)
+    (5, 3, 4, 16, 4, True),      # padded token rows
+    (5, 3, 4, 12, 3, False),     # slots of neighbouring heads overlap
+    (5, 3, 4, 4, 19, False),     # the last token row of head 0 runs into head 1
+    (5, 3, 4, 8, 4, False),      # token rows overlap the next token's heads
+    (5, 1, 4, 4, 0, True),       # one head: its stride is irrelevant
+    (1, 3, 4, 0, 4, True),       # one token: its stride is irrelevant
+    (5, 1, 4, 3, 0, False),
+    (5, 3, 4, -12, 4, False),
+])
+def test_output_layout_checks(bsa, T, H, K, ots, ohs, ok):
+    """Output strides are checked on the host: any layout in which two rows
+    (t, h) cannot overlap is accepted (the call then fails on its NULL
+    pointers, -1); others are rejected (-2)."""
+    L = bsa.lib()
+    nul = ctypes.c_void_p(0)
+    rc = L.bsa_topk_select(nul, 0, T, H, 32, 32 * H, 32, nul, K, 1, 1, nul, ots, ohs, nul, 0,
+                           nul)
+    assert rc == (-1 if ok else -2)
+    rc = L.bsa_topk_select_sparse_table(nul, 0, T, 1, H, 32, 32 * H, 32, nul, K, 1, 1, nul, 3,
+                                        ctypes.c_void_p(0x1000), ots, ohs, nul, nul, nul, 0, nul)
+    assert rc == (-1 if ok else -2)
+
+
+def test_binding_rejects_wrong_shapes_before_any_launch(bsa, monkeypatch):
+    """The binding checks every tensor's shape, dtype and device before it
+    calls the library; a mismatch is a ValueError, never an out-of-bounds
+    device access.  The C entry points are replaced by a recorder, so a
+    launch that should not happen is seen without a GPU."""
+    import torch
+    calls = []
+
+    class FakeLib:
+        def __getattr__(self, name):
+            def rec(*a):
+                calls.append(name)
+                return 0
+            return rec
+
+    def meta(shape, dtype=torch.int32):
+        return torch.empty(shape, dtype=dtype, device="meta")
+
+    monkeypatch.setattr(bsa, "lib", lambda: FakeLib())
+    # meta tensors (no memory) stand in for device tensors; is_cuda is
+    # patched so that the binding's shape checks are the ones reached
+    monkeypatch.setattr(torch.Tensor, "is_cuda", property(lambda self: True))
+    T, H, K, M = 6, 2, 4, 40
+    scores = meta((T, H, M), torch.bfloat16)
+    good_nvp = meta((T,))
+    with pytest.raises(ValueError, match="num_valid_pages"):
+        bsa.bsa_topk_select(scores, meta((T + 1,)), K, out_idx=meta((T, H, K)))
+    with pytest.raises(ValueError, match="out_idx"):
+        bsa.bsa_topk_select(scores, good_nvp, K, out_idx=meta((T, H, K + 1)))
+    with pytest.raises(ValueError, match="out_idx"):
+        bsa.bsa_topk_select(scores, good_nvp, K, out_idx=meta((H, T, K)).transpose(1, 2)[:, :, :])
+    seq = meta((3,))
+    with pytest.raises(ValueError, match="block_table"):
+        bsa.bsa_topk_select_sparse_table(scores, seq, 2, K, 1, 1, meta((4, 9)),
+                                         out_idx=meta((T, H, K)), sparse_bt=meta((T, H, 8 * K)),
+                                         sparse_ctx=meta((T, H)))
+    with pytest.raises(ValueError, match="sparse_bt"):
+        bsa.bsa_topk_select_sparse_table(scores, seq, 2, K, 1, 1, meta((3, 9)),
+                                         out_idx=meta((T, H, K)), sparse_bt=meta((T, H, 8 * K - 1)),
+                                         sparse_ctx=meta((T, H)))
+    with pytest.raises(ValueError, match="sparse_ctx"):
+        bsa.bsa_topk_select_sparse_table(scores, seq, 2, K, 1, 1, meta((3, 9)),
+                                         out_idx=meta((T, H, K)), sparse_bt=meta((T, H, 8 * K)),
+                                         sparse_ctx=meta((T,)))
+    with pytest.raises(ValueError, match="sparse_bt"):
+        bsa.bsa_build_sparse_block_table(meta((T, H, K)), meta((3, 9)), seq, 2,
+                                         sparse_bt=meta((T, H, 8)), sparse_ctx=meta((T, H)))
+    with pytest.raises(ValueError, match="block_table"):
+        bsa.bsa_build_sparse_block_table(meta((T, H, K)), meta((2, 9)), seq, 2)
+    with pytest.raises(ValueError, match="out"):
+        bsa.bsa_num_valid_pages_decode(seq, 2, out=meta((5,)))
+    with pytest.raises(ValueError, match="cu_seqlens_q"):
+        bsa.bsa_num_valid_pages_varlen(meta((3,)), meta((3,)), 10)
+    with pytest.raises(ValueError, match="out_idx"):
+        bsa.bsa_topk_select_noalloc(scores, good_nvp, K, out_idx=meta((T, H, K - 1)))
+    assert calls == [], calls

@@ -41,8 +41,18 @@ def test_roofline_kernel_and_traffic_follow_the_policy():
     assert bench.KERNEL_OF_PATH[p16["path"]] == "pair_select_kernel"
     assert bench.KERNEL_OF_PATH[p64["path"]] == "select_kernel"
     assert bench.dominant_kernel(p64["path"], True).startswith("select_kernel (fused")
-    for path in ("fused", "unfused"):
-        assert bench.read_traffic(path, "pair_select_kernel", 16, 131072) is not None
-        assert bench.read_traffic(path, "select_kernel", 64, 131072) is None
-        assert bench.read_traffic(path, "pair_select_kernel", 32, 131072) is None
-        assert bench.read_traffic(path, "pair_select_kernel", 16, 65536) is None
+    import json
+    import tempfile
+    ent = {"kernel": "pair_select_kernel<bf16, topk<=16>", "topk": 16, "requests": 131072,
+           "dram_bytes_per_launch": 1}
+    with tempfile.TemporaryDirectory() as d:
+        f = os.path.join(d, "traffic.json")
+        for sha, ok in ((bench.select_source_sha(), True), ("0" * 16, False)):
+            with open(f, "w") as fh:
+                json.dump({p: dict(ent, source_sha=sha) for p in ("fused", "unfused")}, fh)
+            for path in ("fused", "unfused"):
+                got = bench.read_traffic(path, "pair_select_kernel", 16, 131072, f)
+                assert (got is not None) == ok, "traffic is used only for the current source"
+                assert bench.read_traffic(path, "select_kernel", 64, 131072, f) is None
+                assert bench.read_traffic(path, "pair_select_kernel", 32, 131072, f) is None
+                assert bench.read_traffic(path, "pair_select_kernel", 16, 65536, f) is None

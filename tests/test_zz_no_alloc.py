@@ -5,15 +5,17 @@ running under a CUDA-graph capture mode that forbids allocation, plugins
 whose host engine owns all device memory, loops that must not enter the
 allocator.  It keeps the split path's scratch in the library's own device
 array instead of a caller workspace.  These tests call it through the C ABI
-and check it against the regular entry point, twice in a row (the array
-keeps the previous call's contents), on workloads that need scratch and on
-one that does not.  The file is named so that pytest collects it last.
+and check it against the regular entry point and against the CPU oracle,
+twice in a row (the array keeps the previous call's contents), on workloads
+that need scratch and on one that does not.  The file is named so that
+pytest collects it last.
 """
 import numpy as np
 import pytest
 import torch
 
 import block_sparse_attention_topk_gb300 as bsa
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -41,10 +43,12 @@ def test_noalloc_matches_regular_entry_point(cuda_device, T, H, M, K, dtype):
         assert need > 0, "this case should exercise the scratch"
     ref = bsa.bsa_topk_select(s, n, K, 1, 2)
     torch.cuda.synchronize()
+    want = oracle.topk_select(scores, nvp.numpy(), K, 1, 2)
     for _ in range(2):
         got = bsa.bsa_topk_select_noalloc(s, n, K, 1, 2)
         torch.cuda.synchronize()
         assert torch.equal(got, ref)
+        assert np.array_equal(got.cpu().numpy(), want)
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(cuda_device):
