@@ -60,9 +60,12 @@ def _declare(lib):
     lib.oracle_topk_select_sparse_table.argtypes = [
         ctypes.c_void_p, ctypes.c_int, i64, i32, i64, i64, i64, i64, i32p, i32, i32,
         i32, i32p, i64, i32p, i32p, i32p]
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    lib.oracle_index_scores.argtypes = [u16p, u16p, i64, i32p, i64, i32p, i64, i32, i64, i64,
+                                        i64, ctypes.POINTER(ctypes.c_double)]
     for name in ("oracle_num_valid_pages_decode", "oracle_num_valid_pages_varlen",
                  "oracle_topk_select", "oracle_build_sparse_block_table",
-                 "oracle_topk_select_sparse_table"):
+                 "oracle_topk_select_sparse_table", "oracle_index_scores"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -205,3 +208,41 @@ def topk_select_sparse_table(scores, seq_lens, dql: int, K: int, num_init: int,
     if rc != 0:
         raise ValueError(f"oracle_topk_select_sparse_table rc={rc}")
     return out_idx, sparse_bt, sparse_ctx
+
+
+def _bf16_bits(x) -> np.ndarray:
+    """bf16 bit patterns (uint16) of a CPU torch bfloat16 tensor or a uint16 array."""
+    if hasattr(x, "detach"):
+        import torch
+        t = x.detach().cpu().contiguous()
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"expected bfloat16, got {t.dtype}")
+        return np.ascontiguousarray(t.view(torch.int16).numpy().view(np.uint16))
+    a = np.ascontiguousarray(np.asarray(x))
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected uint16 bf16 bits, got {a.dtype}")
+    return a
+
+
+def index_scores(q, k, block_table, seq_lens, dql: int, M: int, lib=None) -> np.ndarray:
+    """Index scores of decode rows in float64: q bf16 [T, H, D], k bf16
+    [NB, D] (one pooled key per physical block), block_table int32 [B, MB],
+    seq_lens int32 [B]; returns [T, H, M] (NaN past each row's causal
+    count, -inf for causal blocks without a usable key)."""
+    qb = _bf16_bits(q)
+    kb = _bf16_bits(k)
+    T, H, D = qb.shape
+    NB = kb.shape[0]
+    assert kb.shape[1] == D
+    bt = _i32(block_table)
+    B, MB = bt.shape
+    s = _i32(seq_lens)
+    assert s.shape[0] == B and T == B * dql
+    out = np.empty((T, H, M), dtype=np.float64)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    rc = _load(lib).oracle_index_scores(qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), NB,
+                                        _ptr(bt), MB, _ptr(s), B, dql, H, D, M,
+                                        out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    if rc != 0:
+        raise ValueError(f"oracle_index_scores rc={rc}")
+    return out

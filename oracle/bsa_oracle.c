@@ -303,3 +303,59 @@ int oracle_topk_select_sparse_table(const void* scores, int dtype, int64_t B, in
     free(nvp);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Index scores of decode rows                                                */
+/* ------------------------------------------------------------------------ */
+
+/* The pages name the decode score kernel (minimax_m3_index_decode_score,
+ * writing score_out = unified_scores[:nd]: "vLLM PR #47502 report", section
+ * 实现拆解 item 1) and say that a page, a sparse block and an index-K block
+ * are the same 128 tokens (section 关键源码片段, indexer_msa.py), but they do
+ * not print the score formula.  Reading taken: one pooled index key per
+ * physical 128-token block, shared by the index heads, and
+ *     score[t, h, b] = sum over d of q[t, h, d] * k[block_table[req, b], d]
+ * with req = t / dql (the decode row mapping of PR #47984), no scale factor
+ * (PR #47502 removed sm_scale from the top-k call: section 实现拆解 item 6),
+ * computed here exactly (bf16 products are exact in double, and the sum of
+ * D of them is rounded once per addition in double).  Only the causal blocks
+ * b < v = min(M, cdiv(pos + 1, 128)) have a score; a causal block without a
+ * usable key (b >= MB, or a physical id outside [0, NB)) scores -inf, like
+ * an unwritten tile.  Entries b >= v are set to NaN here: no score kernel
+ * writes them.
+ *
+ * q: bf16 bits [T, H, D]; k: bf16 bits [NB, D]; block_table: int32 [B, MB];
+ * seq_lens: int32 [B]; T = B * dql; out: double [T, H, M]. */
+int oracle_index_scores(const uint16_t* q, const uint16_t* k, int64_t NB,
+                        const int32_t* block_table, int64_t MB, const int32_t* seq_lens,
+                        int64_t B, int32_t dql, int64_t H, int64_t D, int64_t M, double* out) {
+    if (dql < 1 || H < 1 || D < 1 || M < 1) return -1;
+    for (int64_t req = 0; req < B; ++req) {
+        for (int32_t lq = 0; lq < dql; ++lq) {
+            const int64_t t = req * dql + lq;
+            const int64_t pos = (int64_t)seq_lens[req] - dql + lq;
+            int64_t v = pages_for_length(pos + 1 > 0 ? pos + 1 : 0);
+            if (v > M) v = M;
+            for (int64_t h = 0; h < H; ++h) {
+                double* row = out + (t * H + h) * M;
+                const uint16_t* qv = q + (t * H + h) * D;
+                for (int64_t b = 0; b < M; ++b) {
+                    if (b >= v) {
+                        row[b] = NAN;
+                        continue;
+                    }
+                    const int64_t phys = b < MB ? block_table[req * MB + b] : -1;
+                    if (phys < 0 || phys >= NB) {
+                        row[b] = -INFINITY;
+                        continue;
+                    }
+                    double s = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        s += decode_bits(qv[d], 8, 7).value * decode_bits(k[phys * D + d], 8, 7).value;
+                    row[b] = s;
+                }
+            }
+        }
+    }
+    return 0;
+}

@@ -406,6 +406,92 @@ def check_fused_token_enumeration(lib=None, trials=150, seed=32):
                                                           want_ctx)
 
 
+def _index_case(rng, integer_valued):
+    """Small decode batch for the index-score oracle: queries [T, H, D],
+    pooled keys [NB, D] (bf16), a block table of distinct physical ids with
+    some entries out of range, sequence lengths that include padded
+    requests and contexts longer than the table."""
+    import torch
+    dql = int(rng.integers(1, 4))
+    B = int(rng.integers(1, 5))
+    H = int(rng.integers(1, 4))
+    D = int(rng.choice([8, 16, 24]))
+    M = int(rng.integers(2, 10))
+    MB = int(rng.integers(1, M + 3))
+    NB = B * MB + 7
+    if integer_valued:
+        q = torch.from_numpy(rng.integers(-4, 5, (B * dql, H, D)).astype(np.float32))
+        k = torch.from_numpy(rng.integers(-4, 5, (NB, D)).astype(np.float32))
+    else:
+        q = torch.from_numpy(rng.standard_normal((B * dql, H, D)).astype(np.float32))
+        k = torch.from_numpy(rng.standard_normal((NB, D)).astype(np.float32))
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    table = rng.permutation(NB)[:B * MB].astype(np.int32).reshape(B, MB)
+    table[rng.random((B, MB)) < 0.1] = NB + 3           # no usable key
+    seq = rng.integers(0, 128 * (M + 2), B).astype(np.int32)
+    seq[rng.random(B) < 0.2] = 0
+    return q, k, table, seq, dql, M
+
+
+def check_index_scores_against_numpy(lib=None, trials=40, seed=41):
+    """The index-score oracle against a vectorised float64 numpy formulation
+    (gather the request's keys through the block table, einsum with the
+    queries): exact on integer-valued inputs, to 1e-12 relative otherwise;
+    NaN past each row's causal count, -inf for causal blocks without a key."""
+    rng = np.random.default_rng(seed)
+    for trial in range(trials):
+        q, k, table, seq, dql, M = _index_case(rng, integer_valued=trial % 2 == 0)
+        got = oracle.index_scores(q, k, table, seq, dql, M, lib=lib)
+        T, H, D = q.shape
+        B, MB = table.shape
+        qd = q.float().numpy().astype(np.float64)
+        kd = k.float().numpy().astype(np.float64)
+        nvp = oracle.num_valid_pages_decode(seq, dql, lib=lib)
+        for t in range(T):
+            req = t // dql
+            v = min(M, int(nvp[t]))
+            phys = np.array([table[req, b] if b < MB else -1 for b in range(v)], dtype=np.int64)
+            ok = (phys >= 0) & (phys < kd.shape[0])
+            keys = kd[np.where(ok, phys, 0)]                              # [v, D]
+            want = np.einsum("hd,bd->hb", qd[t], keys)
+            want[:, ~ok] = -np.inf
+            row = got[t]
+            assert np.isnan(row[:, v:]).all(), (trial, t)
+            if trial % 2 == 0:
+                assert np.array_equal(row[:, :v], want), (trial, t)
+            else:
+                fin = np.isfinite(want)
+                assert np.array_equal(np.isfinite(row[:, :v]), fin), (trial, t)
+                assert np.allclose(row[:, :v][fin], want[fin], rtol=1e-12, atol=1e-12), (trial, t)
+                assert (row[:, :v][~fin] == -np.inf).all()
+
+
+def check_index_scores_one_hot(lib=None, trials=30, seed=42):
+    """A one-hot query e_j reads coordinate j of the key of the block's
+    physical id: score[t, h, b] = k[block_table[req, b], j(t, h)]."""
+    import torch
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        q, k, table, seq, dql, M = _index_case(rng, integer_valued=False)
+        T, H, D = q.shape
+        j = rng.integers(0, D, (T, H))
+        oh = np.zeros((T, H, D), dtype=np.float32)
+        for t in range(T):
+            for h in range(H):
+                oh[t, h, j[t, h]] = 1.0
+        got = oracle.index_scores(torch.from_numpy(oh).to(torch.bfloat16), k, table, seq, dql, M,
+                                  lib=lib)
+        kd = k.float().numpy()
+        nvp = oracle.num_valid_pages_decode(seq, dql, lib=lib)
+        for t in range(T):
+            req = t // dql
+            for h in range(H):
+                for b in range(min(M, int(nvp[t]))):
+                    p = int(table[req, b]) if b < table.shape[1] else -1
+                    want = kd[p, j[t, h]] if 0 <= p < kd.shape[0] else -np.inf
+                    assert got[t, h, b] == want, (t, h, b, got[t, h, b], want)
+
+
 ALL_CHECKS = [
     check_total_order_golden,
     check_total_order_exhaustive_bf16,
@@ -423,4 +509,6 @@ ALL_CHECKS = [
     check_select_ties_lower_id,
     check_fused_equals_select_then_table,
     check_fused_token_enumeration,
+    check_index_scores_against_numpy,
+    check_index_scores_one_hot,
 ]

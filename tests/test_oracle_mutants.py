@@ -72,6 +72,19 @@ MUTANTS = [
     ("fused_table_from_page_counts",
      "rc = oracle_build_sparse_block_table(out_idx, T, H, K, block_table, B, MB, seq_lens,",
      "rc = oracle_build_sparse_block_table(out_idx, T, H, K, block_table, B, MB, nvp,"),
+    # mistakes in the index scores
+    ("score_logical_block_as_physical",
+     "const int64_t phys = b < MB ? block_table[req * MB + b] : -1;",
+     "const int64_t phys = b < MB ? b : -1;"),
+    ("score_head_ignored",
+     "const uint16_t* qv = q + (t * H + h) * D;", "const uint16_t* qv = q + (t * H) * D;"),
+    ("score_row_position",
+     "const int64_t pos = (int64_t)seq_lens[req] - dql + lq;",
+     "const int64_t pos = (int64_t)seq_lens[req] - dql + lq + 1;"),
+    ("score_missing_key_zero",
+     "row[b] = -INFINITY;", "row[b] = 0.0;"),
+    ("score_key_transposed",
+     "decode_bits(k[phys * D + d], 8, 7)", "decode_bits(k[phys + d * NB], 8, 7)"),
 ]
 
 
