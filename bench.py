@@ -207,7 +207,7 @@ def read_peaks():
 
 
 KERNEL_OF_PATH = {0: "select_kernel", 1: "select_kernel", 2: "group_select_kernel",
-                  3: "pair_select_kernel"}
+                  3: "pair_select_kernel", 4: "octet_select_kernel"}
 
 
 def dominant_kernel(path_id: int, fused: bool) -> str:

@@ -26,6 +26,7 @@ BSA_PATH_ROW = 0
 BSA_PATH_SPLIT = 1
 BSA_PATH_GROUP = 2
 BSA_PATH_PAIR = 3
+BSA_PATH_OCTET = 4
 PAGE_SIZE = 128
 PAGES_PER_SPARSE_BLOCK = 8
 MAX_TOPK = 1024

@@ -102,6 +102,7 @@ int forced_path() {
         if (strcmp(e, "row") == 0) return BSA_PATH_ROW;
         if (strcmp(e, "group") == 0) return BSA_PATH_GROUP;
         if (strcmp(e, "pair") == 0) return BSA_PATH_PAIR;
+        if (strcmp(e, "octet") == 0) return BSA_PATH_OCTET;
         return -1;
     }();
     return v;
@@ -138,8 +139,27 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
     // comparison.  Both fall back to the warp path for overflowing rows.
     const int elem = dtype == BSA_DTYPE_BF16 ? 2 : 4;
     const int forced = forced_path();
-    if (K <= kGroupMaxK && M * elem <= kGroupMaxBytes && forced != BSA_PATH_ROW &&
-        forced != BSA_PATH_GROUP) {
+    const bool short_rows = M * elem <= kGroupMaxBytes;
+    const bool pair_ok = K <= kGroupMaxK && short_rows;
+    const bool oct_ok = K <= kOctMaxK && short_rows;
+    // Octet path (8 lanes per row, 4 rows per warp) for 32 < topk <= 64, or
+    // for any topk <= 64 when forced.
+    if (oct_ok && (forced == BSA_PATH_OCTET || (!pair_ok && forced != BSA_PATH_ROW))) {
+        const int64_t items = (rows + kOctRows - 1) / kOctRows;
+        int64_t grid = (items + kOctWarps - 1) / kOctWarps;
+        if (grid > INT32_MAX) grid = INT32_MAX;
+        if (grid < 1) grid = 1;
+        p->path = BSA_PATH_OCTET;
+        p->vecs_per_lane = 4;
+        p->chunks_per_row = 1;
+        p->reps_per_lane = 16;
+        p->warps_per_cta = kOctWarps;
+        p->grid = (int32_t)grid;
+        p->cand_capacity = cap;
+        p->smem_bytes = kOctWarps * (int)sizeof(OctSmem);
+        return BSA_OK;
+    }
+    if (pair_ok && forced != BSA_PATH_ROW && forced != BSA_PATH_GROUP) {
         const int gsmem = kPairWarps * (int)(dtype == BSA_DTYPE_BF16
                                                  ? sizeof(PairSmem<uint32_t>)
                                                  : sizeof(PairSmem<unsigned long long>));

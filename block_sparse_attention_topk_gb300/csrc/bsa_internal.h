@@ -87,6 +87,21 @@ struct PairSmem {
     PairRowDesc desc[kPairRows];
 };
 
+// Octet path: 8 lanes per row, 4 rows per warp, for 32 < topk <= 64 (see
+// bsa_select.cu).
+constexpr int kOctLanes = 8;         // lanes per row
+constexpr int kOctRows = 4;          // rows per warp
+constexpr int kOctCand = 128;        // candidate capacity per row (16 per lane)
+constexpr int kOctMaxK = 64;         // largest topk the octet path serves
+constexpr int kOctWarps = 4;         // warps per CTA
+
+struct OctSmem {
+    int32_t ckey[kOctRows][kOctCand];   // candidate keys (signed order-preserving), id order
+    uint16_t cid[kOctRows][kOctCand];   // their block ids
+    int32_t sorted[kOctRows][kOctMaxK]; // selected non-forced ids, ascending
+    uint32_t scratch[32][8];            // one 32-byte chunk per lane while candidates are read out
+};
+
 // Everything one selector launch needs.  Pointers are device pointers.
 struct SelectArgs {
     const void* scores;

@@ -1928,6 +1928,403 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
     }
 }
 
+// ===========================================================================
+// Octet path: 8 lanes per row, 4 rows per warp, for 32 < topk <= 64.
+//
+// At topk 64 nearly every 32-byte chunk of a long row holds one of the K'
+// best elements, so the pair path's hot-chunk queue would reload almost the
+// whole row, and a lane pair's 32 representatives give no threshold for
+// K' > 32.  Here the 8 lanes of a row:
+//  1. stream its non-forced range in 32-byte chunks (256 contiguous bytes per
+//     row per step) and keep, for each of the 16 element positions of a
+//     chunk, the largest key seen there: 16 representatives per lane and 128
+//     per row, each the maximum of distinct elements.  Interior chunks are
+//     reduced on raw bits (a raw maximum and minimum per position, turned
+//     into the key maximum once at the end); the two edge chunks are masked
+//     and reduced on keys.
+//  2. theta: each quad of lanes (64 representatives) finds its 32nd largest
+//     representative with packed 16-bit bitonic networks (each lane sorts its
+//     16, lane pairs merge into a sorted 32, the top 32 of the quad's two
+//     pairs are their pairwise maxima); theta is the smaller of the two
+//     quads' values.  At least 64 >= K' representatives, distinct elements,
+//     reach theta, so it is a lower bound on the K'-th best non-forced score.
+//     fp32 rows use the top 16 bits of their keys for this step.
+//  3. candidates: the chunks are read again in order (L2 hits: the row was
+//     prefetched to L2 when its item began), and the elements >= theta are
+//     appended to a 128-entry list in id order, a segmented scan over the 8
+//     lanes giving each lane its place.  Rows of at most 128 non-forced
+//     blocks skip steps 1-2: every element is a candidate.
+//  4. kappa, the K'-th largest candidate key, by a binary search over
+//     [theta, largest candidate] with the candidates spread 16 per lane.  The
+//     candidates above kappa are kept, and of those equal to it the first in
+//     id order, as many as K' still needs; the kept ids, in id order, are
+//     compacted into the sorted list.
+//  5. outputs as on the other paths (8 slots per lane at topk 64).
+// A row whose candidates overflow the list (about 1 row in 1000 on N(0,1)
+// scores, in a CPU model of the long-context input) is redone by the whole
+// warp on the warp path.
+// ===========================================================================
+
+// Exclusive sum of x over the 8 lanes of this lane's row; `total` gets the
+// row's sum.  Every lane of the warp calls this.
+__device__ __forceinline__ int oct_excl_scan(int x, int q, int& total) {
+    int incl = x;
+#pragma unroll
+    for (int d = 1; d < kOctLanes; d <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, d);
+        if (q >= d) incl += y;
+    }
+    total = __shfl_sync(kFull, incl, (int)(threadIdx.x & 31) | (kOctLanes - 1));
+    return incl - x;
+}
+
+__device__ __forceinline__ int oct_sum(int x) {
+    x += __shfl_xor_sync(kFull, x, 1);
+    x += __shfl_xor_sync(kFull, x, 2);
+    x += __shfl_xor_sync(kFull, x, 4);
+    return x;
+}
+
+// Step 2: from the lane's 16 representatives (signed 16-bit keys, packed two
+// per word), the smaller of the row's two quad values (each the 32nd largest
+// of a quad's 64 representatives).  Every lane of the warp calls this.
+__device__ __forceinline__ int32_t oct_theta(uint32_t (&rp)[8], int q) {
+    packed_sort16_desc<true>(rp);
+    // lane pairs: the even lane keeps the top 16 of the pair's 32, the odd
+    // lane the bottom 16 (each bitonic), then both are sorted; word i of a
+    // lane holds its positions i (low half) and i + 8 (high half), and the
+    // partner's list reversed is its word 7 - i with the halves swapped
+    uint32_t y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __shfl_xor_sync(kFull, rp[7 - i], 1);
+    const bool top = (q & 1) == 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t b = __byte_perm(y[i], 0, 0x1032);
+        rp[i] = top ? hmax<true>(rp[i], b) : hmin<true>(rp[i], b);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rp[i] = hsplit<true>(rp[i]);
+    hclean8_desc<true>(rp);
+    // quads: with P0 the sorted 32 of lanes 0-1 and P1 that of lanes 2-3,
+    // max(P0[r], P1[31 - r]) over r are the quad's top 32; lane q meets lane
+    // q ^ 3's list reversed.  Their minimum is the quad's 32nd largest.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __shfl_xor_sync(kFull, rp[7 - i], 3);
+    uint32_t mn = 0x7FFF7FFFu;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        mn = hmin<true>(mn, hmax<true>(rp[i], __byte_perm(y[i], 0, 0x1032)));
+    int32_t m = min((int32_t)(int16_t)(uint16_t)mn, (int32_t)(int16_t)(uint16_t)(mn >> 16));
+    m = min(m, __shfl_xor_sync(kFull, m, 1));
+    m = min(m, __shfl_xor_sync(kFull, m, 4));
+    return m;
+}
+
+template <bool BF16, int FM>
+__global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const KernelParams P) {
+    using E = Elem<BF16>;
+    constexpr int S = E::kBytes;
+    constexpr int CE = 32 / S;                      // elements per 32-byte chunk
+    constexpr int32_t kKeyMin = BF16 ? -32768 : INT32_MIN;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int g = lane >> 3;   // row of the warp's item
+    const int q = lane & 7;    // lane within the row
+    OctSmem& sm = *reinterpret_cast<OctSmem*>(smem_raw + (size_t)warp * sizeof(OctSmem));
+    const SelectArgs& a = P.a;
+    const int64_t nitems = (P.rows + kOctRows - 1) / kOctRows;
+    const int64_t stride = (int64_t)gridDim.x * kOctWarps;
+
+    for (int64_t it = (int64_t)blockIdx.x * kOctWarps + warp; it < nitems; it += stride) {
+        const int64_t row = it * kOctRows + g;
+        const bool active = row < P.rows;
+        RowInfo r{};
+        r.all = true;
+        if (active) r = row_info_from<FM>(a, row, row_meta<FM>(a, row));
+        const bool need = active && r.need;
+
+        // ---- geometry of the non-forced range [lo, hi), 32-byte chunks ----
+        const char* row_ptr = nullptr;
+        uintptr_t c0 = 0;
+        int nchunk = 0, base_id = 0;
+        if (need) {
+            row_ptr = reinterpret_cast<const char*>(a.scores) +
+                      ((int64_t)r.t * a.token_stride + (int64_t)r.h * a.head_stride) * S;
+            const uintptr_t a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * S;
+            const uintptr_t a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * S;
+            c0 = a_lo & ~(uintptr_t)31;
+            nchunk = (int)((a_hi - c0 + 31) >> 5);
+            base_id = r.lo - (int)((a_lo - c0) / S);
+            if (q == 0) {
+                const uintptr_t plo = c0 < P.buf_lo ? (P.buf_lo + 15) & ~(uintptr_t)15 : c0;
+                uintptr_t phi = c0 + ((uintptr_t)nchunk << 5);
+                if (phi > P.buf_hi) phi = P.buf_hi & ~(uintptr_t)15;
+                if (phi > plo) prefetch_l2(plo, (uint32_t)(phi - plo));
+            }
+        }
+        // rows of more than kOctCand non-forced blocks need a threshold
+        const bool full = need && (r.hi - r.lo) > kOctCand;
+
+        // ---- step 1: 16 representatives per lane (packed 16-bit keys) ----
+        uint32_t rp[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) rp[x] = 0x80008000u;
+        if (full) {
+            // full rows have at least 129 non-forced blocks: every lane owns a chunk
+            if constexpr (BF16) {
+                uint32_t rmx[8], rmn[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    rmx[x] = 0x80008000u;
+                    rmn[x] = 0x7FFF7FFFu;
+                }
+                auto take_edge = [&](int k) {
+                    uint32_t w[8];
+                    pair_load_edge<true>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) rp[x] = max_s16x2(rp[x], w[x]);
+                };
+                auto fold = [&](const uint32_t (&w)[8]) {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        rmx[x] = max_s16x2(rmx[x], w[x]);
+                        rmn[x] = min_s16x2(rmn[x], w[x]);
+                    }
+                };
+                if (q == 0) take_edge(0);
+                if ((nchunk - 1) % kOctLanes == q) take_edge(nchunk - 1);
+                // interior chunks k = q + 8 i, 1 <= k <= nchunk - 2, two loads in flight
+                const int klast = nchunk - 2;
+                int k = q == 0 ? kOctLanes : q;
+                const bool any_interior = k <= klast;
+                for (; k + kOctLanes <= klast; k += 2 * kOctLanes) {
+                    uint32_t w0[8], w1[8];
+                    ld32(c0 + ((uintptr_t)k << 5), w0);
+                    ld32(c0 + ((uintptr_t)(k + kOctLanes) << 5), w1);
+                    fold(w0);
+                    fold(w1);
+                }
+                if (k <= klast) {
+                    uint32_t w0[8];
+                    ld32(c0 + ((uintptr_t)k << 5), w0);
+                    fold(w0);
+                }
+                if (any_interior) {
+                    // a position's largest key: its raw maximum when that is
+                    // non-negative, else the key of its raw minimum
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const uint32_t mneg = sign_mask16(rmx[x]);
+                        const uint32_t km = (rmx[x] & ~mneg) | ((rmn[x] ^ 0x7FFF7FFFu) & mneg);
+                        rp[x] = max_s16x2(rp[x], km);
+                    }
+                }
+            } else {
+                // fp32: 8 positions per chunk, two sets by the lane's chunk
+                // parity, so a lane with two or more chunks has 16
+                // representatives; packed as the top 16 bits of the keys
+                int32_t ra[8], rb[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) ra[x] = rb[x] = INT32_MIN;
+                auto load_keys = [&](int k, uint32_t (&w)[8]) {
+                    if (k == 0 || k == nchunk - 1) {
+                        pair_load_edge<false>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
+                    } else {
+                        ld32(c0 + ((uintptr_t)k << 5), w);
+                        chunk_to_keys<false>(w);
+                    }
+                };
+                for (int k = q; k < nchunk; k += 2 * kOctLanes) {
+                    uint32_t w0[8], w1[8];
+                    const bool two = k + kOctLanes < nchunk;
+                    load_keys(k, w0);
+                    if (two) load_keys(k + kOctLanes, w1);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) ra[x] = max(ra[x], (int32_t)w0[x]);
+                    if (two) {
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) rb[x] = max(rb[x], (int32_t)w1[x]);
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    rp[x] = ((uint32_t)ra[2 * x] >> 16) | ((uint32_t)ra[2 * x + 1] & 0xFFFF0000u);
+                    rp[x + 4] = ((uint32_t)rb[2 * x] >> 16) | ((uint32_t)rb[2 * x + 1] & 0xFFFF0000u);
+                }
+            }
+        }
+
+        // ---- step 2: theta (every lane takes part in the networks) ----
+        const int32_t th16 = oct_theta(rp, q);
+        int32_t theta = kKeyMin;
+        if (full) theta = BF16 ? th16 : (int32_t)((uint32_t)th16 << 16);
+
+        // ---- step 3: candidates >= theta, in id order ----
+        const int my_steps = need ? (nchunk - q + kOctLanes - 1) / kOctLanes : 0;
+        const int steps = __reduce_max_sync(kFull, (unsigned)my_steps);
+        const bool raw_ok = theta >= 0;   // raw signed order is key order against it
+        int cbase = 0;
+        for (int st = 0; st < steps; ++st) {
+            const int k = q + kOctLanes * st;
+            const bool has = k < nchunk;
+            uint32_t w[8];
+            uint32_t m = 0;
+            if (has) {
+                const bool edge = k == 0 || k == nchunk - 1;
+                if (edge) {
+                    pair_load_edge<BF16>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
+                } else {
+                    ld32(c0 + ((uintptr_t)k << 5), w);
+                    if (!raw_ok) chunk_to_keys<BF16>(w);
+                }
+                if (theta == kKeyMin) {
+                    m = BF16 ? 0xFFFFu : 0xFFu;
+                } else if constexpr (BF16) {
+                    m = ge_bits16<8>(w, theta);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) m |= ((int32_t)w[x] >= theta ? 1u : 0u) << x;
+                }
+                if (edge) {
+                    const int first_id = base_id + k * CE;
+                    const int lo_e = min(max(r.lo - first_id, 0), CE);
+                    const int hi_e = min(max(r.hi - first_id, 0), CE);
+                    m &= ((1u << hi_e) - 1u) & ~((1u << lo_e) - 1u);
+                }
+            }
+            int tot;
+            const int off = oct_excl_scan(__popc(m), q, tot);
+            if (m) {
+                uint32_t* scr = sm.scratch[lane];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) scr[x] = w[x];
+                const int first_id = base_id + k * CE;
+                int pos = cbase + off;
+                while (m) {
+                    const int e = __ffs(m) - 1;
+                    m &= m - 1;
+                    if (pos < kOctCand) {
+                        int32_t key;
+                        if constexpr (BF16)
+                            key = (int32_t)reinterpret_cast<const int16_t*>(scr)[e];
+                        else
+                            key = (int32_t)scr[e];
+                        sm.ckey[g][pos] = key;
+                        sm.cid[g][pos] = (uint16_t)(first_id + e);
+                    }
+                    ++pos;
+                }
+            }
+            cbase += tot;
+        }
+        const bool ovf = cbase > kOctCand;
+        __syncwarp();
+
+        // ---- step 4: kappa, the K'-th largest candidate key ----
+        const bool sel_ok = need && !ovf;
+        const int c = min(cbase, kOctCand);
+        int32_t kk[16];
+        {
+            const int4* src = reinterpret_cast<const int4*>(&sm.ckey[g][16 * q]);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int4 t4 = src[v];
+                kk[4 * v] = t4.x;
+                kk[4 * v + 1] = t4.y;
+                kk[4 * v + 2] = t4.z;
+                kk[4 * v + 3] = t4.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (!(sel_ok && 16 * q + e < c)) kk[e] = INT32_MIN;
+        }
+        int32_t mx = INT32_MIN;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx = max(mx, kk[e]);
+        mx = max(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = max(mx, __shfl_xor_sync(kFull, mx, 2));
+        mx = max(mx, __shfl_xor_sync(kFull, mx, 4));
+        // invariant: count(>= lo) >= K' > count(>= hi) = cnt_hi; the padding
+        // (INT32_MIN, positions >= c) is never counted because mid > lo
+        int64_t lo = theta, hi = (int64_t)mx + 1;
+        int cnt_hi = 0;
+        if (!sel_ok) hi = lo + 1;
+        const int kp = r.kp;
+        while (__any_sync(kFull, hi - lo > 1)) {
+            const int64_t mid = lo + ((hi - lo) >> 1);
+            const int32_t t = (int32_t)mid;
+            int cnt = 0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) cnt += kk[e] >= t ? 1 : 0;
+            cnt = oct_sum(cnt);
+            if (hi - lo > 1) {
+                if (cnt >= kp) {
+                    lo = mid;
+                } else {
+                    hi = mid;
+                    cnt_hi = cnt;
+                }
+            }
+        }
+        const int32_t kappa = (int32_t)lo;
+        // keep every candidate above kappa and the first (K' - count above)
+        // of those equal to it in id order
+        uint32_t gtm = 0, eqm = 0;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const bool valid = sel_ok && 16 * q + e < c;
+            if (valid && kk[e] > kappa) gtm |= 1u << e;
+            if (valid && kk[e] == kappa) eqm |= 1u << e;
+        }
+        int tall;
+        const int tb = oct_excl_scan(__popc(eqm), q, tall);
+        const int allowed = min(max(kp - cnt_hi - tb, 0), __popc(eqm));
+        uint32_t rest = eqm;
+        for (int i = 0; i < allowed; ++i) rest &= rest - 1;
+        uint32_t selm = gtm | (eqm & ~rest);
+        int stot;
+        int o = oct_excl_scan(__popc(selm), q, stot);
+        while (selm) {
+            const int e = __ffs(selm) - 1;
+            selm &= selm - 1;
+            sm.sorted[g][o++] = sm.cid[g][16 * q + e];
+        }
+        __syncwarp();
+
+        // ---- step 5: outputs ----
+        group_write_outputs<kOctLanes, FM>(P, row, r, r.all, sm.sorted[g], q,
+                                           active && (!need || !ovf));
+
+        // ---- rows whose candidates overflowed: the whole warp redoes them ----
+        unsigned fb = __ballot_sync(kFull, q == 0 && need && ovf);
+        __syncwarp();
+        while (fb) {
+            const int bit = __ffs(fb) - 1;
+            fb &= fb - 1;
+            const int64_t frow = it * kOctRows + (bit >> 3);
+            uint32_t* s_keys = reinterpret_cast<uint32_t*>(&sm);
+            warp_item<BF16, 4, 2>(P, frow, 0, s_keys, reinterpret_cast<int32_t*>(s_keys + P.cap),
+                                  lane);
+            __syncwarp();
+        }
+        __syncwarp();
+    }
+}
+
+template <bool BF16>
+cudaError_t launch_octet(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
+    auto kern = P.a.fused ? octet_select_kernel<BF16, kFusedYes> : octet_select_kernel<BF16, kFusedNo>;
+    if (pol.smem_bytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             pol.smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<pol.grid, kOctWarps * 32, pol.smem_bytes, st>>>(P);
+    return cudaGetLastError();
+}
+
 template <bool BF16, int FM>
 cudaError_t launch_pair_fm(const KernelParams& P, const bsa_launch_policy_t& pol,
                            cudaStream_t st) {
@@ -2028,6 +2425,9 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
     if (pol.path == BSA_PATH_PAIR)
         return a.dtype == BSA_DTYPE_BF16 ? launch_pair<true>(P, pol, stream)
                                          : launch_pair<false>(P, pol, stream);
+    if (pol.path == BSA_PATH_OCTET)
+        return a.dtype == BSA_DTYPE_BF16 ? launch_octet<true>(P, pol, stream)
+                                         : launch_octet<false>(P, pol, stream);
     return a.dtype == BSA_DTYPE_BF16 ? launch_dt<true>(P, pol, stream)
                                      : launch_dt<false>(P, pol, stream);
 }

@@ -77,6 +77,7 @@ extern "C" {
 #define BSA_PATH_SPLIT 1    /* several warps per row + last-arriver merge   */
 #define BSA_PATH_GROUP 2    /* 4 lanes per row, 8 rows per warp (K <= 32)   */
 #define BSA_PATH_PAIR 3     /* 2 lanes per row, 16 rows per warp (K <= 32)  */
+#define BSA_PATH_OCTET 4    /* 8 lanes per row, 4 rows per warp (K <= 64)   */
 
 typedef struct bsa_launch_policy {
     int32_t path;             /* BSA_PATH_*                                   */
@@ -224,10 +225,12 @@ int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_t T, int64_
  * SMs.  Host-only, deterministic, launches nothing; exported so the 74 /
  * 128 / 129 and other capacity boundaries can be tested without a GPU.
  * Paths: BSA_PATH_PAIR when K <= 32 and a row holds at most 2 KB (M * element
- * size <= 2048); otherwise BSA_PATH_ROW, or BSA_PATH_SPLIT when a row needs
- * more than one pass and the rows alone cannot fill the GPU.  The environment
- * variable BSA_SELECT_PATH=row|group|pair, read once per process, forces a
- * path for testing (BSA_PATH_GROUP is reachable only that way).
+ * size <= 2048), BSA_PATH_OCTET when 32 < K <= 64 and a row holds at most
+ * 2 KB; otherwise BSA_PATH_ROW, or BSA_PATH_SPLIT when a row needs more than
+ * one pass and the rows alone cannot fill the GPU.  The environment variable
+ * BSA_SELECT_PATH=row|group|pair|octet, read once per process, forces a path
+ * among those that can serve the call, for testing (BSA_PATH_GROUP is
+ * reachable only that way).
  * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_TOPK, BSA_ERR_DTYPE. */
 int bsa_select_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
                       bsa_launch_policy_t* policy);

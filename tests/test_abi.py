@@ -59,8 +59,10 @@ BF, FP = 0, 1
 @pytest.mark.parametrize("M,dtype,K,path", [
     # pair path: topk <= 32 and a row of at most 2 KB
     (16, FP, 4, 3), (74, BF, 16, 3), (128, BF, 16, 3), (129, BF, 16, 3), (1024, BF, 16, 3),
-    (1025, BF, 16, 0), (512, FP, 16, 3), (513, FP, 16, 0), (1024, BF, 32, 3), (1024, BF, 33, 0),
-    (74, BF, 64, 0), (8192, BF, 16, 0)])
+    (1025, BF, 16, 0), (512, FP, 16, 3), (513, FP, 16, 0), (1024, BF, 32, 3),
+    # octet path: 32 < topk <= 64 and a row of at most 2 KB
+    (1024, BF, 33, 4), (74, BF, 64, 4), (1024, BF, 64, 4), (512, FP, 64, 4), (513, FP, 64, 0),
+    (1025, BF, 64, 0), (1024, BF, 65, 0), (8192, BF, 16, 0)])
 def test_policy_path(bsa, M, dtype, K, path):
     assert _policy(bsa, 10**6, M, K, dtype)["path"] == path
 
@@ -70,22 +72,23 @@ def test_policy_path(bsa, M, dtype, K, path):
     (512, BF, 2), (513, BF, 4), (1024, BF, 4), (8192, BF, 4),
     (74, FP, 1), (128, FP, 1), (129, FP, 2), (256, FP, 2), (257, FP, 4), (1024, FP, 4)])
 def test_policy_vectors_per_lane_warp_path(bsa, M, dtype, nv):
-    """Warp path (topk 64): vectors per lane per pass switch at 32 lanes x
+    """Warp path (topk 65): vectors per lane per pass switch at 32 lanes x
     16 bytes x {1, 2}: bf16 at 256/257 and 512/513, fp32 at 128/129 and
     256/257."""
-    assert _policy(bsa, 1000, M, 64, dtype)["vecs_per_lane"] == nv
+    p = _policy(bsa, 1000, M, 65, dtype)
+    assert p["path"] in (0, 1) and p["vecs_per_lane"] == nv
 
 
 def test_policy_production_capacity(bsa):
     """The production 8k+1k graph (74 blocks, query length 4, topk 16) and
-    every capacity up to 128 run on the pair path; at topk 64 they run one
-    warp per row in a single pass."""
+    every capacity up to 128 run on the pair path; at topk 64 they run on the
+    octet path, never split."""
     for M in (65, 74, 128):
         for rows in (4, 64 * 4 * 4, 10**6):
             p = _policy(bsa, rows, M, 16, BF)
             assert p["path"] == bsa.BSA_PATH_PAIR and p["chunks_per_row"] == 1
             p = _policy(bsa, rows, M, 64, BF)
-            assert p["path"] == bsa.BSA_PATH_ROW and p["vecs_per_lane"] == 1
+            assert p["path"] == bsa.BSA_PATH_OCTET and p["chunks_per_row"] == 1
 
 
 @pytest.mark.parametrize("K,reps", [(1, 16), (16, 16), (17, 16), (32, 16)])
@@ -93,9 +96,19 @@ def test_policy_representatives_pair(bsa, K, reps):
     assert _policy(bsa, 1000, 1024, K, BF)["reps_per_lane"] == reps
 
 
-@pytest.mark.parametrize("K,reps", [(33, 2), (48, 2), (49, 8), (64, 8)])
+@pytest.mark.parametrize("K,reps", [(65, 8), (96, 8)])
 def test_policy_representatives_warp(bsa, K, reps):
     assert _policy(bsa, 1000, 1024, K, BF)["reps_per_lane"] == reps
+
+
+@pytest.mark.parametrize("K", [33, 48, 64])
+def test_policy_octet(bsa, K):
+    """Octet path: 4 rows per warp, 4 warps per CTA, one item per warp; the
+    overflow fallback's buffer fits in a warp's shared memory."""
+    p = _policy(bsa, 10**6, 1024, K, BF)
+    assert p["path"] == bsa.BSA_PATH_OCTET and p["reps_per_lane"] == 16
+    assert p["grid"] == (10**6 // 4 + 3) // 4 and p["warps_per_cta"] == 4
+    assert p["cand_capacity"] * 8 <= p["smem_bytes"] // p["warps_per_cta"]
 
 
 def test_policy_split_only_for_few_long_rows(bsa):
@@ -111,7 +124,7 @@ def test_policy_split_only_for_few_long_rows(bsa):
 
 
 def test_policy_capacity_and_grid(bsa):
-    p = _policy(bsa, 10**6, 1024, 64, BF)
+    p = _policy(bsa, 10**6, 1025, 64, BF)
     assert p["cand_capacity"] >= 64 + 32 * 8 and p["cand_capacity"] % 32 == 0
     assert p["smem_bytes"] == p["warps_per_cta"] * p["cand_capacity"] * 8
     assert p["grid"] == (10**6 + 7) // 8          # one row per warp, 8 warps per CTA

@@ -39,8 +39,8 @@ def test_roofline_kernel_and_traffic_follow_the_policy():
     p16 = bsa.bsa_select_policy(rows, 1024, 16, bsa.BSA_DTYPE_BF16, 152)
     p64 = bsa.bsa_select_policy(rows, 1024, 64, bsa.BSA_DTYPE_BF16, 152)
     assert bench.KERNEL_OF_PATH[p16["path"]] == "pair_select_kernel"
-    assert bench.KERNEL_OF_PATH[p64["path"]] == "select_kernel"
-    assert bench.dominant_kernel(p64["path"], True).startswith("select_kernel (fused")
+    assert bench.KERNEL_OF_PATH[p64["path"]] == "octet_select_kernel"
+    assert bench.dominant_kernel(p64["path"], True).startswith("octet_select_kernel (fused")
     import json
     import tempfile
     ent = {"kernel": "pair_select_kernel<bf16, topk<=16>", "topk": 16, "requests": 131072,

@@ -162,6 +162,53 @@ def test_select_pair_path_topk_sweep(cuda_device, dtype, M, K, I, L):
     _assert_equal(got, want, f"pair sweep dtype={dtype} M={M} K={K} I={I} L={L}")
 
 
+@pytest.mark.parametrize("dtype,M", [(torch.bfloat16, 74), (torch.bfloat16, 300),
+                                     (torch.bfloat16, 1024), (torch.float32, 200),
+                                     (torch.float32, 512)])
+@pytest.mark.parametrize("K,I,L", [(33, 1, 1), (40, 0, 0), (48, 1, 2), (61, 2, 3), (64, 1, 2),
+                                   (64, 0, 0)])
+def test_select_octet_path_topk_sweep(cuda_device, dtype, M, K, I, L):
+    """The octet path (32 < topk <= 64, rows <= 2 KB) over row lengths from a
+    handful of blocks (every block a candidate) past 128 non-forced blocks
+    (threshold from representatives), with NaN / Inf / zero / tie specials,
+    in the plain and the fused call."""
+    dt = 0 if dtype == torch.bfloat16 else 1
+    if K > M:
+        pytest.skip("K > M is rejected by the host")
+    assert bsa.bsa_select_policy(10**5, M, K, dt)["path"] == bsa.BSA_PATH_OCTET
+    rows = 160
+    rng = np.random.default_rng(K * 1000 + M + 7 * I + L)
+    nvp = rng.integers(0, M + 40, rows).astype(np.int32)
+    nvp[:12] = [0, 1, K - 1, K, K + 1, M, M - 1, 2 * K, 128 + I + L, 129 + I + L, 130 + I + L,
+                M // 2]
+    scores = synth.normal_scores((rows, 2, M), dtype, seed=K * 17 + M)
+    synth.inject_specials(scores, seed=K + M + 1, frac_each=0.02, frac_ties=0.05)
+    synth.fill_tail(scores, torch.from_numpy(np.minimum(nvp, M)), float("-inf"))
+    want = oracle.topk_select(scores, nvp, K, I, L)
+    got = _gpu_select(scores, nvp, K, I, L, cuda_device)
+    _assert_equal(got, want, f"octet sweep dtype={dtype} M={M} K={K} I={I} L={L}")
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_fused_octet_path(cuda_device, bf16):
+    """The fused call at topk 64 on the octet path: ids, table and ctx."""
+    dtype = torch.bfloat16 if bf16 else torch.float32
+    w = synth.fused_table(seed=91, B=200, dql=2, H=2, M=1024 if bf16 else 512, K=64,
+                          dtype=dtype)
+    synth.inject_specials(w.scores, seed=92, frac_each=0.005, frac_ties=0.02)
+    nvp = _prep(w)
+    want_idx, want_bt, want_ctx = oracle.topk_select_sparse_table(
+        w.scores, w.seq_lens.numpy(), w.dql, w.K, 1, 2, w.block_table.numpy())
+    dev = cuda_device
+    idx, bt, ctx = bsa.bsa_topk_select_sparse_table(
+        w.scores.to(dev), w.seq_lens.to(dev), w.dql, w.K, 1, 2, w.block_table.to(dev))
+    torch.cuda.synchronize()
+    _assert_equal(idx.cpu().numpy(), want_idx, "fused octet idx")
+    _assert_equal(bt.cpu().numpy(), want_bt, "fused octet table")
+    _assert_equal(ctx.cpu().numpy(), want_ctx, "fused octet ctx")
+    del nvp
+
+
 @pytest.mark.parametrize("M", [16, 74, 128, 129, 256, 257, 512, 513, 1024])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_select_capacity_boundaries(cuda_device, M, dtype):
