@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the topk-64 and index-score measurements")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
 
@@ -321,6 +323,11 @@ def run_ours(args):
     kernel = KERNEL_OF_PATH[pol["path"]]
     traffic = read_traffic(args.path, kernel, K, w.B)
 
+    # ---- the same workload at topk 64 (the long-context config's other topk) ----
+    extra_topk = None
+    if not args.no_extra and w.K != 64:
+        extra_topk = topk_step(w, table, nvp_host, 64, device, stream, args)
+
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -354,6 +361,10 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         result["cpu_baseline"] = cpu_baseline(w, table, args.cpu_seconds)
+    if extra_topk is not None:
+        result["topk64_fused"] = extra_topk
+    if rank == 0 and not args.no_extra and world == 1:
+        result["index_score_select"] = index_score_step(device, args)
     if rank == 0 and not args.no_configs and world == 1:
         result["per_config_latency_us"] = config_latencies(device)
     if rank == 0:
@@ -361,6 +372,102 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def timed_launches(fn, stream, steps, warmup):
+    """Mean CUDA-event duration (ms) of fn() on `stream`, after warm-up; the
+    inputs exceed L2, so consecutive launches do not reuse cached data."""
+    for _ in range(max(3, warmup)):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def topk_step(w, table, nvp_host, K, device, stream, args):
+    """The fused step of the same long-context workload at another topk
+    (same scores, lengths and block table)."""
+    import block_sparse_attention_topk_gb300 as bsa
+    from types import SimpleNamespace
+    out_idx = torch.empty((w.T, w.H, K), dtype=torch.int32, device=device)
+    sparse_bt = torch.empty((w.T, w.H, K * 8), dtype=torch.int32, device=device)
+    sparse_ctx = torch.empty((w.T, w.H), dtype=torch.int32, device=device)
+
+    def fn():
+        bsa.bsa_topk_select_sparse_table(w.scores, w.seq_lens, w.dql, K, w.num_init, w.num_local,
+                                         table, out_idx=out_idx, sparse_bt=sparse_bt,
+                                         sparse_ctx=sparse_ctx)
+
+    ms = timed_launches(fn, stream, max(10, args.steps // 2), args.warmup)
+    wk = SimpleNamespace(K=K, H=w.H, num_init=w.num_init, num_local=w.num_local, dtype=w.dtype,
+                         M=w.M, T=w.T)
+    byt = algorithmic_bytes(wk, nvp_host, "fused")["fused"]
+    peak, src = read_peaks()
+    pol = bsa.bsa_select_policy(w.T * w.H, w.M, K, bsa.BSA_DTYPE_BF16,
+                                torch.cuda.get_device_properties(device).multi_processor_count)
+    achieved = byt / (ms / 1e3) / 1e9
+    return {"kernel": dominant_kernel(pol["path"], True), "topk": K, "kernel_ms": ms,
+            "rows_per_s": w.T * w.H / (ms / 1e3), "algorithmic_bytes_per_launch": byt,
+            "achieved_gbs": achieved, "peak_gbs": peak, "frac": achieved / peak,
+            "peak_source": src}
+
+
+def index_score_bytes(seq, dql, H, D, M, K, valid_blocks):
+    """Bytes the fused index score + select must move: the queries, the
+    block-table entries and pooled keys of every causal block (once per
+    request), the scores it writes for the causal blocks of each row, the
+    sequence lengths and the ids.  The selection re-reads the scores it has
+    just written from L2, which a separate score kernel would read from HBM."""
+    T = seq.shape[0] * dql
+    v_req = np.minimum(-(-np.maximum(seq.astype(np.int64), 0) // 128), M)
+    rows_v = []
+    for lq in range(dql):
+        ln = np.maximum(seq.astype(np.int64) - dql + lq + 1, 0)
+        rows_v.append(np.minimum(-(-ln // 128), M))
+    score_entries = int(sum(x.sum() for x in rows_v)) * H
+    return (T * H * D * 2 + int(v_req.sum()) * 4 + int(valid_blocks) * D * 2 +
+            score_entries * 4 + seq.shape[0] * 4 + T * H * K * 4)
+
+
+def index_score_step(device, args):
+    """The fused index score + select on a long-context decode batch: 8192
+    requests x query length 1, 2 index heads, index dim 128, 1024-tile
+    capacity, seq_len U[16384, 131072], paged keys (a distinct physical block
+    per causal block), topk 16."""
+    import block_sparse_attention_topk_gb300 as bsa
+    import synth
+    B, dql, H, D, M, K = 8192, 1, 2, 128, 1024, 16
+    g = synth.generator(4242, device)
+    seq = torch.randint(16384, 131073, (B,), generator=g, device=device).to(torch.int32)
+    nb = B * M
+    table = synth.paged_block_table(B, M, nb, seed=4243, device=device)
+    q, k = synth.index_inputs(4244, B * dql, H, D, nb, device=device)
+    scores = torch.full((B * dql, H, M), float("-inf"), dtype=torch.float32, device=device)
+    out_idx = torch.empty((B * dql, H, K), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fn():
+        bsa.bsa_index_score_topk_select(q, k, table, seq, dql, K, 1, 2, M=M, scores=scores,
+                                        out_idx=out_idx)
+
+    ms = timed_launches(fn, stream, 10, args.warmup)
+    seq_h = seq.cpu().numpy()
+    valid = int(np.minimum(-(-seq_h.astype(np.int64) // 128), M).sum())
+    byt = index_score_bytes(seq_h, dql, H, D, M, K, valid)
+    peak, src = read_peaks()
+    achieved = byt / (ms / 1e3) / 1e9
+    return {"kernel": "index_score_select_kernel", "workload":
+            f"{B} requests x dql {dql}, H={H}, D={D}, max_k_tiles={M}, topk={K}, "
+            "seq_len U[16384,131072], paged bf16 keys",
+            "kernel_ms": ms, "rows_per_s": B * dql * H / (ms / 1e3),
+            "algorithmic_bytes_per_launch": byt, "achieved_gbs": achieved, "peak_gbs": peak,
+            "frac": achieved / peak, "peak_source": src}
 
 
 def run_e2e(args, w, table, device, stream, rows, expect=None):
@@ -433,8 +540,24 @@ def run_e2e(args, w, table, device, stream, rows, expect=None):
             raise RuntimeError("end-to-end outputs differ from the device-resident run")
     h2d = h_scores.numel() * h_scores.element_size() + h_seq.numel() * 4 + h_table.numel() * 4
     d2h = (h_idx.numel() + h_bt.numel() + h_ctx.numel()) * 4
+    # the host link by itself: one plain pinned copy each way of the step's
+    # largest input and output
+    link = {}
+    for name, src, dst in (("h2d", h_scores, d_scores), ("d2h", d_bt, h_bt)):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        nbytes = src.numel() * src.element_size()
+        link[name] = 3 * nbytes / (a.elapsed_time(b) / 1e3) / 1e9
     return {"value": rows / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "copy_gbs_in_step": (h2d + d2h) / (ms / 1e3) / 1e9,
+            "link_gbs_alone": {"h2d": link["h2d"], "d2h": link["d2h"]},
             "steps": args.e2e_steps, "chunks": C, "kernel_launches_per_step": C}
 
 
@@ -456,6 +579,11 @@ def config_latencies(device):
         # full capacity (1M-token contexts, 4096..8192 blocks): the split path
         "capacity_8192_split": synth.long_decode(device=device, B=64, H=2, M=8192, K=16,
                                                  min_len=524288, max_len=1048576),
+        # prefill-heavy unified batch at the 8192-tile capacity: 32 decode rows
+        # and two 8192-token prefill chunks (one at the end of a 1M context)
+        "prefill_heavy_8192": synth.mixed_prefill_decode(
+            device=device, H=4, M=8192, K=16, dtype=torch.bfloat16,
+            prefill_prefix=(0, 8192 * 128 - 8192), decode_max_prefix=8192 * 128 - 1),
     }
     for name, w in cases.items():
         if w.seq_lens is not None:

@@ -42,7 +42,10 @@ EXPORTED = [
     "bsa_status_string", "bsa_num_valid_pages_decode", "bsa_num_valid_pages_varlen",
     "bsa_topk_workspace_bytes", "bsa_topk_select", "bsa_build_sparse_block_table",
     "bsa_topk_select_sparse_table", "bsa_select_policy", "bsa_topk_select_noalloc",
+    "bsa_index_score_topk_select",
 ]
+MAX_INDEX_DIM = 1024
+MAX_INDEX_QUERIES = 16
 
 
 class BsaError(RuntimeError):
@@ -98,6 +101,9 @@ def lib() -> ctypes.CDLL:
             L.bsa_select_policy.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(LaunchPolicy)]
             L.bsa_topk_select_noalloc.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i32, i32,
                                                   i32, vp, vp]
+            L.bsa_index_score_topk_select.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64,
+                                                      i32, vp, i64, i64, i64, i32, i32, i32, vp,
+                                                      i64, i64, vp, vp, vp]
             for name in EXPORTED[1:]:
                 if name != "bsa_topk_workspace_bytes":
                     getattr(L, name).restype = ctypes.c_int
@@ -361,3 +367,61 @@ def bsa_topk_select_noalloc(scores: torch.Tensor, num_valid_pages: torch.Tensor,
     _call("bsa_topk_select_noalloc", dev, _ptr(scores), dt, T, H, M, ts, hs,
           _ptr(num_valid_pages), K, num_init, num_local, _ptr(out_idx), _stream(dev))
     return out_idx
+
+
+def bsa_index_score_topk_select(q_idx: torch.Tensor, k_idx: torch.Tensor,
+                                block_table: torch.Tensor, seq_lens: torch.Tensor,
+                                decode_query_len: int, K: int, num_init: int = 1,
+                                num_local: int = 1, M: int | None = None,
+                                scores: torch.Tensor | None = None,
+                                out_idx: torch.Tensor | None = None, with_table: bool = False,
+                                sparse_bt: torch.Tensor | None = None,
+                                sparse_ctx: torch.Tensor | None = None):
+    """Fused index score + select of decode rows.  q_idx bf16 [T, H, D],
+    k_idx bf16 [num_phys_blocks, D] (one pooled key per physical block),
+    block_table int32 [num_reqs, max_blocks], seq_lens int32 [num_reqs].
+    `scores` is the fp32 unified buffer [T, H, tiles] (tile dim contiguous;
+    M = tiles used, default all); by default a new one pre-filled with -inf.
+    Returns (scores, out_idx, sparse_bt or None, sparse_ctx or None)."""
+    dev = q_idx.device
+    if not isinstance(q_idx, torch.Tensor) or not q_idx.is_cuda or q_idx.dim() != 3 \
+            or q_idx.dtype != torch.bfloat16 or not q_idx.is_contiguous():
+        raise ValueError("q_idx must be a contiguous bf16 CUDA tensor [T, H, D]")
+    T, H, D = q_idx.shape
+    if not isinstance(k_idx, torch.Tensor) or k_idx.device != dev or k_idx.dim() != 2 \
+            or k_idx.dtype != torch.bfloat16 or not k_idx.is_contiguous() or k_idx.shape[1] != D:
+        raise ValueError(f"k_idx must be a contiguous bf16 tensor [num_phys_blocks, {D}] on {dev}")
+    _dev_i32(seq_lens, "seq_lens", dev)
+    if seq_lens.dim() != 1:
+        raise ValueError("seq_lens must be 1-D [num_reqs]")
+    B = seq_lens.shape[0]
+    if T != B * decode_query_len:
+        raise ValueError(f"q_idx holds {T} token rows, expected {B} x {decode_query_len}")
+    _dev_i32(block_table, "block_table", dev)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"block_table has shape {tuple(block_table.shape)}, expected "
+                         f"[{B}, max_blocks]")
+    MB = block_table.shape[1]
+    if scores is None:
+        cap = MB if M is None else int(M)
+        scores = torch.full((T, H, cap), float("-inf"), dtype=torch.float32, device=dev)
+    if scores.dtype != torch.float32 or scores.device != dev or scores.dim() != 3 \
+            or tuple(scores.shape[:2]) != (T, H):
+        raise ValueError(f"scores must be an fp32 tensor [{T}, {H}, tiles] on {dev}")
+    _, _, M, ts, hs = _score_view(scores, M)
+    if out_idx is None:
+        out_idx = torch.empty((T, H, K), dtype=torch.int32, device=dev)
+    ots, ohs = _out_idx(out_idx, T, H, K, dev)
+    if with_table or sparse_bt is not None or sparse_ctx is not None:
+        if sparse_bt is None:
+            sparse_bt = torch.empty((T, H, K * PAGES_PER_SPARSE_BLOCK), dtype=torch.int32,
+                                    device=dev)
+        _dev_i32(sparse_bt, "sparse_bt", dev, (T, H, K * PAGES_PER_SPARSE_BLOCK))
+        if sparse_ctx is None:
+            sparse_ctx = torch.empty((T, H), dtype=torch.int32, device=dev)
+        _dev_i32(sparse_ctx, "sparse_ctx", dev, (T, H))
+    _call("bsa_index_score_topk_select", dev, _ptr(q_idx), _ptr(k_idx), k_idx.shape[0], H, D,
+          _ptr(block_table), MB, _ptr(seq_lens), B, decode_query_len, _ptr(scores), M, ts, hs, K,
+          num_init, num_local, _ptr(out_idx), ots, ohs, _ptr(sparse_bt), _ptr(sparse_ctx),
+          _stream(dev))
+    return scores, out_idx, sparse_bt, sparse_ctx

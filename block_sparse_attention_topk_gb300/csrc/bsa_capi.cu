@@ -336,6 +336,7 @@ int bsa_topk_select(const void* scores, int32_t dtype, int64_t T, int64_t H, int
     a.out_ts = out_token_stride;
     a.out_hs = out_head_stride;
     a.fused = false;
+    a.table = false;
     return run_select(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
@@ -406,7 +407,64 @@ int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_
     a.sparse_bt = sparse_bt;
     a.sparse_ctx = sparse_ctx;
     a.fused = true;
+    a.table = true;
     return run_select(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int bsa_index_score_topk_select(const void* q_idx, const void* k_idx, int64_t num_phys_blocks,
+                                int64_t H, int64_t D, const int32_t* block_table,
+                                int64_t max_blocks, const int32_t* seq_lens, int64_t num_reqs,
+                                int32_t decode_query_len, float* scores, int64_t M,
+                                int64_t token_stride, int64_t head_stride, int32_t K,
+                                int32_t num_init, int32_t num_local, int32_t* out_idx,
+                                int64_t out_token_stride, int64_t out_head_stride,
+                                int32_t* sparse_bt, int32_t* sparse_ctx, void* stream) {
+    if (num_reqs < 0 || decode_query_len < 1 || H < 1 || M < 1 || M > BSA_MAX_K_TILES ||
+        max_blocks < 0 || num_phys_blocks < 0)
+        return BSA_ERR_SHAPE;
+    if (D < 8 || D > BSA_MAX_INDEX_DIM || D % 8 != 0) return BSA_ERR_SHAPE;
+    if ((int64_t)decode_query_len * H > BSA_MAX_INDEX_QUERIES) return BSA_ERR_SHAPE;
+    int rc = check_topk_args(M, K, num_init, num_local);
+    if (rc != BSA_OK) return rc;
+    if (head_stride < M || token_stride < (H - 1) * head_stride + M) return BSA_ERR_SHAPE;
+    const int64_t T = num_reqs * decode_query_len;
+    rc = check_out_layout(T, H, K, out_token_stride, out_head_stride);
+    if (rc != BSA_OK) return rc;
+    if ((sparse_bt == nullptr) != (sparse_ctx == nullptr)) return BSA_ERR_NULL;
+    if (T == 0) return BSA_OK;
+    if (q_idx == nullptr || k_idx == nullptr || seq_lens == nullptr || scores == nullptr ||
+        out_idx == nullptr || (max_blocks > 0 && block_table == nullptr))
+        return BSA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(q_idx) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(k_idx) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(scores) & 3) != 0)
+        return BSA_ERR_ALIGN;
+    SelectArgs a{};
+    a.scores = scores;
+    a.dtype = BSA_DTYPE_FP32;
+    a.T = T;
+    a.H = H;
+    a.M = M;
+    a.token_stride = token_stride;
+    a.head_stride = head_stride;
+    a.seq_lens = seq_lens;
+    a.dql = decode_query_len;
+    a.K = K;
+    a.num_init = num_init;
+    a.num_local = num_local;
+    a.out_idx = out_idx;
+    a.out_ts = out_token_stride;
+    a.out_hs = out_head_stride;
+    a.block_table = block_table;
+    a.max_blocks = max_blocks;
+    a.sparse_bt = sparse_bt;
+    a.sparse_ctx = sparse_ctx;
+    a.fused = true;
+    a.table = sparse_bt != nullptr;
+    return status_of(launch_index_score_select(a, static_cast<const uint16_t*>(q_idx),
+                                               static_cast<const uint16_t*>(k_idx),
+                                               num_phys_blocks, (int32_t)D, scores,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -96,7 +96,10 @@ constexpr int kOctMaxK = 64;         // largest topk the octet path serves
 constexpr int kOctWarps = 4;         // warps per CTA
 
 struct OctSmem {
-    int32_t ckey[kOctRows][kOctCand];   // candidate keys (signed order-preserving), id order
+    union {
+        int32_t ckey[kOctRows][kOctCand];     // candidate keys (signed order-preserving), id order
+        int16_t ckey16[kOctRows][kOctCand];   // the same for bf16
+    };
     uint16_t cid[kOctRows][kOctCand];   // their block ids
     int32_t sorted[kOctRows][kOctMaxK]; // selected non-forced ids, ascending
     uint32_t scratch[32][8];            // one 32-byte chunk per lane while candidates are read out
@@ -118,7 +121,8 @@ struct SelectArgs {
     int64_t max_blocks;
     int32_t* sparse_bt;
     int32_t* sparse_ctx;
-    bool fused;
+    bool fused;                       // rows are decode rows: page counts from seq_lens
+    bool table;                       // the sparse-table epilogue is written
     // x / H and x / dql for x < 2^31 as (umulhi(x, mul) + x) >> shift
     uint32_t h_mul, h_shift, dql_mul, dql_shift;
 };
@@ -158,6 +162,11 @@ int device_sm_count();
 // Launches the selector (plain or fused) with a policy from bsa_select_policy.
 cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
                           const SplitWorkspace& ws, cudaStream_t stream);
+
+// Fused index score + select of decode rows (see bsa_select.cu); `a` holds
+// the selection over the fp32 score buffer `scores`.
+cudaError_t launch_index_score_select(const SelectArgs& a, const uint16_t* q, const uint16_t* k,
+                                      int64_t nb, int32_t D, float* scores, cudaStream_t stream);
 
 cudaError_t launch_num_valid_pages_decode(const int32_t* seq_lens, int64_t num_reqs,
                                           int32_t dql, int32_t* out, cudaStream_t stream);

@@ -89,6 +89,16 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return r;
 }
 
+// The same through L2 only (coherent with writes made earlier in the kernel,
+// which the non-coherent path above is not).
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -122,6 +132,9 @@ struct Elem<true> {
     __device__ static int32_t raw_of_nonneg_key(uint32_t k) { return (int32_t)(k - 0x8000u); }
     __device__ static int32_t load_one(const char* p) {
         return (int32_t)(int16_t)__ldg(reinterpret_cast<const unsigned short*>(p));
+    }
+    __device__ static int32_t load_one_cg(const char* p) {
+        return (int32_t)(int16_t)__ldcg(reinterpret_cast<const unsigned short*>(p));
     }
     __device__ static void set(uint4& w, int e, int32_t raw) {
         uint32_t* word = e < 2 ? &w.x : e < 4 ? &w.y : e < 6 ? &w.z : &w.w;
@@ -159,6 +172,9 @@ struct Elem<false> {
     __device__ static int32_t raw_of_nonneg_key(uint32_t k) { return (int32_t)(k - 0x80000000u); }
     __device__ static int32_t load_one(const char* p) {
         return (int32_t)__ldg(reinterpret_cast<const unsigned int*>(p));
+    }
+    __device__ static int32_t load_one_cg(const char* p) {
+        return (int32_t)__ldcg(reinterpret_cast<const unsigned int*>(p));
     }
     __device__ static void set(uint4& w, int e, int32_t raw) {
         uint32_t* word = e == 0 ? &w.x : e == 1 ? &w.y : e == 2 ? &w.z : &w.w;
@@ -310,7 +326,7 @@ __device__ void write_outputs(const KernelParams& P, int64_t row, int64_t t, int
         for (int s = lane; s < K; s += 32)
             out[s] = s < n ? selected_id(s, lo, hi, kp, all, buf_ids) : -1;
     }
-    if (a.fused) {
+    if (a.table) {
         const int width = K * kPagesPerBlock;
         int32_t* bt = a.sparse_bt + row * (int64_t)width;
         const int32_t* table = a.block_table + req * a.max_blocks;
@@ -408,8 +424,10 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int64_t row) {
 }
 
 // One work item (row, chunk) processed by a whole warp: the warp path, and
-// the fallback of the group path for rows whose candidates overflow.
-template <bool BF16, int NV, int R>
+// the fallback of the group path for rows whose candidates overflow.  COH:
+// the scores were written earlier in the same kernel, so they are read
+// through L2 only.
+template <bool BF16, int NV, int R, bool COH = false>
 __device__ void warp_item(const KernelParams& P, int64_t row, int chunk, uint32_t* s_keys,
                           int32_t* s_ids, int lane) {
     using E = Elem<BF16>;
@@ -454,13 +472,16 @@ __device__ void warp_item(const KernelParams& P, int64_t row, int chunk, uint32_
                 w[j] = make_uint4(E::kMaskWord, E::kMaskWord, E::kMaskWord, E::kMaskWord);
                 if (k < k_end) {
                     if (addr >= a_lo && addr + 16 <= a_hi) {
-                        w[j] = ld_stream_v4(reinterpret_cast<const void*>(addr));
+                        w[j] = COH ? ld_cg_v4(reinterpret_cast<const void*>(addr))
+                                   : ld_stream_v4(reinterpret_cast<const void*>(addr));
                     } else {
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) {
                             const int id = base_id + k * VEC + e;
-                            if (id >= lo && id < hi)
-                                E::set(w[j], e, E::load_one(row_ptr + (int64_t)id * S));
+                            if (id >= lo && id < hi) {
+                                const char* ep = row_ptr + (int64_t)id * S;
+                                E::set(w[j], e, COH ? E::load_one_cg(ep) : E::load_one(ep));
+                            }
                         }
                     }
                 }
@@ -2095,7 +2116,8 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
                 };
                 if (q == 0) take_edge(0);
                 if ((nchunk - 1) % kOctLanes == q) take_edge(nchunk - 1);
-                // interior chunks k = q + 8 i, 1 <= k <= nchunk - 2, two loads in flight
+                // interior chunks k = q + 8 i, 1 <= k <= nchunk - 2, up to four
+                // loads in flight
                 const int klast = nchunk - 2;
                 int k = q == 0 ? kOctLanes : q;
                 const bool any_interior = k <= klast;
@@ -2166,6 +2188,13 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
         const int steps = __reduce_max_sync(kFull, (unsigned)my_steps);
         const bool raw_ok = theta >= 0;   // raw signed order is key order against it
         int cbase = 0;
+        // the next step's interior chunk is loaded while this one is processed
+        uint32_t nx[8];
+        auto issue = [&](int st) {
+            const int k = q + kOctLanes * st;
+            if (k < nchunk && k != 0 && k != nchunk - 1) ld32(c0 + ((uintptr_t)k << 5), nx);
+        };
+        issue(0);
         for (int st = 0; st < steps; ++st) {
             const int k = q + kOctLanes * st;
             const bool has = k < nchunk;
@@ -2176,9 +2205,14 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
                 if (edge) {
                     pair_load_edge<BF16>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
                 } else {
-                    ld32(c0 + ((uintptr_t)k << 5), w);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) w[x] = nx[x];
                     if (!raw_ok) chunk_to_keys<BF16>(w);
                 }
+            }
+            issue(st + 1);
+            if (has) {
+                const bool edge = k == 0 || k == nchunk - 1;
                 if (theta == kKeyMin) {
                     m = BF16 ? 0xFFFFu : 0xFFu;
                 } else if constexpr (BF16) {
@@ -2206,12 +2240,10 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
                     const int e = __ffs(m) - 1;
                     m &= m - 1;
                     if (pos < kOctCand) {
-                        int32_t key;
                         if constexpr (BF16)
-                            key = (int32_t)reinterpret_cast<const int16_t*>(scr)[e];
+                            sm.ckey16[g][pos] = reinterpret_cast<const int16_t*>(scr)[e];
                         else
-                            key = (int32_t)scr[e];
-                        sm.ckey[g][pos] = key;
+                            sm.ckey[g][pos] = (int32_t)scr[e];
                         sm.cid[g][pos] = (uint16_t)(first_id + e);
                     }
                     ++pos;
@@ -2223,60 +2255,111 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
         __syncwarp();
 
         // ---- step 4: kappa, the K'-th largest candidate key ----
+        // A binary search over [theta, largest candidate]: count(>= lo) >= K'
+        // > count(>= hi) = cnt_hi throughout.  The lane's list positions
+        // 16 q .. 16 q + 15 past the count c are masked out.
         const bool sel_ok = need && !ovf;
         const int c = min(cbase, kOctCand);
-        int32_t kk[16];
-        {
-            const int4* src = reinterpret_cast<const int4*>(&sm.ckey[g][16 * q]);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int4 t4 = src[v];
-                kk[4 * v] = t4.x;
-                kk[4 * v + 1] = t4.y;
-                kk[4 * v + 2] = t4.z;
-                kk[4 * v + 3] = t4.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                if (!(sel_ok && 16 * q + e < c)) kk[e] = INT32_MIN;
-        }
-        int32_t mx = INT32_MIN;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) mx = max(mx, kk[e]);
-        mx = max(mx, __shfl_xor_sync(kFull, mx, 1));
-        mx = max(mx, __shfl_xor_sync(kFull, mx, 2));
-        mx = max(mx, __shfl_xor_sync(kFull, mx, 4));
-        // invariant: count(>= lo) >= K' > count(>= hi) = cnt_hi; the padding
-        // (INT32_MIN, positions >= c) is never counted because mid > lo
-        int64_t lo = theta, hi = (int64_t)mx + 1;
-        int cnt_hi = 0;
-        if (!sel_ok) hi = lo + 1;
+        const int nvalid = sel_ok ? min(max(c - 16 * q, 0), 16) : 0;
+        const uint32_t valid = (1u << nvalid) - 1u;
         const int kp = r.kp;
-        while (__any_sync(kFull, hi - lo > 1)) {
-            const int64_t mid = lo + ((hi - lo) >> 1);
-            const int32_t t = (int32_t)mid;
-            int cnt = 0;
+        uint32_t gtm = 0, eqm = 0;
+        int cnt_hi = 0;
+        if constexpr (BF16) {
+            // 16 keys per lane, two per word; padding holds -32768, which no
+            // searched threshold (> lo >= -32768) counts
+            uint32_t kw[8];
+            {
+                const uint4* src = reinterpret_cast<const uint4*>(&sm.ckey16[g][16 * q]);
+                const uint4 v0 = src[0], v1 = src[1];
+                kw[0] = v0.x; kw[1] = v0.y; kw[2] = v0.z; kw[3] = v0.w;
+                kw[4] = v1.x; kw[5] = v1.y; kw[6] = v1.z; kw[7] = v1.w;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) cnt += kk[e] >= t ? 1 : 0;
-            cnt = oct_sum(cnt);
-            if (hi - lo > 1) {
-                if (cnt >= kp) {
-                    lo = mid;
-                } else {
-                    hi = mid;
-                    cnt_hi = cnt;
+                for (int x = 0; x < 8; ++x) {
+                    const uint32_t keep = ((valid >> (2 * x)) & 1u ? 0x0000FFFFu : 0u) |
+                                          ((valid >> (2 * x + 1)) & 1u ? 0xFFFF0000u : 0u);
+                    kw[x] = (kw[x] & keep) | (0x80008000u & ~keep);
                 }
             }
-        }
-        const int32_t kappa = (int32_t)lo;
-        // keep every candidate above kappa and the first (K' - count above)
-        // of those equal to it in id order
-        uint32_t gtm = 0, eqm = 0;
+            uint32_t mw = kw[0];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const bool valid = sel_ok && 16 * q + e < c;
-            if (valid && kk[e] > kappa) gtm |= 1u << e;
-            if (valid && kk[e] == kappa) eqm |= 1u << e;
+            for (int x = 1; x < 8; ++x) mw = max_s16x2(mw, kw[x]);
+            int32_t mx = max((int32_t)(int16_t)(uint16_t)mw, (int32_t)(int16_t)(uint16_t)(mw >> 16));
+            mx = max(mx, __shfl_xor_sync(kFull, mx, 1));
+            mx = max(mx, __shfl_xor_sync(kFull, mx, 2));
+            mx = max(mx, __shfl_xor_sync(kFull, mx, 4));
+            int32_t lo = theta, hi = mx + 1;
+            if (!sel_ok) hi = lo + 1;
+            while (__any_sync(kFull, hi - lo > 1)) {
+                const int32_t mid = (lo + hi) >> 1;
+                const uint32_t t2 = ((uint32_t)(mid - 1) & 0xFFFFu) * 0x10001u;
+                uint32_t sacc = 0;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) sacc += min_u16x2(max_s16x2(kw[x], t2) ^ t2, 0x00010001u);
+                const int cnt = oct_sum((int)((sacc & 0xFFFFu) + (sacc >> 16)));
+                if (hi - lo > 1) {
+                    if (cnt >= kp) {
+                        lo = mid;
+                    } else {
+                        hi = mid;
+                        cnt_hi = cnt;
+                    }
+                }
+            }
+            // kappa = lo: keep every candidate above it and the first
+            // (K' - count above) of those equal to it, in id order
+            if (sel_ok) {
+                gtm = ge_bits16<8>(kw, lo + 1) & valid;
+                eqm = (lo == kKeyMin ? valid : ge_bits16<8>(kw, lo) & valid) & ~gtm;
+            }
+        } else {
+            int32_t kk[16];
+            {
+                const int4* src = reinterpret_cast<const int4*>(&sm.ckey[g][16 * q]);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int4 t4 = src[v];
+                    kk[4 * v] = t4.x;
+                    kk[4 * v + 1] = t4.y;
+                    kk[4 * v + 2] = t4.z;
+                    kk[4 * v + 3] = t4.w;
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (!((valid >> e) & 1u)) kk[e] = INT32_MIN;
+            }
+            int32_t mx = INT32_MIN;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) mx = max(mx, kk[e]);
+            mx = max(mx, __shfl_xor_sync(kFull, mx, 1));
+            mx = max(mx, __shfl_xor_sync(kFull, mx, 2));
+            mx = max(mx, __shfl_xor_sync(kFull, mx, 4));
+            // the padding (INT32_MIN) is never counted because mid > lo
+            int64_t lo = theta, hi = (int64_t)mx + 1;
+            if (!sel_ok) hi = lo + 1;
+            while (__any_sync(kFull, hi - lo > 1)) {
+                const int64_t mid = lo + ((hi - lo) >> 1);
+                const int32_t t = (int32_t)mid;
+                int cnt = 0;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) cnt += kk[e] >= t ? 1 : 0;
+                cnt = oct_sum(cnt);
+                if (hi - lo > 1) {
+                    if (cnt >= kp) {
+                        lo = mid;
+                    } else {
+                        hi = mid;
+                        cnt_hi = cnt;
+                    }
+                }
+            }
+            const int32_t kappa = (int32_t)lo;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const bool vd = (valid >> e) & 1u;
+                if (vd && kk[e] > kappa) gtm |= 1u << e;
+                if (vd && kk[e] == kappa) eqm |= 1u << e;
+            }
         }
         int tall;
         const int tb = oct_excl_scan(__popc(eqm), q, tall);
@@ -2396,6 +2479,139 @@ cudaError_t launch_dt(const KernelParams& P, const bsa_launch_policy_t& pol, cud
     }
 }
 
+// ===========================================================================
+// Fused index score + select for decode rows.
+//
+// The decode side of the indexer first writes block scores into the unified
+// buffer and then selects from it (vLLM PR #47502 report, 实现拆解 items
+// 1-3: minimax_m3_index_decode_score with score_out = unified_scores[:nd],
+// then one top-k pass).  The pages do not print the score formula; the
+// reading taken is one pooled index key per physical 128-token block (page =
+// sparse block = index-K block, section 关键源码片段), shared by the index
+// heads, with
+//     score[t, h, b] = sum over d of q[t, h, d] * k[block_table[req, b], d]
+// accumulated in fp32 and no scale factor (item 6 removed sm_scale).
+//
+// One CTA per request: its dql * H query rows are staged in shared memory as
+// fp32, each thread scores one causal block at a time against all of them
+// (the block's key row is read once, as 16-byte vectors, and shared by every
+// query row of the request), writes the scores of the causal blocks into the
+// caller's unified buffer, and after a block barrier the CTA's warps select
+// the top-k of its rows from that buffer with the warp path, reading through
+// L2 what the CTA has just written (no second launch and no re-read from
+// HBM).  A causal block whose table entry is missing (b >= max_blocks) or
+// out of range scores -inf.
+// ===========================================================================
+constexpr int kScoreThreads = 256;
+constexpr int kScoreWarps = kScoreThreads / 32;
+
+struct ScoreParams {
+    KernelParams P;          // the selection over the score buffer (fp32, decode rows)
+    const uint16_t* q;       // bf16 [T, H, D]
+    const uint16_t* k;       // bf16 [nb, D]
+    int64_t nb;
+    int32_t D;
+    int32_t nq;              // dql * H query rows per request
+    float* scores;           // element (t, h, b) at t * token_stride + h * head_stride + b
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int NQ>
+__global__ void __launch_bounds__(kScoreThreads, 2) index_score_select_kernel(const ScoreParams S) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const SelectArgs& a = S.P.a;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int D = S.D;
+    const int nq = S.nq;
+    float* qs = reinterpret_cast<float*>(smem_raw);                       // [nq][D]
+    const size_t qbytes = ((size_t)nq * D * 4 + 15) & ~(size_t)15;
+    uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem_raw + qbytes) + (size_t)warp * S.P.cap * 2;
+    int32_t* s_ids = reinterpret_cast<int32_t*>(s_keys + S.P.cap);
+    const int64_t B = a.T / a.dql;
+    for (int64_t req = blockIdx.x; req < B; req += gridDim.x) {
+        const int64_t seq = __ldg(a.seq_lens + req);
+        // the last query row (local_q = dql - 1, position seq - 1) has the
+        // most causal blocks
+        int64_t vmax = seq > 0 ? (seq + kPageSize - 1) >> kLogPageSize : 0;
+        if (vmax > a.M) vmax = a.M;
+        __syncthreads();   // the previous request's readers of qs are done
+        const uint16_t* qsrc = S.q + req * (int64_t)nq * D;
+        for (int i = tid; i < nq * D; i += kScoreThreads) qs[i] = __uint_as_float((uint32_t)qsrc[i] << 16);
+        __syncthreads();
+        const int32_t* table = a.block_table + req * a.max_blocks;
+        for (int64_t b = tid; b < vmax; b += kScoreThreads) {
+            float acc[NQ];
+#pragma unroll
+            for (int x = 0; x < NQ; ++x) acc[x] = 0.f;
+            const int64_t phys = b < a.max_blocks ? (int64_t)__ldg(table + b) : -1;
+            const bool ok = phys >= 0 && phys < S.nb;
+            if (ok) {
+                const uint4* kr = reinterpret_cast<const uint4*>(S.k + phys * D);
+#pragma unroll 4
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 kv = __ldg(kr + c);
+                    const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
+                                         bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
+#pragma unroll
+                    for (int x = 0; x < NQ; ++x) {
+                        if (x < nq) {
+                            const float4* qv = reinterpret_cast<const float4*>(qs + x * D + 8 * c);
+                            const float4 q0 = qv[0], q1 = qv[1];
+                            float s = acc[x];
+                            s = fmaf(kf[0], q0.x, s);
+                            s = fmaf(kf[1], q0.y, s);
+                            s = fmaf(kf[2], q0.z, s);
+                            s = fmaf(kf[3], q0.w, s);
+                            s = fmaf(kf[4], q1.x, s);
+                            s = fmaf(kf[5], q1.y, s);
+                            s = fmaf(kf[6], q1.z, s);
+                            s = fmaf(kf[7], q1.w, s);
+                            acc[x] = s;
+                        }
+                    }
+                }
+            }
+            // rows whose causal count covers b get its score
+#pragma unroll
+            for (int x = 0; x < NQ; ++x) {
+                if (x < nq) {
+                    const int lq = x / (int)a.H;
+                    const int h = x - lq * (int)a.H;
+                    const int64_t len = seq - a.dql + lq + 1;   // causal length of the row
+                    int64_t v = len > 0 ? (len + kPageSize - 1) >> kLogPageSize : 0;
+                    if (v > a.M) v = a.M;
+                    if (b < v) {
+                        const int64_t t = req * a.dql + lq;
+                        S.scores[t * a.token_stride + h * a.head_stride + b] =
+                            ok ? acc[x] : __int_as_float(0xFF800000);
+                    }
+                }
+            }
+        }
+        __syncthreads();   // the request's scores are visible to the whole CTA
+        for (int x = warp; x < nq; x += kScoreWarps) {
+            warp_item<false, 4, 2, true>(S.P, req * nq + x, 0, s_keys, s_ids, lane);
+            __syncwarp();
+        }
+    }
+}
+
+template <int NQ>
+cudaError_t launch_score_nq(const ScoreParams& S, int grid, size_t smem, cudaStream_t st) {
+    auto kern = index_score_select_kernel<NQ>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<grid, kScoreThreads, smem, st>>>(S);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
@@ -2430,6 +2646,42 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
                                          : launch_octet<false>(P, pol, stream);
     return a.dtype == BSA_DTYPE_BF16 ? launch_dt<true>(P, pol, stream)
                                      : launch_dt<false>(P, pol, stream);
+}
+
+cudaError_t launch_index_score_select(const SelectArgs& a, const uint16_t* q, const uint16_t* k,
+                                      int64_t nb, int32_t D, float* scores, cudaStream_t stream) {
+    ScoreParams S;
+    KernelParams& P = S.P;
+    P.a = a;
+    div_magic((uint32_t)(a.H > 0 ? a.H : 1), &P.a.h_mul, &P.a.h_shift);
+    div_magic((uint32_t)(a.dql > 0 ? a.dql : 1), &P.a.dql_mul, &P.a.dql_shift);
+    P.ws = Split{nullptr, nullptr, nullptr, nullptr};
+    P.chunks_per_row = 1;
+    // the warp path with 4 fp32 vectors per lane per pass
+    P.cap = (a.K + 32 * 4 + 31) / 32 * 32;
+    P.rows = a.T * a.H;
+    P.buf_lo = reinterpret_cast<uintptr_t>(scores);
+    P.buf_hi = P.buf_lo + (uintptr_t)(((a.T > 0 ? a.T - 1 : 0) * a.token_stride +
+                                        (a.H > 0 ? a.H - 1 : 0) * a.head_stride + a.M) * 4);
+    const int64_t max_vecs = (a.M + 3) / 4 + 1;
+    P.vecs_per_chunk = (int32_t)((max_vecs + 127) / 128 * 128);
+    S.q = q;
+    S.k = k;
+    S.nb = nb;
+    S.D = D;
+    S.nq = (int32_t)(a.dql * a.H);
+    S.scores = scores;
+    const int64_t B = a.T / a.dql;
+    if (B == 0) return cudaSuccess;
+    const size_t smem = (((size_t)S.nq * D * 4 + 15) & ~(size_t)15) +
+                        (size_t)kScoreWarps * P.cap * 8;
+    int64_t grid = (int64_t)device_sm_count() * 4;
+    if (grid > B) grid = B;
+    if (S.nq <= 1) return launch_score_nq<1>(S, (int)grid, smem, stream);
+    if (S.nq <= 2) return launch_score_nq<2>(S, (int)grid, smem, stream);
+    if (S.nq <= 4) return launch_score_nq<4>(S, (int)grid, smem, stream);
+    if (S.nq <= 8) return launch_score_nq<8>(S, (int)grid, smem, stream);
+    return launch_score_nq<16>(S, (int)grid, smem, stream);
 }
 
 }  // namespace bsa

@@ -200,6 +200,42 @@ int bsa_topk_select_sparse_table(const void* scores, int32_t dtype, int64_t num_
                                  int32_t* sparse_bt, int32_t* sparse_ctx, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* Limits of the fused index score + select. */
+#define BSA_MAX_INDEX_DIM 1024       /* index head dimension D                    */
+#define BSA_MAX_INDEX_QUERIES 16     /* decode_query_len * H query rows per request */
+
+/* Fused index score + select (+ optional sparse table) of decode rows
+ * ([47502] 实现拆解 items 1-3: the decode score kernel writes score_out =
+ * unified_scores[:nd] and one top-k pass selects from it; here both run in
+ * one launch).  The pages do not print the score formula.  Reading taken:
+ * one pooled bf16 index key per physical 128-token block (page = sparse block
+ * = index-K block, [47502] 关键源码片段), shared by the index heads, and
+ *   score[t, h, b] = sum_d q_idx[t, h, d] * k_idx[block_table[req, b], d]
+ * accumulated in fp32 with no scale factor (item 6 removed sm_scale), for
+ * the causal blocks b < v_t = min(M, cdiv(pos + 1, 128)) of each decode row
+ * (t = req * decode_query_len + local_q, pos = seq_lens[req] -
+ * decode_query_len + local_q).  A causal block with no usable key (b >=
+ * max_blocks, or a physical id outside [0, num_phys_blocks)) scores -inf.
+ *   q_idx: bf16 [T, H, D], 16-byte aligned; k_idx: bf16 [num_phys_blocks, D],
+ *   16-byte aligned; D a multiple of 8, at most BSA_MAX_INDEX_DIM;
+ *   decode_query_len * H at most BSA_MAX_INDEX_QUERIES.
+ *   scores: fp32 unified buffer, element (t, h, b) at t * token_stride +
+ *   h * head_stride + b; the causal entries b < v_t are written, the rest is
+ *   left as it is (the pages pre-fill it with -inf).
+ *   The selection over the written scores is that of
+ *   bsa_topk_select_sparse_table (same K, num_init, num_local, output
+ *   layouts); sparse_bt / sparse_ctx may both be NULL (no table).
+ *   Needs no workspace.
+ * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_TOPK, BSA_ERR_ALIGN. */
+int bsa_index_score_topk_select(const void* q_idx, const void* k_idx, int64_t num_phys_blocks,
+                                int64_t H, int64_t D, const int32_t* block_table,
+                                int64_t max_blocks, const int32_t* seq_lens, int64_t num_reqs,
+                                int32_t decode_query_len, float* scores, int64_t M,
+                                int64_t token_stride, int64_t head_stride, int32_t K,
+                                int32_t num_init, int32_t num_local, int32_t* out_idx,
+                                int64_t out_token_stride, int64_t out_head_stride,
+                                int32_t* sparse_bt, int32_t* sparse_ctx, void* stream);
+
 /* Size of the device scratch array behind bsa_topk_select_noalloc. */
 #define BSA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -232,3 +232,29 @@ def random_block_table(B: int, MB: int, seed: int, device="cpu") -> torch.Tensor
     """Physical block ids drawn uniformly from [0, 2^27) (so id*8+7 fits int32)."""
     g = generator(seed, device)
     return torch.randint(0, 1 << 27, (B, MB), generator=g, device=device, dtype=torch.int32)
+
+
+def index_inputs(seed: int, T: int, H: int, D: int, num_phys_blocks: int, device="cpu"):
+    """Index queries bf16 [T, H, D] drawn N(0, 1/D) and pooled index keys bf16
+    [num_phys_blocks, D] drawn N(0, 1), so that a block score (a dot product
+    over D) is about N(0, 1) like the score workloads above."""
+    g = generator(seed, device)
+    q = torch.randn(T, H, D, generator=g, device=device) / (D ** 0.5)
+    k = torch.randn(num_phys_blocks, D, generator=g, device=device)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16)
+
+
+def paged_block_table(B: int, MB: int, num_phys_blocks: int, seed: int, frac_missing: float = 0.0,
+                      device="cpu") -> torch.Tensor:
+    """int32 [B, MB] of distinct physical block ids from [0, num_phys_blocks)
+    (a seeded permutation), with about `frac_missing` of the entries set to
+    -1 or to an id past the end."""
+    g = generator(seed, device)
+    perm = torch.randperm(num_phys_blocks, generator=g, device=device)[:B * MB]
+    bt = perm.view(B, MB).to(torch.int32)
+    if frac_missing > 0:
+        u = torch.rand((B, MB), generator=g, device=device)
+        bt = torch.where(u < frac_missing / 2, torch.full_like(bt, -1), bt)
+        bt = torch.where((u >= frac_missing / 2) & (u < frac_missing),
+                         torch.full_like(bt, num_phys_blocks + 5), bt)
+    return bt

@@ -56,3 +56,18 @@ def test_roofline_kernel_and_traffic_follow_the_policy():
                 assert bench.read_traffic(path, "select_kernel", 64, 131072, f) is None
                 assert bench.read_traffic(path, "pair_select_kernel", 32, 131072, f) is None
                 assert bench.read_traffic(path, "pair_select_kernel", 16, 65536, f) is None
+
+
+def test_index_score_bytes_hand_example():
+    """The fused index score + select's byte count: queries, the table
+    entries and keys of each request's causal blocks, the causal scores of
+    each row, sequence lengths and ids."""
+    sys.path.insert(0, ROOT)
+    import bench
+    seq = np.array([0, 200, 129], dtype=np.int32)    # 0, 2, 2 causal blocks
+    b = bench.index_score_bytes(seq, 1, 2, 8, 4, 3, valid_blocks=3)
+    q = 3 * 2 * 8 * 2                 # [T, H, D] bf16
+    table = 4 * 4                     # 4 causal blocks
+    keys = 3 * 8 * 2                  # 3 usable keys of D bf16
+    scores = (0 + 2 + 2) * 2 * 4      # causal entries x heads x fp32
+    assert b == q + table + keys + scores + 3 * 4 + 3 * 2 * 3 * 4
