@@ -63,9 +63,13 @@ def _declare(lib):
     u16p = ctypes.POINTER(ctypes.c_uint16)
     lib.oracle_index_scores.argtypes = [u16p, u16p, i64, i32p, i64, i32p, i64, i32, i64, i64,
                                         i64, ctypes.POINTER(ctypes.c_double)]
+    lib.oracle_sparse_decode_attention.argtypes = [u16p, u16p, u16p, i64, i32p, i32p, i64, i64,
+                                                   i64, i64, i32, ctypes.c_double,
+                                                   ctypes.POINTER(ctypes.c_double)]
     for name in ("oracle_num_valid_pages_decode", "oracle_num_valid_pages_varlen",
                  "oracle_topk_select", "oracle_build_sparse_block_table",
-                 "oracle_topk_select_sparse_table", "oracle_index_scores"):
+                 "oracle_topk_select_sparse_table", "oracle_index_scores",
+                 "oracle_sparse_decode_attention"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -245,4 +249,29 @@ def index_scores(q, k, block_table, seq_lens, dql: int, M: int, lib=None) -> np.
                                         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     if rc != 0:
         raise ValueError(f"oracle_index_scores rc={rc}")
+    return out
+
+
+def sparse_decode_attention(q, k_cache, v_cache, sparse_bt, sparse_ctx, scale: float,
+                            lib=None) -> np.ndarray:
+    """Sparse decode attention in float64: q bf16 [T, H, G, D], k_cache and
+    v_cache bf16 [num_pages, 16, H, D], sparse_bt int32 [T, H, K*8],
+    sparse_ctx int32 [T, H]; returns [T, H, G, D]."""
+    qb = _bf16_bits(q)
+    kb = _bf16_bits(k_cache)
+    vb = _bf16_bits(v_cache)
+    T, H, G, D = qb.shape
+    NP = kb.shape[0]
+    assert kb.shape == (NP, 16, H, D) and vb.shape == kb.shape
+    bt = _i32(sparse_bt)
+    ctx = _i32(sparse_ctx)
+    assert bt.shape[:2] == (T, H) and bt.shape[2] % 8 == 0 and ctx.shape == (T, H)
+    K = bt.shape[2] // 8
+    out = np.empty((T, H, G, D), dtype=np.float64)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    rc = _load(lib).oracle_sparse_decode_attention(
+        qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p), NP, _ptr(bt),
+        _ptr(ctx), T, H, G, D, K, float(scale), out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    if rc != 0:
+        raise ValueError(f"oracle_sparse_decode_attention rc={rc}")
     return out

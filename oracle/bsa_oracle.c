@@ -359,3 +359,72 @@ int oracle_index_scores(const uint16_t* q, const uint16_t* k, int64_t NB,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Sparse decode attention over the page-16 table                            */
+/* ------------------------------------------------------------------------ */
+
+/* The consumer of the sparse table: "vLLM PR #47984 report", 实现拆解 items
+ * 1-2 (the ROCm sparse paged-attention decode reads the page-16 table and
+ * its sparse_ctx) and "vLLM PR #47502 report", 实现拆解 item 5 (the sparse
+ * decode kernels count their valid blocks from the sequence position).  The
+ * pages show the interface only.  Readings taken: index head h selects for
+ * KV head h, which G query heads share; the KV cache is paged in 16-token
+ * pages (bf16 [num_pages, 16, H, D], page id = physical 128-token block * 8
+ * + page, as the table writes it); row (t, h) attends to its first
+ * ctx = sparse_ctx[t, h] table tokens, token j sitting in page
+ * sparse_bt[t, h, j / 16] at slot j % 16; and each query head g takes
+ *     out[t, h, g] = sum_j softmax_j(scale * q[t, h, g] . k_j) v_j
+ * in exact arithmetic (here double).  A row with an empty context yields
+ * zeros; a token whose page id lies outside [0, num_pages) takes no part.
+ *
+ * q: bf16 [T, H, G, D]; k_cache, v_cache: bf16 [num_pages, 16, H, D];
+ * sparse_bt: int32 [T, H, K * 8]; sparse_ctx: int32 [T, H];
+ * out: double [T, H, G, D]. */
+int oracle_sparse_decode_attention(const uint16_t* q, const uint16_t* k_cache,
+                                   const uint16_t* v_cache, int64_t num_pages,
+                                   const int32_t* sparse_bt, const int32_t* sparse_ctx,
+                                   int64_t T, int64_t H, int64_t G, int64_t D, int32_t K,
+                                   double scale, double* out) {
+    if (T < 0 || H < 1 || G < 1 || D < 1 || K < 1) return -1;
+    const int64_t width = (int64_t)K * ORACLE_PAGES_PER_BLOCK;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(width * ORACLE_SUB_PAGE));
+    if (!s) return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            const int32_t* bt = sparse_bt + (t * H + h) * width;
+            int64_t ctx = sparse_ctx[t * H + h];
+            if (ctx > width * ORACLE_SUB_PAGE) ctx = width * ORACLE_SUB_PAGE;
+            for (int64_t g = 0; g < G; ++g) {
+                const uint16_t* qv = q + ((t * H + h) * G + g) * D;
+                double* o = out + ((t * H + h) * G + g) * D;
+                for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+                double mx = -INFINITY;
+                for (int64_t j = 0; j < ctx; ++j) {
+                    const int64_t page = bt[j / ORACLE_SUB_PAGE];
+                    s[j] = -INFINITY;
+                    if (page < 0 || page >= num_pages) continue;
+                    const uint16_t* kv = k_cache + ((page * ORACLE_SUB_PAGE + j % ORACLE_SUB_PAGE) * H + h) * D;
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        dot += decode_bits(qv[d], 8, 7).value * decode_bits(kv[d], 8, 7).value;
+                    s[j] = scale * dot;
+                    if (s[j] > mx) mx = s[j];
+                }
+                if (mx == -INFINITY) continue;   /* empty context: zeros */
+                double sum = 0.0;
+                for (int64_t j = 0; j < ctx; ++j) {
+                    if (s[j] == -INFINITY) continue;
+                    const double p = exp(s[j] - mx);
+                    const int64_t page = bt[j / ORACLE_SUB_PAGE];
+                    const uint16_t* vv = v_cache + ((page * ORACLE_SUB_PAGE + j % ORACLE_SUB_PAGE) * H + h) * D;
+                    for (int64_t d = 0; d < D; ++d) o[d] += p * decode_bits(vv[d], 8, 7).value;
+                    sum += p;
+                }
+                for (int64_t d = 0; d < D; ++d) o[d] /= sum;
+            }
+        }
+    }
+    free(s);
+    return 0;
+}

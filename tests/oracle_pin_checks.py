@@ -492,6 +492,89 @@ def check_index_scores_one_hot(lib=None, trials=30, seed=42):
                     assert got[t, h, b] == want, (t, h, b, got[t, h, b], want)
 
 
+def _attention_case(rng, G=None, D=None):
+    """A small decode batch for the attention oracle: a sparse table built by
+    the (pinned) table oracle from random selections, and random bf16 q, k,
+    v over a page-16 cache."""
+    import torch
+    dql = int(rng.integers(1, 4))
+    B = int(rng.integers(1, 4))
+    H = int(rng.integers(1, 3))
+    G = int(rng.integers(1, 4)) if G is None else G
+    D = int(rng.choice([4, 8, 16])) if D is None else D
+    K = int(rng.integers(1, 6))
+    MB = 6
+    seq = rng.integers(0, 128 * MB, B).astype(np.int32)
+    seq[rng.random(B) < 0.2] = 0
+    ids = rng.integers(-1, MB + 1, (B * dql, H, K)).astype(np.int32)
+    NP = B * MB * 8
+    table = rng.permutation(B * MB).astype(np.int32).reshape(B, MB)
+    bt, ctx = oracle.build_sparse_block_table(ids, table, seq, dql)
+    q = torch.from_numpy(rng.standard_normal((B * dql, H, G, D)).astype(np.float32))
+    k = torch.from_numpy(rng.standard_normal((NP, 16, H, D)).astype(np.float32))
+    v = torch.from_numpy(rng.standard_normal((NP, 16, H, D)).astype(np.float32))
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), bt, ctx
+
+
+def check_attention_against_numpy(lib=None, trials=30, seed=51):
+    """The attention oracle against a vectorised float64 numpy formulation:
+    gather the row's ctx tokens through the page-16 table, softmax of the
+    scaled dot products, weighted sum of the values; zeros for an empty
+    context."""
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        q, k, v, bt, ctx = _attention_case(rng)
+        scale = float(rng.uniform(0.05, 1.0))
+        got = oracle.sparse_decode_attention(q, k, v, bt, ctx, scale, lib=lib)
+        qd = q.float().numpy().astype(np.float64)
+        kd = k.float().numpy().astype(np.float64)
+        vd = v.float().numpy().astype(np.float64)
+        T, H, G, D = qd.shape
+        for t in range(T):
+            for h in range(H):
+                n = int(ctx[t, h])
+                if n == 0:
+                    assert (got[t, h] == 0).all()
+                    continue
+                j = np.arange(n)
+                pages = bt[t, h][j // 16]
+                kj = kd[pages, j % 16, h]                       # [n, D]
+                vj = vd[pages, j % 16, h]
+                sc = scale * (qd[t, h] @ kj.T)                  # [G, n]
+                p = np.exp(sc - sc.max(axis=1, keepdims=True))
+                want = (p / p.sum(axis=1, keepdims=True)) @ vj
+                assert np.allclose(got[t, h], want, rtol=1e-12, atol=1e-12), (t, h)
+
+
+def check_attention_closed_forms(lib=None, seed=52):
+    """Equal keys give uniform weights, so the output is the mean of the
+    context's values; a one-token context returns that token's value
+    exactly."""
+    import torch
+    rng = np.random.default_rng(seed)
+    for _ in range(10):
+        q, k, v, bt, ctx = _attention_case(rng)
+        k = torch.ones_like(k)                          # every key equal
+        got = oracle.sparse_decode_attention(q, k, v, bt, ctx, 0.7, lib=lib)
+        vd = v.float().numpy().astype(np.float64)
+        T, H = ctx.shape
+        for t in range(T):
+            for h in range(H):
+                n = int(ctx[t, h])
+                if n == 0:
+                    continue
+                j = np.arange(n)
+                mean = vd[bt[t, h][j // 16], j % 16, h].mean(axis=0)
+                assert np.allclose(got[t, h], mean[None, :], rtol=1e-12, atol=1e-12)
+        one = np.minimum(ctx, 1).astype(np.int32)
+        got = oracle.sparse_decode_attention(q, k, v, bt, one, 0.7, lib=lib)
+        for t in range(T):
+            for h in range(H):
+                if one[t, h]:
+                    want = vd[bt[t, h][0], 0, h]
+                    assert np.array_equal(got[t, h], np.broadcast_to(want, got[t, h].shape))
+
+
 ALL_CHECKS = [
     check_total_order_golden,
     check_total_order_exhaustive_bf16,
@@ -511,4 +594,6 @@ ALL_CHECKS = [
     check_fused_token_enumeration,
     check_index_scores_against_numpy,
     check_index_scores_one_hot,
+    check_attention_against_numpy,
+    check_attention_closed_forms,
 ]

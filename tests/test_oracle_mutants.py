@@ -85,6 +85,18 @@ MUTANTS = [
      "row[b] = -INFINITY;", "row[b] = 0.0;"),
     ("score_key_transposed",
      "decode_bits(k[phys * D + d], 8, 7)", "decode_bits(k[phys + d * NB], 8, 7)"),
+    # mistakes in the sparse decode attention
+    ("attn_scale_dropped",
+     "s[j] = scale * dot;", "s[j] = dot;"),
+    ("attn_key_slot_reversed",
+     "k_cache + ((page * ORACLE_SUB_PAGE + j % ORACLE_SUB_PAGE) * H + h) * D;",
+     "k_cache + ((page * ORACLE_SUB_PAGE + 15 - j % ORACLE_SUB_PAGE) * H + h) * D;"),
+    ("attn_value_head_ignored",
+     "v_cache + ((page * ORACLE_SUB_PAGE + j % ORACLE_SUB_PAGE) * H + h) * D;",
+     "v_cache + ((page * ORACLE_SUB_PAGE + j % ORACLE_SUB_PAGE) * H) * D;"),
+    ("attn_last_token_dropped",
+     "if (ctx > width * ORACLE_SUB_PAGE) ctx = width * ORACLE_SUB_PAGE;",
+     "if (ctx > width * ORACLE_SUB_PAGE) ctx = width * ORACLE_SUB_PAGE;\n            ctx -= ctx > 0;"),
 ]
 
 
