@@ -42,8 +42,9 @@ EXPORTED = [
     "bsa_status_string", "bsa_num_valid_pages_decode", "bsa_num_valid_pages_varlen",
     "bsa_topk_workspace_bytes", "bsa_topk_select", "bsa_build_sparse_block_table",
     "bsa_topk_select_sparse_table", "bsa_select_policy", "bsa_topk_select_noalloc",
-    "bsa_index_score_topk_select",
+    "bsa_index_score_topk_select", "bsa_sparse_decode_attention",
 ]
+MAX_ATTN_GROUP = 8
 MAX_INDEX_DIM = 1024
 MAX_INDEX_QUERIES = 16
 
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
             L.bsa_index_score_topk_select.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64,
                                                       i32, vp, i64, i64, i64, i32, i32, i32, vp,
                                                       i64, i64, vp, vp, vp]
+            L.bsa_sparse_decode_attention.argtypes = [vp, vp, vp, i64, vp, vp, i64, i64, i64, i64,
+                                                      i32, ctypes.c_float, vp, vp]
             for name in EXPORTED[1:]:
                 if name != "bsa_topk_workspace_bytes":
                     getattr(L, name).restype = ctypes.c_int
@@ -425,3 +428,41 @@ def bsa_index_score_topk_select(q_idx: torch.Tensor, k_idx: torch.Tensor,
           num_init, num_local, _ptr(out_idx), ots, ohs, _ptr(sparse_bt), _ptr(sparse_ctx),
           _stream(dev))
     return scores, out_idx, sparse_bt, sparse_ctx
+
+
+def bsa_sparse_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                sparse_bt: torch.Tensor, sparse_ctx: torch.Tensor,
+                                scale: float | None = None,
+                                out: torch.Tensor | None = None) -> torch.Tensor:
+    """Sparse decode attention over the page-16 table.  q bf16 [T, H, G, D],
+    k_cache / v_cache bf16 [num_pages, 16, H, D], sparse_bt int32
+    [T, H, K*8], sparse_ctx int32 [T, H]; returns fp32 [T, H, G, D].  The
+    scale defaults to 1 / sqrt(D)."""
+    dev = q.device
+    if not isinstance(q, torch.Tensor) or not q.is_cuda or q.dim() != 4 \
+            or q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bf16 CUDA tensor [T, H, G, D]")
+    T, H, G, D = q.shape
+    for name, c in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if not isinstance(c, torch.Tensor) or c.device != dev or c.dtype != torch.bfloat16 \
+                or not c.is_contiguous() or c.dim() != 4 or tuple(c.shape[1:]) != (16, H, D):
+            raise ValueError(f"{name} must be a contiguous bf16 tensor [num_pages, 16, {H}, {D}] "
+                             f"on {dev}")
+    if k_cache.shape[0] != v_cache.shape[0]:
+        raise ValueError("k_cache and v_cache hold different page counts")
+    _dev_i32(sparse_bt, "sparse_bt", dev)
+    if sparse_bt.dim() != 3 or tuple(sparse_bt.shape[:2]) != (T, H) or sparse_bt.shape[2] % 8:
+        raise ValueError(f"sparse_bt must be [{T}, {H}, K*8]")
+    K = sparse_bt.shape[2] // PAGES_PER_SPARSE_BLOCK
+    _dev_i32(sparse_ctx, "sparse_ctx", dev, (T, H))
+    if out is None:
+        out = torch.empty((T, H, G, D), dtype=torch.float32, device=dev)
+    if out.dtype != torch.float32 or out.device != dev or not out.is_contiguous() \
+            or tuple(out.shape) != (T, H, G, D):
+        raise ValueError(f"out must be a contiguous fp32 tensor [{T}, {H}, {G}, {D}] on {dev}")
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    _call("bsa_sparse_decode_attention", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          k_cache.shape[0], _ptr(sparse_bt), _ptr(sparse_ctx), T, H, G, D, K, ctypes.c_float(scale),
+          _ptr(out), _stream(dev))
+    return out

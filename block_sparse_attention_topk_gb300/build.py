@@ -21,7 +21,7 @@ BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_NAME = f"libbsa_topk_{platform.machine()}.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
-SOURCES = ["bsa_select.cu", "bsa_table.cu", "bsa_capi.cu", "bsa_noalloc.cu"]
+SOURCES = ["bsa_select.cu", "bsa_table.cu", "bsa_capi.cu", "bsa_noalloc.cu", "bsa_attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

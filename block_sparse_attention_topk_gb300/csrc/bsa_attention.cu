@@ -1,0 +1,257 @@
+// bsa_attention.cu -- sparse decode attention over the page-16 sparse block
+// table: the consumer of the selector's table.
+//
+// What it computes (vLLM PR #47984 report, "[ROCm][MiniMax-M3][Spec Decode]
+// Support speculative decode with AITER sparse PA", sections 实现拆解 items
+// 1-2: the decode sparse paged attention reads the page-16 table and its
+// sparse context length; vLLM PR #47502 report, 实现拆解 item 5: the sparse
+// decode kernels take their valid blocks from the sequence position).  The
+// pages show only the interface; the readings taken are: index head h
+// selects for KV head h, shared by G query heads; the KV cache is paged in
+// 16-token pages, bf16 [num_pages, 16, H, D], and a table entry is a page
+// id (physical 128-token block * 8 + page); row (t, h) attends to its first
+// ctx = sparse_ctx[t, h] tokens in table order, token j in page
+// sparse_bt[t, h, j / 16] at slot j % 16; and query head g takes
+//     out[t, h, g] = sum_j softmax_j(scale * q[t, h, g] . k_j) v_j.
+// A row with an empty context yields zeros, and a token whose page id lies
+// outside [0, num_pages) takes no part.
+//
+// How: one warp per row (t, h) and all its G query heads.  The row's queries
+// sit in shared memory as fp32.  The context is walked 32 tokens (two pages)
+// at a time: each lane scores one token against every query head (reading
+// the token's key row as 16-byte vectors), the warp folds the tile into a
+// running maximum and sum per head (online softmax, Milakov and Gimelshein,
+// "Online normalizer calculation for softmax", 2018), and then the lanes,
+// each owning D / 32 output dimensions, accumulate the tile's value rows
+// (one coalesced row per token) weighted by the broadcast probabilities.
+// Decode attention moves each key and value once and does O(G) flops per
+// element, so it is bound by memory and runs on the CUDA cores.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "bsa_internal.h"
+
+namespace bsa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kAttnWarps = 4;
+
+struct AttnParams {
+    const uint16_t* q;       // bf16 [rows, G, D]
+    const uint16_t* k;       // bf16 [num_pages, 16, H, D]
+    const uint16_t* v;       // bf16 [num_pages, 16, H, D]
+    int64_t num_pages;
+    const int32_t* bt;       // int32 [rows, width]
+    const int32_t* ctx;      // int32 [rows]
+    int64_t rows;            // T * H
+    int32_t H, G, width;     // width = topk * 8 table entries per row
+    float scale;
+    float* out;              // fp32 [rows, G, D]
+};
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, d));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) x += __shfl_xor_sync(kFull, x, d);
+    return x;
+}
+
+// DL bf16 values at p (DL * 2 bytes, aligned to that) as fp32.
+template <int DL>
+__device__ __forceinline__ void load_dl(const uint16_t* p, float (&f)[DL]) {
+    if constexpr (DL == 2) {
+        const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(p));
+        f[0] = bf_lo(w);
+        f[1] = bf_hi(w);
+    } else if constexpr (DL == 4) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+        f[0] = bf_lo(w.x);
+        f[1] = bf_hi(w.x);
+        f[2] = bf_lo(w.y);
+        f[3] = bf_hi(w.y);
+    } else {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = bf_lo(ws[i]);
+            f[2 * i + 1] = bf_hi(ws[i]);
+        }
+    }
+}
+
+// GP >= G query heads (a power of two), DL = D / 32 dimensions per lane.
+template <int GP, int DL>
+__global__ void __launch_bounds__(kAttnWarps * 32)
+sparse_decode_attention_kernel(const AttnParams A) {
+    constexpr int D = 32 * DL;
+    extern __shared__ __align__(16) float qs_all[];   // [warps][GP][D]
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    float* qs = qs_all + (size_t)warp * GP * D;
+    const int G = A.G;
+    const int cap = A.width * BSA_SUB_PAGE_SIZE;
+    for (int64_t row = (int64_t)blockIdx.x * kAttnWarps + warp; row < A.rows;
+         row += (int64_t)gridDim.x * kAttnWarps) {
+        const int h = (int)(row % A.H);
+        const int32_t* bt = A.bt + row * A.width;
+        const int ctx = max(0, min(__ldg(A.ctx + row), cap));
+        const uint16_t* qrow = A.q + row * (int64_t)G * D;
+        for (int i = lane; i < G * D; i += 32) qs[i] = __uint_as_float((uint32_t)__ldg(qrow + i) << 16);
+        __syncwarp();
+        float m[GP], l[GP], acc[GP][DL];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int d = 0; d < DL; ++d) acc[g][d] = 0.f;
+        }
+        for (int tile = 0; tile < ctx; tile += 32) {
+            // ---- scores: lane j of the tile takes token tile + j ----
+            const int j = tile + lane;
+            const int32_t page = j < ctx ? __ldg(bt + (j >> 4)) : -1;
+            const bool ok = page >= 0 && page < A.num_pages;
+            float s[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) s[g] = 0.f;
+            if (ok) {
+                const uint4* kr = reinterpret_cast<const uint4*>(
+                    A.k + (((int64_t)page * BSA_SUB_PAGE_SIZE + (j & 15)) * A.H + h) * D);
+#pragma unroll 4
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 kv = __ldg(kr + c);
+                    const float kf[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
+                                         bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        if (g < G) {
+                            const float4* qv = reinterpret_cast<const float4*>(qs + g * D + 8 * c);
+                            const float4 q0 = qv[0], q1 = qv[1];
+                            float a = s[g];
+                            a = fmaf(kf[0], q0.x, a);
+                            a = fmaf(kf[1], q0.y, a);
+                            a = fmaf(kf[2], q0.z, a);
+                            a = fmaf(kf[3], q0.w, a);
+                            a = fmaf(kf[4], q1.x, a);
+                            a = fmaf(kf[5], q1.y, a);
+                            a = fmaf(kf[6], q1.z, a);
+                            a = fmaf(kf[7], q1.w, a);
+                            s[g] = a;
+                        }
+                    }
+                }
+            }
+            // ---- online softmax: fold the tile into the running max / sum ----
+            float p[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                const float sg = ok ? s[g] * A.scale : -INFINITY;
+                const float mn = fmaxf(m[g], warp_max(sg));
+                // mn stays -inf until a usable token has been seen
+                const float corr = mn == -INFINITY ? 1.f : expf(m[g] - mn);
+                p[g] = ok ? expf(sg - mn) : 0.f;
+                l[g] = l[g] * corr + warp_sum(p[g]);
+#pragma unroll
+                for (int d = 0; d < DL; ++d) acc[g][d] *= corr;
+                m[g] = mn;
+            }
+            // ---- values: the lane owns dimensions [lane * DL, lane * DL + DL) ----
+            const int nt = min(32, ctx - tile);
+            for (int jj = 0; jj < nt; ++jj) {
+                const int jt = tile + jj;
+                const int32_t pg = __ldg(bt + (jt >> 4));
+                if (pg < 0 || pg >= A.num_pages) continue;   // the same for every lane
+                float vf[DL];
+                load_dl<DL>(A.v + (((int64_t)pg * BSA_SUB_PAGE_SIZE + (jt & 15)) * A.H + h) * D +
+                                lane * DL,
+                            vf);
+#pragma unroll
+                for (int g = 0; g < GP; ++g) {
+                    const float pj = __shfl_sync(kFull, p[g], jj);
+#pragma unroll
+                    for (int d = 0; d < DL; ++d) acc[g][d] = fmaf(pj, vf[d], acc[g][d]);
+                }
+            }
+        }
+        float* orow = A.out + row * (int64_t)G * D;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            if (g < G) {
+                const float inv = l[g] > 0.f ? 1.f / l[g] : 0.f;
+#pragma unroll
+                for (int d = 0; d < DL; ++d) orow[g * D + lane * DL + d] = acc[g][d] * inv;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+template <int GP, int DL>
+cudaError_t launch_attn(const AttnParams& A, cudaStream_t st) {
+    const size_t smem = (size_t)kAttnWarps * GP * 32 * DL * sizeof(float);
+    int64_t grid = (A.rows + kAttnWarps - 1) / kAttnWarps;
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    if (grid > cap) grid = cap;
+    sparse_decode_attention_kernel<GP, DL><<<(int)grid, kAttnWarps * 32, smem, st>>>(A);
+    return cudaGetLastError();
+}
+
+template <int DL>
+cudaError_t launch_attn_g(const AttnParams& A, cudaStream_t st) {
+    if (A.G <= 1) return launch_attn<1, DL>(A, st);
+    if (A.G <= 2) return launch_attn<2, DL>(A, st);
+    if (A.G <= 4) return launch_attn<4, DL>(A, st);
+    return launch_attn<8, DL>(A, st);
+}
+
+}  // namespace
+}  // namespace bsa
+
+using namespace bsa;
+
+extern "C" int bsa_sparse_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                           int64_t num_pages, const int32_t* sparse_bt,
+                                           const int32_t* sparse_ctx, int64_t T, int64_t H,
+                                           int64_t G, int64_t D, int32_t K, float scale,
+                                           float* out, void* stream) {
+    if (T < 0 || H < 1 || num_pages < 0) return BSA_ERR_SHAPE;
+    if (G < 1 || G > BSA_MAX_ATTN_GROUP) return BSA_ERR_SHAPE;
+    if (D != 64 && D != 128 && D != 256) return BSA_ERR_SHAPE;
+    if (K < 1 || K > BSA_MAX_TOPK) return BSA_ERR_TOPK;
+    if (T == 0) return BSA_OK;
+    if (q == nullptr || sparse_bt == nullptr || sparse_ctx == nullptr || out == nullptr ||
+        (num_pages > 0 && (k_cache == nullptr || v_cache == nullptr)))
+        return BSA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(q) & 15) != 0 || (reinterpret_cast<uintptr_t>(k_cache) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(v_cache) & 15) != 0 || (reinterpret_cast<uintptr_t>(out) & 3) != 0)
+        return BSA_ERR_ALIGN;
+    AttnParams A;
+    A.q = static_cast<const uint16_t*>(q);
+    A.k = static_cast<const uint16_t*>(k_cache);
+    A.v = static_cast<const uint16_t*>(v_cache);
+    A.num_pages = num_pages;
+    A.bt = sparse_bt;
+    A.ctx = sparse_ctx;
+    A.rows = T * H;
+    A.H = (int32_t)H;
+    A.G = (int32_t)G;
+    A.width = K * BSA_PAGES_PER_SPARSE_BLOCK;
+    A.scale = scale;
+    A.out = out;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (D == 64) e = launch_attn_g<2>(A, st);
+    else if (D == 128) e = launch_attn_g<4>(A, st);
+    else e = launch_attn_g<8>(A, st);
+    return e == cudaSuccess ? BSA_OK : (int)e;
+}

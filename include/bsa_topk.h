@@ -236,6 +236,32 @@ int bsa_index_score_topk_select(const void* q_idx, const void* k_idx, int64_t nu
                                 int64_t out_token_stride, int64_t out_head_stride,
                                 int32_t* sparse_bt, int32_t* sparse_ctx, void* stream);
 
+/* Largest number of query heads sharing one KV head in the attention call. */
+#define BSA_MAX_ATTN_GROUP 8
+
+/* Sparse decode attention over the page-16 sparse block table: the consumer
+ * of bsa_topk_select_sparse_table's output ([47984] 实现拆解 items 1-2, the
+ * decode sparse paged attention reading the page-16 table and its sparse
+ * context length; [47502] 实现拆解 item 5).  The pages show the interface
+ * only.  Readings taken: index head h selects for KV head h, shared by G
+ * query heads; the KV cache is paged in 16-token pages; row (t, h) attends to
+ * its first ctx = sparse_ctx[t, h] table tokens, token j in page
+ * sparse_bt[t, h, j / 16] at slot j % 16; and
+ *   out[t, h, g] = sum_j softmax_j(scale * q[t, h, g] . k_j) v_j
+ * with fp32 arithmetic.  A row with an empty context yields zeros; a token
+ * whose page id lies outside [0, num_pages) takes no part.
+ *   q: bf16 [T, H, G, D]; k_cache, v_cache: bf16 [num_pages, 16, H, D]
+ *   (page id = physical 128-token block * 8 + page, as the table writes it);
+ *   all three 16-byte aligned; D in {64, 128, 256}; 1 <= G <=
+ *   BSA_MAX_ATTN_GROUP.  sparse_bt: int32 [T, H, K * 8]; sparse_ctx: int32
+ *   [T, H]; out: fp32 [T, H, G, D].
+ * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_TOPK (K < 1 or > BSA_MAX_TOPK),
+ * BSA_ERR_ALIGN. */
+int bsa_sparse_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                int64_t num_pages, const int32_t* sparse_bt,
+                                const int32_t* sparse_ctx, int64_t T, int64_t H, int64_t G,
+                                int64_t D, int32_t K, float scale, float* out, void* stream);
+
 /* Size of the device scratch array behind bsa_topk_select_noalloc. */
 #define BSA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -234,13 +234,21 @@ def random_block_table(B: int, MB: int, seed: int, device="cpu") -> torch.Tensor
     return torch.randint(0, 1 << 27, (B, MB), generator=g, device=device, dtype=torch.int32)
 
 
-def index_inputs(seed: int, T: int, H: int, D: int, num_phys_blocks: int, device="cpu"):
+def index_inputs(seed: int, T: int, H: int, D: int, num_phys_blocks: int, device="cpu",
+                 integer_valued: bool = False):
     """Index queries bf16 [T, H, D] drawn N(0, 1/D) and pooled index keys bf16
     [num_phys_blocks, D] drawn N(0, 1), so that a block score (a dot product
-    over D) is about N(0, 1) like the score workloads above."""
+    over D) is about N(0, 1) like the score workloads above.  With
+    `integer_valued`, both hold integers in [-3, 3] instead: every product
+    and partial sum is then an integer below 2^24, exact in fp32 whatever
+    the summation order, and equal scores (ties) are common."""
     g = generator(seed, device)
-    q = torch.randn(T, H, D, generator=g, device=device) / (D ** 0.5)
-    k = torch.randn(num_phys_blocks, D, generator=g, device=device)
+    if integer_valued:
+        q = torch.randint(-3, 4, (T, H, D), generator=g, device=device).float()
+        k = torch.randint(-3, 4, (num_phys_blocks, D), generator=g, device=device).float()
+    else:
+        q = torch.randn(T, H, D, generator=g, device=device) / (D ** 0.5)
+        k = torch.randn(num_phys_blocks, D, generator=g, device=device)
     return q.to(torch.bfloat16), k.to(torch.bfloat16)
 
 

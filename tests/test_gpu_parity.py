@@ -591,19 +591,23 @@ def test_host_rejects_bad_arguments(cuda_device):
 
 # ---------------------------------------------------------------- full size
 
-def test_full_size_bench_workload_sampled(cuda_device):
+@pytest.mark.parametrize("K", [16, 64])
+def test_full_size_bench_workload_sampled(cuda_device, K):
     """The benchmark's workload at full size (131072 requests, 2 heads, 1024
-    tiles, topk 16) in the benchmark's launch configuration: every row is
-    checked for the properties any correct answer has, and a random sample of
-    token rows is compared with the oracle element by element."""
-    import bench
+    tiles, topk 16 and 64) in the benchmark's launch configuration: every row
+    is checked for the properties any correct answer has, and a random sample
+    of token rows is compared with the oracle element by element."""
     dev = cuda_device
-
-    class A:
-        requests = 131072
-        topk = 16
-
-    w, nvp, table = bench.build_workload(A, dev, 0)
+    # the benchmark's workload (synth.long_decode with 131072 requests, its
+    # block table) with the -inf tail and the planted block placed by the
+    # oracle's page counts
+    w = synth.long_decode(seed=1003, device=dev, B=131072, H=2, M=1024, K=K,
+                          dtype=torch.bfloat16)
+    nvp_host = oracle.num_valid_pages_decode(w.seq_lens.cpu().numpy(), w.dql)
+    nvp = torch.from_numpy(nvp_host).to(dev)
+    synth.fill_tail(w.scores, nvp, float("-inf"))
+    synth.plant(w.scores, nvp, w.plant_u, w.plant_value)
+    table = synth.random_block_table(w.B, w.M, seed=2003, device=dev)
     idx, bt, ctx = bsa.bsa_topk_select_sparse_table(w.scores, w.seq_lens, w.dql, w.K,
                                                     w.num_init, w.num_local, table)
     torch.cuda.synchronize()
@@ -619,6 +623,9 @@ def test_full_size_bench_workload_sampled(cuda_device):
     assert bool((idx[:, :, 0] == 0).all())                     # init block
     assert bool((idx[:, :, K - 1] == v[:, :, 0] - 1).all())    # local blocks
     assert bool((idx[:, :, K - 2] == v[:, :, 0] - 2).all())
+    # every row: a valid selection, including the exchange property
+    from tests import _props
+    _props.check_selection(w.scores, nvp, idx, K, w.num_init, w.num_local)
     # sampled rows against the oracle
     g = torch.Generator().manual_seed(11)
     rows = torch.randperm(w.T, generator=g)[:3000].sort().values
