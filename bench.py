@@ -54,7 +54,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true")
     p.add_argument("--no-extra", action="store_true",
-                   help="skip the topk-64 and index-score measurements")
+                   help="skip the topk-64, index-score and attention measurements")
+    p.add_argument("--extras-only", choices=["index_score", "attention"], default=None,
+                   help="time only this call and print its record (for profiling)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
 
@@ -365,6 +367,7 @@ def run_ours(args):
         result["topk64_fused"] = extra_topk
     if rank == 0 and not args.no_extra and world == 1:
         result["index_score_select"] = index_score_step(device, args)
+        result["sparse_decode_attention"] = attention_step(device, args)
     if rank == 0 and not args.no_configs and world == 1:
         result["per_config_latency_us"] = config_latencies(device)
     if rank == 0:
@@ -465,6 +468,49 @@ def index_score_step(device, args):
     return {"kernel": "index_score_select_kernel", "workload":
             f"{B} requests x dql {dql}, H={H}, D={D}, max_k_tiles={M}, topk={K}, "
             "seq_len U[16384,131072], paged bf16 keys",
+            "kernel_ms": ms, "rows_per_s": B * dql * H / (ms / 1e3),
+            "algorithmic_bytes_per_launch": byt, "achieved_gbs": achieved, "peak_gbs": peak,
+            "frac": achieved / peak, "peak_source": src}
+
+
+def attention_bytes(ctx, H, G, D, K):
+    """Bytes the sparse decode attention must move: each row's key and value
+    rows for its ctx tokens, its table entries, ctx, queries and output."""
+    rows = ctx.size
+    return (int(ctx.sum()) * D * 2 * 2 + rows * (K * 8 * 4 + 4) + rows * G * D * (2 + 4))
+
+
+def attention_step(device, args):
+    """Sparse decode attention over the tables of the fused-table workload
+    shape: 128 requests x query length 4, 1 index head, topk 16, seq_len
+    U[1, 65536] with ~5% padded, 4 query heads of dim 64 per KV head, a
+    page-16 bf16 KV cache of 524288 pages (1 GB each for keys and values; the
+    rows read about 260 MB of it per launch, more than L2 holds)."""
+    import block_sparse_attention_topk_gb300 as bsa
+    import synth
+    B, dql, H, G, D, M, K = 128, 4, 1, 4, 64, 512, 16
+    w = synth.fused_table(seed=1005, device=device, B=B, dql=dql, H=H, M=M, K=K)
+    nvp = bsa.bsa_num_valid_pages_decode(w.seq_lens, dql)
+    synth.fill_tail(w.scores, nvp, float("-inf"))
+    _, bt, ctx = bsa.bsa_topk_select_sparse_table(w.scores, w.seq_lens, dql, K, 1, 1,
+                                                  w.block_table, want_idx=False)
+    num_pages = B * M * 8
+    q = synth.normal_scores((B * dql, H, G, D), torch.bfloat16, seed=31, device=device)
+    kc = synth.normal_scores((num_pages, 16, H, D), torch.bfloat16, seed=32, device=device)
+    vc = synth.normal_scores((num_pages, 16, H, D), torch.bfloat16, seed=33, device=device)
+    out = torch.empty((B * dql, H, G, D), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fn():
+        bsa.bsa_sparse_decode_attention(q, kc, vc, bt, ctx, out=out)
+
+    ms = timed_launches(fn, stream, 10, args.warmup)
+    byt = attention_bytes(ctx.cpu().numpy(), H, G, D, K)
+    peak, src = read_peaks()
+    achieved = byt / (ms / 1e3) / 1e9
+    return {"kernel": "sparse_decode_attention_kernel", "workload":
+            f"{B} requests x dql {dql}, H={H}, G={G}, D={D}, topk={K}, seq_len U[1,65536], "
+            "tables from the fused select",
             "kernel_ms": ms, "rows_per_s": B * dql * H / (ms / 1e3),
             "algorithmic_bytes_per_launch": byt, "achieved_gbs": achieved, "peak_gbs": peak,
             "frac": achieved / peak, "peak_source": src}
@@ -696,9 +742,20 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_extras_only(args):
+    import block_sparse_attention_topk_gb300 as bsa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    bsa.lib()
+    fn = index_score_step if args.extras_only == "index_score" else attention_step
+    print(json.dumps({args.extras_only: fn(device, args)}), flush=True)
+
+
 if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.extras_only:
+        run_extras_only(a)
     else:
         run_ours(a)

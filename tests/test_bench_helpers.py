@@ -71,3 +71,16 @@ def test_index_score_bytes_hand_example():
     keys = 3 * 8 * 2                  # 3 usable keys of D bf16
     scores = (0 + 2 + 2) * 2 * 4      # causal entries x heads x fp32
     assert b == q + table + keys + scores + 3 * 4 + 3 * 2 * 3 * 4
+
+
+def test_attention_bytes_hand_example():
+    """Sparse attention bytes: key and value rows of every context token,
+    table entries and ctx, queries in and outputs out."""
+    sys.path.insert(0, ROOT)
+    import bench
+    ctx = np.array([[0], [100]], dtype=np.int32)        # 2 rows, H = 1
+    b = bench.attention_bytes(ctx, 1, 2, 64, 4)
+    kv = 100 * 64 * 2 * 2
+    table = 2 * (4 * 8 * 4 + 4)
+    qo = 2 * 2 * 64 * (2 + 4)
+    assert b == kv + table + qo
