@@ -415,10 +415,12 @@ def topk_step(w, table, nvp_host, K, device, stream, args):
     pol = bsa.bsa_select_policy(w.T * w.H, w.M, K, bsa.BSA_DTYPE_BF16,
                                 torch.cuda.get_device_properties(device).multi_processor_count)
     achieved = byt / (ms / 1e3) / 1e9
+    traffic = read_traffic(f"fused_topk{K}", KERNEL_OF_PATH[pol["path"]], K, w.B)
     return {"kernel": dominant_kernel(pol["path"], True), "topk": K, "kernel_ms": ms,
             "rows_per_s": w.T * w.H / (ms / 1e3), "algorithmic_bytes_per_launch": byt,
             "achieved_gbs": achieved, "peak_gbs": peak, "frac": achieved / peak,
-            "peak_source": src}
+            "peak_source": src,
+            "traffic": None if traffic is None else traffic["dram_bytes_per_launch"]}
 
 
 def index_score_bytes(seq, dql, H, D, M, K, valid_blocks):

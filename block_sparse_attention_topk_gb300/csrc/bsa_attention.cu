@@ -16,19 +16,24 @@
 // A row with an empty context yields zeros, and a token whose page id lies
 // outside [0, num_pages) takes no part.
 //
-// How: one warp per row (t, h) and all its G query heads.  The row's queries
-// sit in shared memory as fp32.  The context is walked 32 tokens (two pages)
-// at a time: each lane scores one token against every query head (reading
-// the token's key row as 16-byte vectors), the warp folds the tile into a
-// running maximum and sum per head (online softmax, Milakov and Gimelshein,
-// "Online normalizer calculation for softmax", 2018), and then the lanes,
-// each owning D / 32 output dimensions, accumulate the tile's value rows
-// (one coalesced row per token) weighted by the broadcast probabilities.
-// Decode attention moves each key and value once and does O(G) flops per
-// element, so it is bound by memory and runs on the CUDA cores.
+// How: one CTA of 8 warps per row (t, h) and all its G query heads; the
+// warps split the row's context.  The row's queries sit in shared memory as
+// fp32.  Each warp walks its share 32 tokens (two pages) at a time: each
+// lane scores one token against every query head (reading the token's key
+// row as 16-byte vectors), the warp folds the tile into a running maximum
+// and sum per head (online softmax, Milakov and Gimelshein, "Online
+// normalizer calculation for softmax", 2018), and then the lanes, each
+// owning D / 32 output dimensions, accumulate the tile's value rows (one
+// coalesced row per token) weighted by the broadcast probabilities.  The
+// warps' partial maxima, sums and outputs then merge in shared memory (each
+// rescaled by exp(its maximum - the overall maximum)).  Decode attention
+// moves each key and value once and does O(G) flops per element, so it is
+// bound by memory and runs on the CUDA cores.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <climits>
 
 #include "bsa_internal.h"
 
@@ -36,7 +41,7 @@ namespace bsa {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kAttnWarps = 4;
+constexpr int kAttnWarps = 8;   // warps sharing one row's context
 
 struct AttnParams {
     const uint16_t* q;       // bf16 [rows, G, D]
@@ -90,24 +95,30 @@ __device__ __forceinline__ void load_dl(const uint16_t* p, float (&f)[DL]) {
 }
 
 // GP >= G query heads (a power of two), DL = D / 32 dimensions per lane.
+// Shared memory: queries [GP][D], then per warp its partial maxima [GP],
+// sums [GP] and outputs [GP][D].
 template <int GP, int DL>
 __global__ void __launch_bounds__(kAttnWarps * 32)
 sparse_decode_attention_kernel(const AttnParams A) {
     constexpr int D = 32 * DL;
-    extern __shared__ __align__(16) float qs_all[];   // [warps][GP][D]
+    extern __shared__ __align__(16) float smem[];
+    float* qs = smem;
+    float* pm = qs + GP * D;
+    float* pl = pm + kAttnWarps * GP;
+    float* pacc = pl + kAttnWarps * GP;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    float* qs = qs_all + (size_t)warp * GP * D;
     const int G = A.G;
     const int cap = A.width * BSA_SUB_PAGE_SIZE;
-    for (int64_t row = (int64_t)blockIdx.x * kAttnWarps + warp; row < A.rows;
-         row += (int64_t)gridDim.x * kAttnWarps) {
+    for (int64_t row = blockIdx.x; row < A.rows; row += gridDim.x) {
         const int h = (int)(row % A.H);
         const int32_t* bt = A.bt + row * A.width;
         const int ctx = max(0, min(__ldg(A.ctx + row), cap));
         const uint16_t* qrow = A.q + row * (int64_t)G * D;
-        for (int i = lane; i < G * D; i += 32) qs[i] = __uint_as_float((uint32_t)__ldg(qrow + i) << 16);
-        __syncwarp();
+        __syncthreads();   // the previous row's readers of shared memory are done
+        for (int i = threadIdx.x; i < G * D; i += kAttnWarps * 32)
+            qs[i] = __uint_as_float((uint32_t)__ldg(qrow + i) << 16);
+        __syncthreads();
         float m[GP], l[GP], acc[GP][DL];
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
@@ -116,7 +127,7 @@ sparse_decode_attention_kernel(const AttnParams A) {
 #pragma unroll
             for (int d = 0; d < DL; ++d) acc[g][d] = 0.f;
         }
-        for (int tile = 0; tile < ctx; tile += 32) {
+        for (int tile = 32 * warp; tile < ctx; tile += 32 * kAttnWarps) {
             // ---- scores: lane j of the tile takes token tile + j ----
             const int j = tile + lane;
             const int32_t page = j < ctx ? __ldg(bt + (j >> 4)) : -1;
@@ -127,7 +138,7 @@ sparse_decode_attention_kernel(const AttnParams A) {
             if (ok) {
                 const uint4* kr = reinterpret_cast<const uint4*>(
                     A.k + (((int64_t)page * BSA_SUB_PAGE_SIZE + (j & 15)) * A.H + h) * D);
-#pragma unroll 4
+#pragma unroll 8
                 for (int c = 0; c < D / 8; ++c) {
                     const uint4 kv = __ldg(kr + c);
                     const float kf[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
@@ -165,44 +176,84 @@ sparse_decode_attention_kernel(const AttnParams A) {
                 for (int d = 0; d < DL; ++d) acc[g][d] *= corr;
                 m[g] = mn;
             }
-            // ---- values: the lane owns dimensions [lane * DL, lane * DL + DL) ----
+            // ---- values: the lane owns dimensions [lane * DL, lane * DL + DL);
+            // VB value rows are loaded before any of them is used ----
+            constexpr int VB = DL >= 8 ? 2 : 16 / DL;
             const int nt = min(32, ctx - tile);
-            for (int jj = 0; jj < nt; ++jj) {
-                const int jt = tile + jj;
-                const int32_t pg = __ldg(bt + (jt >> 4));
-                if (pg < 0 || pg >= A.num_pages) continue;   // the same for every lane
-                float vf[DL];
-                load_dl<DL>(A.v + (((int64_t)pg * BSA_SUB_PAGE_SIZE + (jt & 15)) * A.H + h) * D +
-                                lane * DL,
-                            vf);
+            for (int j0 = 0; j0 < nt; j0 += VB) {
+                float vf[VB][DL];
 #pragma unroll
-                for (int g = 0; g < GP; ++g) {
-                    const float pj = __shfl_sync(kFull, p[g], jj);
+                for (int u = 0; u < VB; ++u) {
+                    const int jt = tile + j0 + u;
+                    const int32_t pg = j0 + u < nt ? __ldg(bt + (jt >> 4)) : -1;
+                    if (pg >= 0 && pg < A.num_pages) {
+                        load_dl<DL>(A.v + (((int64_t)pg * BSA_SUB_PAGE_SIZE + (jt & 15)) * A.H + h) * D +
+                                        lane * DL,
+                                    vf[u]);
+                    } else {
 #pragma unroll
-                    for (int d = 0; d < DL; ++d) acc[g][d] = fmaf(pj, vf[d], acc[g][d]);
+                        for (int d = 0; d < DL; ++d) vf[u][d] = 0.f;
+                    }
+                }
+                // tokens past the context or on unusable pages have p = 0
+#pragma unroll
+                for (int u = 0; u < VB; ++u) {
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        const float pj = __shfl_sync(kFull, p[g], (j0 + u) & 31);
+#pragma unroll
+                        for (int d = 0; d < DL; ++d) acc[g][d] = fmaf(pj, vf[u][d], acc[g][d]);
+                    }
                 }
             }
         }
-        float* orow = A.out + row * (int64_t)G * D;
+        // ---- merge the warps' partial results ----
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-            if (g < G) {
-                const float inv = l[g] > 0.f ? 1.f / l[g] : 0.f;
-#pragma unroll
-                for (int d = 0; d < DL; ++d) orow[g * D + lane * DL + d] = acc[g][d] * inv;
+            if (lane == 0) {
+                pm[warp * GP + g] = m[g];
+                pl[warp * GP + g] = l[g];
             }
+#pragma unroll
+            for (int d = 0; d < DL; ++d) pacc[(warp * GP + g) * D + lane * DL + d] = acc[g][d];
         }
-        __syncwarp();
+        __syncthreads();
+        float* orow = A.out + row * (int64_t)G * D;
+        for (int i = threadIdx.x; i < G * D; i += kAttnWarps * 32) {
+            const int g = i / D;
+            const int d = i - g * D;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) mx = fmaxf(mx, pm[w * GP + g]);
+            float den = 0.f, num = 0.f;
+            if (mx != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kAttnWarps; ++w) {
+                    const float mw = pm[w * GP + g];
+                    const float e = mw == -INFINITY ? 0.f : expf(mw - mx);
+                    den = fmaf(pl[w * GP + g], e, den);
+                    num = fmaf(pacc[(w * GP + g) * D + d], e, num);
+                }
+            }
+            orow[i] = den > 0.f ? num / den : 0.f;
+        }
     }
 }
 
 template <int GP, int DL>
 cudaError_t launch_attn(const AttnParams& A, cudaStream_t st) {
-    const size_t smem = (size_t)kAttnWarps * GP * 32 * DL * sizeof(float);
-    int64_t grid = (A.rows + kAttnWarps - 1) / kAttnWarps;
-    const int64_t cap = (int64_t)device_sm_count() * 16;
-    if (grid > cap) grid = cap;
-    sparse_decode_attention_kernel<GP, DL><<<(int)grid, kAttnWarps * 32, smem, st>>>(A);
+    const size_t D = 32 * DL;
+    const size_t smem = (GP * D + 2 * kAttnWarps * GP + (size_t)kAttnWarps * GP * D) * sizeof(float);
+    auto kern = sparse_decode_attention_kernel<GP, DL>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    // one row per CTA, not capped at the resident CTAs
+    int64_t grid = A.rows;
+    if (grid > INT32_MAX) grid = INT32_MAX;
+    kern<<<(int)grid, kAttnWarps * 32, smem, st>>>(A);
     return cudaGetLastError();
 }
 

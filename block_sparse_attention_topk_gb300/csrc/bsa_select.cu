@@ -2492,15 +2492,17 @@ cudaError_t launch_dt(const KernelParams& P, const bsa_launch_policy_t& pol, cud
 //     score[t, h, b] = sum over d of q[t, h, d] * k[block_table[req, b], d]
 // accumulated in fp32 and no scale factor (item 6 removed sm_scale).
 //
-// One CTA per request: its dql * H query rows are staged in shared memory as
-// fp32, each thread scores one causal block at a time against all of them
-// (the block's key row is read once, as 16-byte vectors, and shared by every
-// query row of the request), writes the scores of the causal blocks into the
-// caller's unified buffer, and after a block barrier the CTA's warps select
-// the top-k of its rows from that buffer with the warp path, reading through
-// L2 what the CTA has just written (no second launch and no re-read from
-// HBM).  A causal block whose table entry is missing (b >= max_blocks) or
-// out of range scores -inf.
+// A CTA takes a group of R requests at a time, R = max(1, 8 / (dql * H)), so
+// that its 8 warps have rows to select: the group's query rows are staged in
+// shared memory as fp32, each thread scores one causal block of a request at
+// a time against all of that request's query rows (the block's key row is
+// read once, as 16-byte vectors, and shared by every query row of the
+// request), writes the scores of the causal blocks into the caller's unified
+// buffer, and after a block barrier the CTA's warps select the top-k of the
+// group's rows from that buffer with the warp path, reading through L2 what
+// the CTA has just written (no second launch and no re-read from HBM).  A
+// causal block whose table entry is missing (b >= max_blocks) or out of
+// range scores -inf.
 // ===========================================================================
 constexpr int kScoreThreads = 256;
 constexpr int kScoreWarps = kScoreThreads / 32;
@@ -2512,6 +2514,7 @@ struct ScoreParams {
     int64_t nb;
     int32_t D;
     int32_t nq;              // dql * H query rows per request
+    int32_t group;           // requests a CTA takes at a time
     float* scores;           // element (t, h, b) at t * token_stride + h * head_stride + b
 };
 
@@ -2527,74 +2530,85 @@ __global__ void __launch_bounds__(kScoreThreads, 2) index_score_select_kernel(co
     const int warp = tid >> 5;
     const int D = S.D;
     const int nq = S.nq;
-    float* qs = reinterpret_cast<float*>(smem_raw);                       // [nq][D]
-    const size_t qbytes = ((size_t)nq * D * 4 + 15) & ~(size_t)15;
+    const int R = S.group;
+    float* qs = reinterpret_cast<float*>(smem_raw);                       // [R * nq][D]
+    const size_t qbytes = ((size_t)R * nq * D * 4 + 15) & ~(size_t)15;
     uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem_raw + qbytes) + (size_t)warp * S.P.cap * 2;
     int32_t* s_ids = reinterpret_cast<int32_t*>(s_keys + S.P.cap);
     const int64_t B = a.T / a.dql;
-    for (int64_t req = blockIdx.x; req < B; req += gridDim.x) {
-        const int64_t seq = __ldg(a.seq_lens + req);
-        // the last query row (local_q = dql - 1, position seq - 1) has the
-        // most causal blocks
-        int64_t vmax = seq > 0 ? (seq + kPageSize - 1) >> kLogPageSize : 0;
-        if (vmax > a.M) vmax = a.M;
-        __syncthreads();   // the previous request's readers of qs are done
-        const uint16_t* qsrc = S.q + req * (int64_t)nq * D;
-        for (int i = tid; i < nq * D; i += kScoreThreads) qs[i] = __uint_as_float((uint32_t)qsrc[i] << 16);
+    const int64_t ngroups = (B + R - 1) / R;
+    for (int64_t grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
+        const int64_t req0 = grp * R;
+        const int nreq = (int)min((int64_t)R, B - req0);
+        __syncthreads();   // the previous group's readers of qs are done
+        // the group's query rows are contiguous: rows (req0 * dql + lq) * H + h
+        const uint16_t* qsrc = S.q + req0 * (int64_t)nq * D;
+        for (int i = tid; i < nreq * nq * D; i += kScoreThreads)
+            qs[i] = __uint_as_float((uint32_t)qsrc[i] << 16);
         __syncthreads();
-        const int32_t* table = a.block_table + req * a.max_blocks;
-        for (int64_t b = tid; b < vmax; b += kScoreThreads) {
-            float acc[NQ];
+        for (int rr = 0; rr < nreq; ++rr) {
+            const int64_t req = req0 + rr;
+            const float* qr = qs + (size_t)rr * nq * D;
+            const int64_t seq = __ldg(a.seq_lens + req);
+            // the last query row (local_q = dql - 1, position seq - 1) has the
+            // most causal blocks
+            int64_t vmax = seq > 0 ? (seq + kPageSize - 1) >> kLogPageSize : 0;
+            if (vmax > a.M) vmax = a.M;
+            const int32_t* table = a.block_table + req * a.max_blocks;
+            for (int64_t b = tid; b < vmax; b += kScoreThreads) {
+                float acc[NQ];
 #pragma unroll
-            for (int x = 0; x < NQ; ++x) acc[x] = 0.f;
-            const int64_t phys = b < a.max_blocks ? (int64_t)__ldg(table + b) : -1;
-            const bool ok = phys >= 0 && phys < S.nb;
-            if (ok) {
-                const uint4* kr = reinterpret_cast<const uint4*>(S.k + phys * D);
-#pragma unroll 4
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint4 kv = __ldg(kr + c);
-                    const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
-                                         bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
+                for (int x = 0; x < NQ; ++x) acc[x] = 0.f;
+                const int64_t phys = b < a.max_blocks ? (int64_t)__ldg(table + b) : -1;
+                const bool ok = phys >= 0 && phys < S.nb;
+                if (ok) {
+                    const uint4* kr = reinterpret_cast<const uint4*>(S.k + phys * D);
+#pragma unroll 8
+                    for (int c = 0; c < D / 8; ++c) {
+                        const uint4 kv = __ldg(kr + c);
+                        const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y),
+                                             bf16_hi(kv.y), bf16_lo(kv.z), bf16_hi(kv.z),
+                                             bf16_lo(kv.w), bf16_hi(kv.w)};
 #pragma unroll
-                    for (int x = 0; x < NQ; ++x) {
-                        if (x < nq) {
-                            const float4* qv = reinterpret_cast<const float4*>(qs + x * D + 8 * c);
-                            const float4 q0 = qv[0], q1 = qv[1];
-                            float s = acc[x];
-                            s = fmaf(kf[0], q0.x, s);
-                            s = fmaf(kf[1], q0.y, s);
-                            s = fmaf(kf[2], q0.z, s);
-                            s = fmaf(kf[3], q0.w, s);
-                            s = fmaf(kf[4], q1.x, s);
-                            s = fmaf(kf[5], q1.y, s);
-                            s = fmaf(kf[6], q1.z, s);
-                            s = fmaf(kf[7], q1.w, s);
-                            acc[x] = s;
+                        for (int x = 0; x < NQ; ++x) {
+                            if (x < nq) {
+                                const float4* qv = reinterpret_cast<const float4*>(qr + x * D + 8 * c);
+                                const float4 q0 = qv[0], q1 = qv[1];
+                                float sc = acc[x];
+                                sc = fmaf(kf[0], q0.x, sc);
+                                sc = fmaf(kf[1], q0.y, sc);
+                                sc = fmaf(kf[2], q0.z, sc);
+                                sc = fmaf(kf[3], q0.w, sc);
+                                sc = fmaf(kf[4], q1.x, sc);
+                                sc = fmaf(kf[5], q1.y, sc);
+                                sc = fmaf(kf[6], q1.z, sc);
+                                sc = fmaf(kf[7], q1.w, sc);
+                                acc[x] = sc;
+                            }
+                        }
+                    }
+                }
+                // rows whose causal count covers b get its score
+#pragma unroll
+                for (int x = 0; x < NQ; ++x) {
+                    if (x < nq) {
+                        const int lq = x / (int)a.H;
+                        const int h = x - lq * (int)a.H;
+                        const int64_t len = seq - a.dql + lq + 1;   // causal length of the row
+                        int64_t v = len > 0 ? (len + kPageSize - 1) >> kLogPageSize : 0;
+                        if (v > a.M) v = a.M;
+                        if (b < v) {
+                            const int64_t t = req * a.dql + lq;
+                            S.scores[t * a.token_stride + h * a.head_stride + b] =
+                                ok ? acc[x] : __int_as_float(0xFF800000);
                         }
                     }
                 }
             }
-            // rows whose causal count covers b get its score
-#pragma unroll
-            for (int x = 0; x < NQ; ++x) {
-                if (x < nq) {
-                    const int lq = x / (int)a.H;
-                    const int h = x - lq * (int)a.H;
-                    const int64_t len = seq - a.dql + lq + 1;   // causal length of the row
-                    int64_t v = len > 0 ? (len + kPageSize - 1) >> kLogPageSize : 0;
-                    if (v > a.M) v = a.M;
-                    if (b < v) {
-                        const int64_t t = req * a.dql + lq;
-                        S.scores[t * a.token_stride + h * a.head_stride + b] =
-                            ok ? acc[x] : __int_as_float(0xFF800000);
-                    }
-                }
-            }
         }
-        __syncthreads();   // the request's scores are visible to the whole CTA
-        for (int x = warp; x < nq; x += kScoreWarps) {
-            warp_item<false, 4, 2, true>(S.P, req * nq + x, 0, s_keys, s_ids, lane);
+        __syncthreads();   // the group's scores are visible to the whole CTA
+        for (int x = warp; x < nreq * nq; x += kScoreWarps) {
+            warp_item<false, 4, 2, true>(S.P, req0 * nq + x, 0, s_keys, s_ids, lane);
             __syncwarp();
         }
     }
@@ -2670,13 +2684,15 @@ cudaError_t launch_index_score_select(const SelectArgs& a, const uint16_t* q, co
     S.nb = nb;
     S.D = D;
     S.nq = (int32_t)(a.dql * a.H);
+    S.group = S.nq >= kScoreWarps ? 1 : kScoreWarps / S.nq;
     S.scores = scores;
     const int64_t B = a.T / a.dql;
     if (B == 0) return cudaSuccess;
-    const size_t smem = (((size_t)S.nq * D * 4 + 15) & ~(size_t)15) +
+    const size_t smem = (((size_t)S.group * S.nq * D * 4 + 15) & ~(size_t)15) +
                         (size_t)kScoreWarps * P.cap * 8;
+    const int64_t ngroups = (B + S.group - 1) / S.group;
     int64_t grid = (int64_t)device_sm_count() * 4;
-    if (grid > B) grid = B;
+    if (grid > ngroups) grid = ngroups;
     if (S.nq <= 1) return launch_score_nq<1>(S, (int)grid, smem, stream);
     if (S.nq <= 2) return launch_score_nq<2>(S, (int)grid, smem, stream);
     if (S.nq <= 4) return launch_score_nq<4>(S, (int)grid, smem, stream);
