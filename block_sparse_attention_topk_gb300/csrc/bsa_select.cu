@@ -1958,11 +1958,12 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
 // K' > 32.  Here the 8 lanes of a row:
 //  1. stream its non-forced range in 32-byte chunks (256 contiguous bytes per
 //     row per step) and keep, for each of the 16 element positions of a
-//     chunk, the largest key seen there: 16 representatives per lane and 128
-//     per row, each the maximum of distinct elements.  Interior chunks are
+//     chunk, the largest key seen there: 16 representatives per lane and up
+//     to 128 per row, each the maximum of distinct elements.  Chunks are
 //     reduced on raw bits (a raw maximum and minimum per position, turned
-//     into the key maximum once at the end); the two edge chunks are masked
-//     and reduced on keys.
+//     into the key maximum once at the end).  The two edge chunks are left
+//     out: a row that needs a threshold has at least 9 chunks, so lanes 1-7
+//     hold interior ones and each quad keeps at least 32 representatives.
 //  2. theta: each quad of lanes (64 representatives) finds its 32nd largest
 //     representative with packed 16-bit bitonic networks (each lane sorts its
 //     16, lane pairs merge into a sorted 32, the top 32 of the quad's two
@@ -2101,12 +2102,6 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
                     rmx[x] = 0x80008000u;
                     rmn[x] = 0x7FFF7FFFu;
                 }
-                auto take_edge = [&](int k) {
-                    uint32_t w[8];
-                    pair_load_edge<true>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) rp[x] = max_s16x2(rp[x], w[x]);
-                };
                 auto fold = [&](const uint32_t (&w)[8]) {
 #pragma unroll
                     for (int x = 0; x < 8; ++x) {
@@ -2114,10 +2109,8 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
                         rmn[x] = min_s16x2(rmn[x], w[x]);
                     }
                 };
-                if (q == 0) take_edge(0);
-                if ((nchunk - 1) % kOctLanes == q) take_edge(nchunk - 1);
-                // interior chunks k = q + 8 i, 1 <= k <= nchunk - 2, up to four
-                // loads in flight
+                // interior chunks k = q + 8 i, 1 <= k <= nchunk - 2, two loads
+                // in flight; the edge chunks (0 and nchunk - 1) are left out
                 const int klast = nchunk - 2;
                 int k = q == 0 ? kOctLanes : q;
                 const bool any_interior = k <= klast;
@@ -2150,22 +2143,21 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
                 int32_t ra[8], rb[8];
 #pragma unroll
                 for (int x = 0; x < 8; ++x) ra[x] = rb[x] = INT32_MIN;
-                auto load_keys = [&](int k, uint32_t (&w)[8]) {
-                    if (k == 0 || k == nchunk - 1) {
-                        pair_load_edge<false>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
-                    } else {
-                        ld32(c0 + ((uintptr_t)k << 5), w);
-                        chunk_to_keys<false>(w);
-                    }
-                };
+                // interior chunks only, as for bf16
                 for (int k = q; k < nchunk; k += 2 * kOctLanes) {
                     uint32_t w0[8], w1[8];
-                    const bool two = k + kOctLanes < nchunk;
-                    load_keys(k, w0);
-                    if (two) load_keys(k + kOctLanes, w1);
+                    const bool one = k != 0 && k != nchunk - 1;
+                    const int k1 = k + kOctLanes;
+                    const bool two = k1 < nchunk - 1;
+                    if (one) ld32(c0 + ((uintptr_t)k << 5), w0);
+                    if (two) ld32(c0 + ((uintptr_t)k1 << 5), w1);
+                    if (one) {
+                        chunk_to_keys<false>(w0);
 #pragma unroll
-                    for (int x = 0; x < 8; ++x) ra[x] = max(ra[x], (int32_t)w0[x]);
+                        for (int x = 0; x < 8; ++x) ra[x] = max(ra[x], (int32_t)w0[x]);
+                    }
                     if (two) {
+                        chunk_to_keys<false>(w1);
 #pragma unroll
                         for (int x = 0; x < 8; ++x) rb[x] = max(rb[x], (int32_t)w1[x]);
                     }
@@ -2188,11 +2180,17 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
         const int steps = __reduce_max_sync(kFull, (unsigned)my_steps);
         const bool raw_ok = theta >= 0;   // raw signed order is key order against it
         int cbase = 0;
-        // the next step's interior chunk is loaded while this one is processed
+        // the next step's chunk is loaded while this one is processed; an
+        // edge chunk is loaded whole when it lies inside the score buffer (its
+        // ids outside [lo, hi) are cut by the range mask below)
         uint32_t nx[8];
+        auto plain = [&](int k) {
+            const uintptr_t addr = c0 + ((uintptr_t)k << 5);
+            return (k != 0 && k != nchunk - 1) || (addr >= P.buf_lo && addr + 32 <= P.buf_hi);
+        };
         auto issue = [&](int st) {
             const int k = q + kOctLanes * st;
-            if (k < nchunk && k != 0 && k != nchunk - 1) ld32(c0 + ((uintptr_t)k << 5), nx);
+            if (k < nchunk && plain(k)) ld32(c0 + ((uintptr_t)k << 5), nx);
         };
         issue(0);
         for (int st = 0; st < steps; ++st) {
@@ -2201,8 +2199,8 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
             uint32_t w[8];
             uint32_t m = 0;
             if (has) {
-                const bool edge = k == 0 || k == nchunk - 1;
-                if (edge) {
+                if (!plain(k)) {
+                    // masked keys, which compare like raw bits against theta >= 0
                     pair_load_edge<BF16>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
                 } else {
 #pragma unroll
