@@ -2490,20 +2490,32 @@ cudaError_t launch_dt(const KernelParams& P, const bsa_launch_policy_t& pol, cud
 //     score[t, h, b] = sum over d of q[t, h, d] * k[block_table[req, b], d]
 // accumulated in fp32 and no scale factor (item 6 removed sm_scale).
 //
-// A CTA takes a group of R requests at a time, R = max(1, 8 / (dql * H)), so
-// that its 8 warps have rows to select: the group's query rows are staged in
-// shared memory as fp32, each thread scores one causal block of a request at
-// a time against all of that request's query rows (the block's key row is
-// read once, as 16-byte vectors, and shared by every query row of the
-// request), writes the scores of the causal blocks into the caller's unified
-// buffer, and after a block barrier the CTA's warps select the top-k of the
-// group's rows from that buffer with the warp path, reading through L2 what
-// the CTA has just written (no second launch and no re-read from HBM).  A
-// causal block whose table entry is missing (b >= max_blocks) or out of
-// range scores -inf.
+// A CTA of 4 warps takes a group of R requests at a time, R = max(1, 8 /
+// (dql * H)), so that each warp has about two rows to select.  The group's
+// query rows are staged in shared memory as fp32 and the causal blocks are
+// scored in one of two ways:
+//  * segment scoring (D = 64 or 128 and at most 4 query rows per request):
+//    a segment of D / 8 lanes reads one key row with one 16-byte load per
+//    lane, so that a warp-wide load covers whole rows (two of D = 128, four
+//    of D = 64) and a warp keeps 32 rows in flight.  Each lane holds its 8
+//    dimensions of every query row in registers and forms 8-term partial dot
+//    products for the segment's D / 8 rows; a reduce-scatter over the
+//    segment's lanes (recursive halving with shuffles) leaves each lane with
+//    the full dot products of one row.  The warps of the CTA take 32-block
+//    rounds of the group's requests in turn.
+//  * thread scoring (every other D and query count): a thread takes one
+//    causal block at a time, reads its key row as 16-byte vectors and scores
+//    it against every query row of the request.
+// The scores of the causal blocks go into the caller's unified buffer, and
+// after a block barrier the CTA's warps select the top-k of the group's rows
+// from that buffer with the warp path, reading through L2 what the CTA has
+// just written (no second launch and no re-read from HBM).  A causal block
+// whose table entry is missing (b >= max_blocks) or out of range scores -inf.
 // ===========================================================================
-constexpr int kScoreThreads = 256;
+constexpr int kScoreThreads = 128;
 constexpr int kScoreWarps = kScoreThreads / 32;
+constexpr int kScoreRows = 8;        // query rows per group when dql * H is small
+constexpr int kSegMaxQ = 4;          // segment scoring takes up to 4 query rows per request
 
 struct ScoreParams {
     KernelParams P;          // the selection over the score buffer (fp32, decode rows)
@@ -2519,16 +2531,175 @@ struct ScoreParams {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-template <int NQ>
-__global__ void __launch_bounds__(kScoreThreads, 2) index_score_select_kernel(const ScoreParams S) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+__device__ __forceinline__ int64_t causal_blocks_of(int64_t len, int64_t M) {
+    int64_t v = len > 0 ? (len + kPageSize - 1) >> kLogPageSize : 0;
+    return v < M ? v : M;
+}
+
+// Writes block b's score for query row x of request req if b is below that
+// row's causal count.
+__device__ __forceinline__ void store_score(const ScoreParams& S, int64_t req, int64_t seq, int x,
+                                            int64_t b, float val) {
     const SelectArgs& a = S.P.a;
+    const int lq = x / (int)a.H;
+    const int h = x - lq * (int)a.H;
+    if (b < causal_blocks_of(seq - a.dql + lq + 1, a.M)) {
+        const int64_t t = req * a.dql + lq;
+        S.scores[t * a.token_stride + h * a.head_stride + b] = val;
+    }
+}
+
+__device__ __forceinline__ float dot8(const float (&kf)[8], const float (&qv)[8], float acc) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc = fmaf(kf[e], qv[e], acc);
+    return acc;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& kv, float (&kf)[8]) {
+    kf[0] = bf16_lo(kv.x); kf[1] = bf16_hi(kv.x); kf[2] = bf16_lo(kv.y); kf[3] = bf16_hi(kv.y);
+    kf[4] = bf16_lo(kv.z); kf[5] = bf16_hi(kv.z); kf[6] = bf16_lo(kv.w); kf[7] = bf16_hi(kv.w);
+}
+
+// Thread scoring of the group's requests (any D that is a multiple of 8).
+template <int NQ>
+__device__ __forceinline__ void score_group_threads(const ScoreParams& S, int64_t req0, int nreq,
+                                                    const float* qs, int tid) {
+    const SelectArgs& a = S.P.a;
+    const int D = S.D;
+    const int nq = S.nq;
+    for (int rr = 0; rr < nreq; ++rr) {
+        const int64_t req = req0 + rr;
+        const float* qr = qs + (size_t)rr * nq * D;
+        const int64_t seq = __ldg(a.seq_lens + req);
+        // the last query row (local_q = dql - 1, position seq - 1) has the
+        // most causal blocks
+        const int64_t vmax = causal_blocks_of(seq, a.M);
+        const int32_t* table = a.block_table + req * a.max_blocks;
+        for (int64_t b = tid; b < vmax; b += kScoreThreads) {
+            float acc[NQ];
+#pragma unroll
+            for (int x = 0; x < NQ; ++x) acc[x] = 0.f;
+            const int64_t phys = b < a.max_blocks ? (int64_t)__ldg(table + b) : -1;
+            const bool ok = phys >= 0 && phys < S.nb;
+            if (ok) {
+                const uint4* kr = reinterpret_cast<const uint4*>(S.k + phys * D);
+#pragma unroll 8
+                for (int c = 0; c < D / 8; ++c) {
+                    float kf[8];
+                    unpack_bf16x8(__ldg(kr + c), kf);
+#pragma unroll
+                    for (int x = 0; x < NQ; ++x) {
+                        if (x < nq) {
+                            const float4* qv = reinterpret_cast<const float4*>(qr + x * D + 8 * c);
+                            const float4 q0 = qv[0], q1 = qv[1];
+                            const float qf[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                            acc[x] = dot8(kf, qf, acc[x]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < NQ; ++x)
+                if (x < nq) store_score(S, req, seq, x, b, ok ? acc[x] : __int_as_float(0xFF800000));
+        }
+    }
+}
+
+// Segment scoring of the group's requests: SL = D / 8 lanes per key row.
+template <int NQ, int SL>
+__device__ __forceinline__ void score_group_segments(const ScoreParams& S, int64_t req0, int nreq,
+                                                     const float* qs, int warp, int lane) {
+    constexpr int SEGS = 32 / SL;     // key rows per warp-wide load
+    constexpr int D = 8 * SL;
+    const SelectArgs& a = S.P.a;
+    const int nq = S.nq;
+    const int sg = lane / SL;         // this lane's segment
+    const int j = lane % SL;          // its 8 dimensions [8 j, 8 j + 8)
+    // 32-block rounds over the group's requests, flattened: the warp takes
+    // rounds warp, warp + 4, ...; `before` counts the rounds of earlier requests
+    int64_t next = warp, before = 0;
+    for (int rr = 0; rr < nreq; ++rr) {
+        const int64_t req = req0 + rr;
+        const int64_t seq = __ldg(a.seq_lens + req);
+        const int64_t vmax = causal_blocks_of(seq, a.M);
+        const int64_t rounds = (vmax + 31) >> 5;
+        if (next < before + rounds) {
+            const int32_t* table = a.block_table + req * a.max_blocks;
+            const int64_t tab_end = vmax < a.max_blocks ? vmax : a.max_blocks;
+            float qv[NQ][8];
+            const float* qr = qs + (size_t)rr * nq * D + 8 * j;
+#pragma unroll
+            for (int x = 0; x < NQ; ++x) {
+                float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0;
+                if (x < nq) {
+                    q0 = *reinterpret_cast<const float4*>(qr + x * D);
+                    q1 = *reinterpret_cast<const float4*>(qr + x * D + 4);
+                }
+                qv[x][0] = q0.x; qv[x][1] = q0.y; qv[x][2] = q0.z; qv[x][3] = q0.w;
+                qv[x][4] = q1.x; qv[x][5] = q1.y; qv[x][6] = q1.z; qv[x][7] = q1.w;
+            }
+            for (; next < before + rounds; next += kScoreWarps) {
+                const int64_t base = (next - before) << 5;
+                // lane l holds the table entry of block base + l (-1 past the table)
+                const int32_t tb = base + lane < tab_end ? __ldg(table + base + lane) : -1;
+                uint4 kv[SL];
+#pragma unroll
+                for (int i = 0; i < SL; ++i) {   // row i of the segment: block base + sg + SEGS i
+                    const int64_t phys = __shfl_sync(kFull, tb, sg + SEGS * i);
+                    kv[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (phys >= 0 && phys < S.nb)
+                        kv[i] = __ldg(reinterpret_cast<const uint4*>(S.k + phys * D) + j);
+                }
+                float acc[SL][NQ];
+#pragma unroll
+                for (int i = 0; i < SL; ++i) {
+                    float kf[8];
+                    unpack_bf16x8(kv[i], kf);
+#pragma unroll
+                    for (int x = 0; x < NQ; ++x) acc[i][x] = dot8(kf, qv[x], 0.f);
+                }
+                // reduce-scatter over the segment: at distance m the lanes with
+                // bit m set keep the upper half of the rows and the others the
+                // lower half, each adding its partner's partial sums of the
+                // half it keeps; lane j ends with row j
+#pragma unroll
+                for (int m = SL / 2; m >= 1; m >>= 1) {
+                    const bool up = (j & m) != 0;
+#pragma unroll
+                    for (int i = 0; i < m; ++i) {
+#pragma unroll
+                        for (int x = 0; x < NQ; ++x) {
+                            const float keep = up ? acc[i + m][x] : acc[i][x];
+                            const float send = up ? acc[i][x] : acc[i + m][x];
+                            acc[i][x] = keep + __shfl_xor_sync(kFull, send, m);
+                        }
+                    }
+                }
+                const int own = sg + SEGS * j;           // this lane's block, relative to base
+                const int64_t ph = __shfl_sync(kFull, tb, own);
+                const bool ok = ph >= 0 && ph < S.nb;
+#pragma unroll
+                for (int x = 0; x < NQ; ++x)
+                    if (x < nq)
+                        store_score(S, req, seq, x, base + own,
+                                    ok ? acc[0][x] : __int_as_float(0xFF800000));
+            }
+        }
+        before += rounds;
+    }
+}
+
+// SL = 0: thread scoring; SL = 8 or 16: segment scoring with D = 8 SL.
+template <int NQ, int SL>
+__global__ void __launch_bounds__(kScoreThreads, 4) index_score_select_kernel(const ScoreParams S) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int D = S.D;
     const int nq = S.nq;
     const int R = S.group;
+    const SelectArgs& a = S.P.a;
     float* qs = reinterpret_cast<float*>(smem_raw);                       // [R * nq][D]
     const size_t qbytes = ((size_t)R * nq * D * 4 + 15) & ~(size_t)15;
     uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem_raw + qbytes) + (size_t)warp * S.P.cap * 2;
@@ -2544,66 +2715,10 @@ __global__ void __launch_bounds__(kScoreThreads, 2) index_score_select_kernel(co
         for (int i = tid; i < nreq * nq * D; i += kScoreThreads)
             qs[i] = __uint_as_float((uint32_t)qsrc[i] << 16);
         __syncthreads();
-        for (int rr = 0; rr < nreq; ++rr) {
-            const int64_t req = req0 + rr;
-            const float* qr = qs + (size_t)rr * nq * D;
-            const int64_t seq = __ldg(a.seq_lens + req);
-            // the last query row (local_q = dql - 1, position seq - 1) has the
-            // most causal blocks
-            int64_t vmax = seq > 0 ? (seq + kPageSize - 1) >> kLogPageSize : 0;
-            if (vmax > a.M) vmax = a.M;
-            const int32_t* table = a.block_table + req * a.max_blocks;
-            for (int64_t b = tid; b < vmax; b += kScoreThreads) {
-                float acc[NQ];
-#pragma unroll
-                for (int x = 0; x < NQ; ++x) acc[x] = 0.f;
-                const int64_t phys = b < a.max_blocks ? (int64_t)__ldg(table + b) : -1;
-                const bool ok = phys >= 0 && phys < S.nb;
-                if (ok) {
-                    const uint4* kr = reinterpret_cast<const uint4*>(S.k + phys * D);
-#pragma unroll 8
-                    for (int c = 0; c < D / 8; ++c) {
-                        const uint4 kv = __ldg(kr + c);
-                        const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y),
-                                             bf16_hi(kv.y), bf16_lo(kv.z), bf16_hi(kv.z),
-                                             bf16_lo(kv.w), bf16_hi(kv.w)};
-#pragma unroll
-                        for (int x = 0; x < NQ; ++x) {
-                            if (x < nq) {
-                                const float4* qv = reinterpret_cast<const float4*>(qr + x * D + 8 * c);
-                                const float4 q0 = qv[0], q1 = qv[1];
-                                float sc = acc[x];
-                                sc = fmaf(kf[0], q0.x, sc);
-                                sc = fmaf(kf[1], q0.y, sc);
-                                sc = fmaf(kf[2], q0.z, sc);
-                                sc = fmaf(kf[3], q0.w, sc);
-                                sc = fmaf(kf[4], q1.x, sc);
-                                sc = fmaf(kf[5], q1.y, sc);
-                                sc = fmaf(kf[6], q1.z, sc);
-                                sc = fmaf(kf[7], q1.w, sc);
-                                acc[x] = sc;
-                            }
-                        }
-                    }
-                }
-                // rows whose causal count covers b get its score
-#pragma unroll
-                for (int x = 0; x < NQ; ++x) {
-                    if (x < nq) {
-                        const int lq = x / (int)a.H;
-                        const int h = x - lq * (int)a.H;
-                        const int64_t len = seq - a.dql + lq + 1;   // causal length of the row
-                        int64_t v = len > 0 ? (len + kPageSize - 1) >> kLogPageSize : 0;
-                        if (v > a.M) v = a.M;
-                        if (b < v) {
-                            const int64_t t = req * a.dql + lq;
-                            S.scores[t * a.token_stride + h * a.head_stride + b] =
-                                ok ? acc[x] : __int_as_float(0xFF800000);
-                        }
-                    }
-                }
-            }
-        }
+        if constexpr (SL == 0)
+            score_group_threads<NQ>(S, req0, nreq, qs, tid);
+        else
+            score_group_segments<NQ, SL>(S, req0, nreq, qs, warp, lane);
         __syncthreads();   // the group's scores are visible to the whole CTA
         for (int x = warp; x < nreq * nq; x += kScoreWarps) {
             warp_item<false, 4, 2, true>(S.P, req0 * nq + x, 0, s_keys, s_ids, lane);
@@ -2612,9 +2727,9 @@ __global__ void __launch_bounds__(kScoreThreads, 2) index_score_select_kernel(co
     }
 }
 
-template <int NQ>
-cudaError_t launch_score_nq(const ScoreParams& S, int grid, size_t smem, cudaStream_t st) {
-    auto kern = index_score_select_kernel<NQ>;
+template <int NQ, int SL>
+cudaError_t launch_score(const ScoreParams& S, int grid, size_t smem, cudaStream_t st) {
+    auto kern = index_score_select_kernel<NQ, SL>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
@@ -2622,6 +2737,13 @@ cudaError_t launch_score_nq(const ScoreParams& S, int grid, size_t smem, cudaStr
     }
     kern<<<grid, kScoreThreads, smem, st>>>(S);
     return cudaGetLastError();
+}
+
+template <int SL>
+cudaError_t launch_score_seg(const ScoreParams& S, int grid, size_t smem, cudaStream_t st) {
+    if (S.nq <= 1) return launch_score<1, SL>(S, grid, smem, st);
+    if (S.nq <= 2) return launch_score<2, SL>(S, grid, smem, st);
+    return launch_score<4, SL>(S, grid, smem, st);
 }
 
 }  // namespace
@@ -2682,20 +2804,22 @@ cudaError_t launch_index_score_select(const SelectArgs& a, const uint16_t* q, co
     S.nb = nb;
     S.D = D;
     S.nq = (int32_t)(a.dql * a.H);
-    S.group = S.nq >= kScoreWarps ? 1 : kScoreWarps / S.nq;
+    S.group = S.nq >= kScoreRows ? 1 : kScoreRows / S.nq;
     S.scores = scores;
     const int64_t B = a.T / a.dql;
     if (B == 0) return cudaSuccess;
     const size_t smem = (((size_t)S.group * S.nq * D * 4 + 15) & ~(size_t)15) +
                         (size_t)kScoreWarps * P.cap * 8;
     const int64_t ngroups = (B + S.group - 1) / S.group;
-    int64_t grid = (int64_t)device_sm_count() * 4;
+    int64_t grid = (int64_t)device_sm_count() * 8;
     if (grid > ngroups) grid = ngroups;
-    if (S.nq <= 1) return launch_score_nq<1>(S, (int)grid, smem, stream);
-    if (S.nq <= 2) return launch_score_nq<2>(S, (int)grid, smem, stream);
-    if (S.nq <= 4) return launch_score_nq<4>(S, (int)grid, smem, stream);
-    if (S.nq <= 8) return launch_score_nq<8>(S, (int)grid, smem, stream);
-    return launch_score_nq<16>(S, (int)grid, smem, stream);
+    if (S.nq <= kSegMaxQ && D == 128) return launch_score_seg<16>(S, (int)grid, smem, stream);
+    if (S.nq <= kSegMaxQ && D == 64) return launch_score_seg<8>(S, (int)grid, smem, stream);
+    if (S.nq <= 1) return launch_score<1, 0>(S, (int)grid, smem, stream);
+    if (S.nq <= 2) return launch_score<2, 0>(S, (int)grid, smem, stream);
+    if (S.nq <= 4) return launch_score<4, 0>(S, (int)grid, smem, stream);
+    if (S.nq <= 8) return launch_score<8, 0>(S, (int)grid, smem, stream);
+    return launch_score<16, 0>(S, (int)grid, smem, stream);
 }
 
 }  // namespace bsa

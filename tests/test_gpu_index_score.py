@@ -29,9 +29,9 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-2
 
 
-def _case(seed, B, dql, H, D, M, integer_valued=False):
+def _case(seed, B, dql, H, D, M, integer_valued=False, MB=None):
     g = np.random.default_rng(seed)
-    MB = M
+    MB = M if MB is None else MB
     nb = B * MB + 100
     seq = g.integers(1, M * 128 + 1, B).astype(np.int32)
     seq[g.random(B) < 0.06] = 0                       # padded requests
@@ -52,13 +52,21 @@ def _oracle_all(seq, table, q, k, dql, M, K, I, L):
     return want, nvp, idx, bt, ctx
 
 
+# D = 64 or 128 with at most 4 query rows per request take segment scoring
+# (a group of D / 8 lanes per key row); every other shape takes thread scoring
 CASES = [
-    (48, 1, 2, 128, 1024, 16, 1, 2),    # long-context decode shape, topk 16
+    (48, 1, 2, 128, 1024, 16, 1, 2),    # long-context decode shape, topk 16 (segments)
     (48, 1, 2, 128, 1024, 64, 1, 2),    # the same at topk 64
-    (32, 4, 4, 64, 74, 16, 1, 1),       # production short decode: 16 query rows per request
-    (40, 2, 1, 256, 300, 16, 1, 1),
-    (8, 2, 2, 128, 8192, 32, 1, 1),     # capture-time capacity: multi-pass rows
-    (12, 3, 1, 8, 40, 40, 0, 0),        # topk = capacity, smallest key width
+    (32, 4, 4, 64, 74, 16, 1, 1),       # production short decode: 16 query rows (threads)
+    (40, 2, 1, 256, 300, 16, 1, 1),     # threads
+    (8, 2, 2, 128, 8192, 32, 1, 1),     # capture-time capacity: multi-pass rows (segments)
+    (12, 3, 1, 8, 40, 40, 0, 0),        # topk = capacity, smallest key width (threads)
+    (40, 1, 1, 64, 200, 16, 1, 2),      # segments of 8 lanes, one query row
+    (40, 2, 1, 64, 300, 16, 1, 1),      # segments of 8 lanes, two query rows
+    (24, 4, 1, 64, 130, 32, 2, 2),      # segments of 8 lanes, four query rows
+    (30, 3, 1, 128, 500, 16, 1, 2),     # segments of 16 lanes, three of four query slots
+    (36, 1, 1, 128, 65, 8, 0, 1),       # segments, one block past a 32-block round
+    (16, 5, 1, 128, 200, 16, 1, 1),     # five query rows: threads
 ]
 
 
@@ -110,6 +118,27 @@ def test_index_score_select_matches_oracle(cuda_device, B, dql, H, D, M, K, I, L
         thr = min(s[x] for x in b)      # the oracle's worst selected non-forced score
         for x in a ^ b:
             assert abs(s[x] - thr) <= 2 * TOL, (t, h, x, s[x], thr)
+
+
+@pytest.mark.parametrize("D,dql,H", [(128, 1, 2), (64, 2, 2), (96, 1, 1)])
+def test_index_score_select_narrow_table(cuda_device, D, dql, H):
+    """A block table narrower than the capacity (max_blocks < M): the causal
+    blocks past the table score -inf, in every scoring path."""
+    dev = cuda_device
+    B, M, MB, K = 20, 400, 150, 16
+    seq, table, q, k = _case(77 + D, B, dql, H, D, M, integer_valued=True, MB=MB)
+    scores, idx, bt, ctx = bsa.bsa_index_score_topk_select(
+        q.to(dev), k.to(dev), table.to(dev), torch.from_numpy(seq).to(dev), dql, K, 1, 1, M=M,
+        with_table=True)
+    torch.cuda.synchronize()
+    want, _, want_idx, want_bt, want_ctx = _oracle_all(seq, table, q, k, dql, M, K, 1, 1)
+    got = scores.cpu().numpy().astype(np.float64)
+    causal = ~np.isnan(want)
+    assert np.isneginf(want[:, :, MB:][causal[:, :, MB:]]).all()
+    assert np.array_equal(got[causal], want[causal])
+    assert np.array_equal(idx.cpu().numpy(), want_idx)
+    assert np.array_equal(bt.cpu().numpy(), want_bt)
+    assert np.array_equal(ctx.cpu().numpy(), want_ctx)
 
 
 def test_index_score_select_strided_outputs(cuda_device):
