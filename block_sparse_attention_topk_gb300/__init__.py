@@ -42,8 +42,13 @@ EXPORTED = [
     "bsa_status_string", "bsa_num_valid_pages_decode", "bsa_num_valid_pages_varlen",
     "bsa_topk_workspace_bytes", "bsa_topk_select", "bsa_build_sparse_block_table",
     "bsa_topk_select_sparse_table", "bsa_select_policy", "bsa_topk_select_noalloc",
-    "bsa_index_score_topk_select", "bsa_sparse_decode_attention",
+    "bsa_index_score_topk_select", "bsa_sparse_decode_attention", "bsa_set_status_word",
+    "bsa_read_status",
 ]
+# bits of the device status word (bsa_set_status_word)
+BSA_STATUS_BAD_BLOCK_ID = 0x1
+BSA_STATUS_BAD_PAGE = 0x2
+BSA_STATUS_BAD_CONTEXT = 0x4
 MAX_ATTN_GROUP = 8
 MAX_INDEX_DIM = 1024
 MAX_INDEX_QUERIES = 16
@@ -107,6 +112,8 @@ def lib() -> ctypes.CDLL:
                                                       i64, i64, vp, vp, vp]
             L.bsa_sparse_decode_attention.argtypes = [vp, vp, vp, i64, vp, vp, i64, i64, i64, i64,
                                                       i32, ctypes.c_float, vp, vp]
+            L.bsa_set_status_word.argtypes = [vp]
+            L.bsa_read_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
             for name in EXPORTED[1:]:
                 if name != "bsa_topk_workspace_bytes":
                     getattr(L, name).restype = ctypes.c_int
@@ -466,3 +473,37 @@ def bsa_sparse_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
           k_cache.shape[0], _ptr(sparse_bt), _ptr(sparse_ctx), T, H, G, D, K, ctypes.c_float(scale),
           _ptr(out), _stream(dev))
     return out
+
+
+_status_words: dict[int, torch.Tensor] = {}
+
+
+def bsa_set_status_word(word: torch.Tensor | None, device: torch.device | None = None) -> None:
+    """Registers `word`, a one-element int32 CUDA tensor that the caller has
+    zeroed, as the status word of its device, or with None unregisters the
+    word of `device` (default: the current device).  The kernels of later
+    calls on that device set BSA_STATUS_* bits in it instead of faulting on
+    invalid block-table entries, pages or context lengths.  The binding keeps
+    a reference to the tensor while it is registered."""
+    if word is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        _call("bsa_set_status_word", dev, ctypes.c_void_p(0))
+        _status_words.pop(dev.index, None)
+        return
+    if not isinstance(word, torch.Tensor) or not word.is_cuda or word.dtype != torch.int32 \
+            or word.numel() != 1:
+        raise ValueError("word must be a one-element int32 CUDA tensor")
+    _call("bsa_set_status_word", word.device, _ptr(word))
+    _status_words[word.device.index] = word
+
+
+def bsa_read_status(clear: bool = True, device: torch.device | None = None) -> int:
+    """The status word of `device` (default: the current device) once the work
+    queued so far on its current stream is done, cleared when `clear`; 0 when
+    no word is registered."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    out = ctypes.c_uint32(0)
+    _call("bsa_read_status", dev, ctypes.byref(out), int(bool(clear)), _stream(dev))
+    return int(out.value)

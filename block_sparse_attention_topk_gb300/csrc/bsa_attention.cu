@@ -54,6 +54,7 @@ struct AttnParams {
     int32_t H, G, width;     // width = topk * 8 table entries per row
     float scale;
     float* out;              // fp32 [rows, G, D]
+    uint32_t* status;        // the device status word, or null
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -113,7 +114,9 @@ sparse_decode_attention_kernel(const AttnParams A) {
     for (int64_t row = blockIdx.x; row < A.rows; row += gridDim.x) {
         const int h = (int)(row % A.H);
         const int32_t* bt = A.bt + row * A.width;
-        const int ctx = max(0, min(__ldg(A.ctx + row), cap));
+        const int ctx_in = __ldg(A.ctx + row);
+        const int ctx = max(0, min(ctx_in, cap));
+        if (threadIdx.x == 0) report_status(A.status, ctx != ctx_in, BSA_STATUS_BAD_CONTEXT);
         const uint16_t* qrow = A.q + row * (int64_t)G * D;
         __syncthreads();   // the previous row's readers of shared memory are done
         for (int i = threadIdx.x; i < G * D; i += kAttnWarps * 32)
@@ -132,6 +135,7 @@ sparse_decode_attention_kernel(const AttnParams A) {
             const int j = tile + lane;
             const int32_t page = j < ctx ? __ldg(bt + (j >> 4)) : -1;
             const bool ok = page >= 0 && page < A.num_pages;
+            report_status(A.status, j < ctx && !ok, BSA_STATUS_BAD_PAGE);
             float s[GP];
 #pragma unroll
             for (int g = 0; g < GP; ++g) s[g] = 0.f;
@@ -298,6 +302,7 @@ extern "C" int bsa_sparse_decode_attention(const void* q, const void* k_cache, c
     A.G = (int32_t)G;
     A.width = K * BSA_PAGES_PER_SPARSE_BLOCK;
     A.scale = scale;
+    A.status = current_status_word();
     A.out = out;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;

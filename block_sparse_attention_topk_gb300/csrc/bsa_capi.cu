@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <climits>
 #include <mutex>
 
@@ -17,6 +18,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];
 std::once_flag g_sm_once[kMaxDevices];
+std::atomic<uint32_t*> g_status_word[kMaxDevices];
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -34,6 +36,12 @@ int device_sm_count() {
         g_sm_count[dev] = n;
     });
     return g_sm_count[dev];
+}
+
+uint32_t* current_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    return g_status_word[dev].load(std::memory_order_acquire);
 }
 
 size_t split_workspace_bytes(int64_t rows, int32_t chunks, int32_t K) {
@@ -468,3 +476,28 @@ int bsa_index_score_topk_select(const void* q_idx, const void* k_idx, int64_t nu
 }
 
 }  // extern "C"
+
+extern "C" int bsa_set_status_word(uint32_t* word) {
+    if ((reinterpret_cast<uintptr_t>(word) & 3) != 0) return BSA_ERR_ALIGN;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev < 0 || dev >= kMaxDevices) return BSA_ERR_SHAPE;
+    g_status_word[dev].store(word, std::memory_order_release);
+    return BSA_OK;
+}
+
+extern "C" int bsa_read_status(uint32_t* out, int32_t clear, void* stream) {
+    if (out == nullptr) return BSA_ERR_NULL;
+    *out = 0;
+    uint32_t* word = current_status_word();
+    if (word == nullptr) return BSA_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t got = 0;
+    cudaError_t e = cudaMemcpyAsync(&got, word, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(word, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return (int)e;
+    *out = got;
+    return BSA_OK;
+}

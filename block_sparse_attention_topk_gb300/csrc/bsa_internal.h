@@ -123,11 +123,21 @@ struct SelectArgs {
     int32_t* sparse_ctx;
     bool fused;                       // rows are decode rows: page counts from seq_lens
     bool table;                       // the sparse-table epilogue is written
+    uint32_t* status;                 // the device status word, or null (no checks)
     // x / H and x / dql for x < 2^31 as (umulhi(x, mul) + x) >> shift
     uint32_t h_mul, h_shift, dql_mul, dql_shift;
 };
 
 #ifdef __CUDACC__
+// Sets `bit` in the status word when `bad` holds and a word is registered.
+__device__ __forceinline__ void report_status(uint32_t* word, bool bad, uint32_t bit) {
+    if (word != nullptr && bad) atomicOr(word, bit);
+}
+// A physical block id whose page ids phys * 8 + p are not valid int32 page ids.
+__device__ __forceinline__ bool bad_phys_block(int32_t phys) {
+    return (uint32_t)phys > (uint32_t)BSA_MAX_PHYS_BLOCK;
+}
+
 // One 256-bit store of eight int32 (a full 32-byte sector); p 32-byte aligned.
 __device__ __forceinline__ void st_v8(int32_t* p, const int32_t (&v)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
@@ -158,6 +168,9 @@ size_t split_workspace_bytes(int64_t rows, int32_t chunks, int32_t K);
 SplitWorkspace carve_split_workspace(void* base, int64_t rows, int32_t chunks, int32_t K);
 
 int device_sm_count();
+
+// The status word registered for the current device (bsa_set_status_word), or null.
+uint32_t* current_status_word();
 
 // Launches the selector (plain or fused) with a policy from bsa_select_policy.
 cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,

@@ -337,8 +337,11 @@ __device__ void write_outputs(const KernelParams& P, int64_t row, int64_t t, int
             if (j < n) {
                 const int32_t b = selected_id(j, lo, hi, kp, all, buf_ids);
                 if (b < a.max_blocks &&
-                    (int64_t)b * kPageSize + (int64_t)pg * kSubPage < causal_len)
-                    val = __ldg(table + b) * kPagesPerBlock + pg;
+                    (int64_t)b * kPageSize + (int64_t)pg * kSubPage < causal_len) {
+                    const int32_t phys = __ldg(table + b);
+                    report_status(a.status, pg == 0 && bad_phys_block(phys), BSA_STATUS_BAD_BLOCK_ID);
+                    val = phys * kPagesPerBlock + pg;
+                }
             }
             bt[e] = val;
         }
@@ -893,6 +896,12 @@ __device__ void group_write_outputs(const KernelParams& P, int64_t row, const Ro
 #pragma unroll
             for (int u = 0; u < 8; ++u)
                 if (okb[u]) phys[u] = __ldg(table + bs[u]);
+            if (a.status != nullptr) {
+                bool bad = false;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) bad |= okb[u] && bad_phys_block(phys[u]);
+                report_status(a.status, bad, BSA_STATUS_BAD_BLOCK_ID);
+            }
             if (out != nullptr) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -2490,10 +2499,11 @@ cudaError_t launch_dt(const KernelParams& P, const bsa_launch_policy_t& pol, cud
 //     score[t, h, b] = sum over d of q[t, h, d] * k[block_table[req, b], d]
 // accumulated in fp32 and no scale factor (item 6 removed sm_scale).
 //
-// A CTA of 4 warps takes a group of R requests at a time, R = max(1, 8 /
-// (dql * H)), so that each warp has about two rows to select.  The group's
-// query rows are staged in shared memory as fp32 and the causal blocks are
-// scored in one of two ways:
+// A CTA of 4 warps takes one group of R requests, R = max(1, 4 / (dql * H)),
+// so that each warp has about one row to select; the grid has one CTA per
+// group and the hardware balances CTAs of unequal length (requests differ in
+// their causal block counts).  The group's query rows are staged in shared
+// memory as fp32 and the causal blocks are scored in one of two ways:
 //  * segment scoring (D = 64 or 128 and at most 4 query rows per request):
 //    a segment of D / 8 lanes reads one key row with one 16-byte load per
 //    lane, so that a warp-wide load covers whole rows (two of D = 128, four
@@ -2502,7 +2512,8 @@ cudaError_t launch_dt(const KernelParams& P, const bsa_launch_policy_t& pol, cud
 //    products for the segment's D / 8 rows; a reduce-scatter over the
 //    segment's lanes (recursive halving with shuffles) leaves each lane with
 //    the full dot products of one row.  The warps of the CTA take 32-block
-//    rounds of the group's requests in turn.
+//    rounds of the group's requests in turn, each loading its next round's
+//    table entries one round ahead.
 //  * thread scoring (every other D and query count): a thread takes one
 //    causal block at a time, reads its key row as 16-byte vectors and scores
 //    it against every query row of the request.
@@ -2514,7 +2525,7 @@ cudaError_t launch_dt(const KernelParams& P, const bsa_launch_policy_t& pol, cud
 // ===========================================================================
 constexpr int kScoreThreads = 128;
 constexpr int kScoreWarps = kScoreThreads / 32;
-constexpr int kScoreRows = 8;        // query rows per group when dql * H is small
+constexpr int kScoreRows = 4;        // query rows per group when dql * H is small
 constexpr int kSegMaxQ = 4;          // segment scoring takes up to 4 query rows per request
 
 struct ScoreParams {
@@ -2581,6 +2592,7 @@ __device__ __forceinline__ void score_group_threads(const ScoreParams& S, int64_
             for (int x = 0; x < NQ; ++x) acc[x] = 0.f;
             const int64_t phys = b < a.max_blocks ? (int64_t)__ldg(table + b) : -1;
             const bool ok = phys >= 0 && phys < S.nb;
+            report_status(a.status, b < a.max_blocks && !ok, BSA_STATUS_BAD_BLOCK_ID);
             if (ok) {
                 const uint4* kr = reinterpret_cast<const uint4*>(S.k + phys * D);
 #pragma unroll 8
@@ -2638,10 +2650,21 @@ __device__ __forceinline__ void score_group_segments(const ScoreParams& S, int64
                 qv[x][0] = q0.x; qv[x][1] = q0.y; qv[x][2] = q0.z; qv[x][3] = q0.w;
                 qv[x][4] = q1.x; qv[x][5] = q1.y; qv[x][6] = q1.z; qv[x][7] = q1.w;
             }
+            // each lane keeps the table entry of its block in the warp's next
+            // round, loaded one round ahead
+            int32_t tbn;
+            {
+                const int64_t base = (next - before) << 5;
+                tbn = base + lane < tab_end ? __ldg(table + base + lane) : -1;
+            }
             for (; next < before + rounds; next += kScoreWarps) {
                 const int64_t base = (next - before) << 5;
                 // lane l holds the table entry of block base + l (-1 past the table)
-                const int32_t tb = base + lane < tab_end ? __ldg(table + base + lane) : -1;
+                const int32_t tb = tbn;
+                {
+                    const int64_t nb2 = base + 32 * kScoreWarps + lane;
+                    tbn = nb2 < tab_end ? __ldg(table + nb2) : -1;
+                }
                 uint4 kv[SL];
 #pragma unroll
                 for (int i = 0; i < SL; ++i) {   // row i of the segment: block base + sg + SEGS i
@@ -2678,6 +2701,7 @@ __device__ __forceinline__ void score_group_segments(const ScoreParams& S, int64
                 const int own = sg + SEGS * j;           // this lane's block, relative to base
                 const int64_t ph = __shfl_sync(kFull, tb, own);
                 const bool ok = ph >= 0 && ph < S.nb;
+                report_status(a.status, base + own < tab_end && !ok, BSA_STATUS_BAD_BLOCK_ID);
 #pragma unroll
                 for (int x = 0; x < NQ; ++x)
                     if (x < nq)
@@ -2752,6 +2776,7 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
                           const SplitWorkspace& ws, cudaStream_t stream) {
     KernelParams P;
     P.a = a;
+    P.a.status = current_status_word();
     div_magic((uint32_t)(a.H > 0 ? a.H : 1), &P.a.h_mul, &P.a.h_shift);
     div_magic((uint32_t)(a.dql > 0 ? a.dql : 1), &P.a.dql_mul, &P.a.dql_shift);
     P.ws = Split{ws.keys, ws.ids, ws.counts, ws.tickets};
@@ -2787,6 +2812,7 @@ cudaError_t launch_index_score_select(const SelectArgs& a, const uint16_t* q, co
     ScoreParams S;
     KernelParams& P = S.P;
     P.a = a;
+    P.a.status = current_status_word();
     div_magic((uint32_t)(a.H > 0 ? a.H : 1), &P.a.h_mul, &P.a.h_shift);
     div_magic((uint32_t)(a.dql > 0 ? a.dql : 1), &P.a.dql_mul, &P.a.dql_shift);
     P.ws = Split{nullptr, nullptr, nullptr, nullptr};
@@ -2811,8 +2837,7 @@ cudaError_t launch_index_score_select(const SelectArgs& a, const uint16_t* q, co
     const size_t smem = (((size_t)S.group * S.nq * D * 4 + 15) & ~(size_t)15) +
                         (size_t)kScoreWarps * P.cap * 8;
     const int64_t ngroups = (B + S.group - 1) / S.group;
-    int64_t grid = (int64_t)device_sm_count() * 8;
-    if (grid > ngroups) grid = ngroups;
+    int64_t grid = ngroups < INT32_MAX ? ngroups : INT32_MAX;
     if (S.nq <= kSegMaxQ && D == 128) return launch_score_seg<16>(S, (int)grid, smem, stream);
     if (S.nq <= kSegMaxQ && D == 64) return launch_score_seg<8>(S, (int)grid, smem, stream);
     if (S.nq <= 1) return launch_score<1, 0>(S, (int)grid, smem, stream);

@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(kTableWarps * 32)
 sparse_table_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t H, int32_t K,
                     const int32_t* __restrict__ block_table, int64_t max_blocks,
                     const int32_t* __restrict__ seq_lens, int32_t dql,
-                    int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx) {
+                    int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx,
+                    uint32_t* status) {
     extern __shared__ int32_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -121,8 +122,11 @@ sparse_table_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t 
             int32_t val = 0;
             if (j < n) {
                 const int32_t b = s_sorted[j];
-                if ((int64_t)b * kPageSize + (int64_t)pg * kSubPage < causal_len)
-                    val = __ldg(table + b) * kPagesPerBlock + pg;
+                if ((int64_t)b * kPageSize + (int64_t)pg * kSubPage < causal_len) {
+                    const int32_t phys = __ldg(table + b);
+                    report_status(status, pg == 0 && bad_phys_block(phys), BSA_STATUS_BAD_BLOCK_ID);
+                    val = phys * kPagesPerBlock + pg;
+                }
             }
             bt[e] = val;
         }
@@ -147,7 +151,8 @@ __global__ void __launch_bounds__(kSegWarps * 32)
 sparse_table_seg_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t H, int32_t K,
                         const int32_t* __restrict__ block_table, int64_t max_blocks,
                         const int32_t* __restrict__ seq_lens, int32_t dql,
-                        int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx) {
+                        int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx,
+                        uint32_t* status) {
     constexpr int R = 32 / G;                  // rows per warp
     constexpr int32_t kNone = 0x7FFFFFFF;      // sorts after every (id << 5 | lane)
     __shared__ int32_t s_blk[kSegWarps][32];
@@ -209,6 +214,7 @@ sparse_table_seg_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int6
             if (g < n) {
                 const int32_t b = s_blk[warp][lane];
                 const int32_t ph = s_phys[warp][lane];
+                report_status(status, bad_phys_block(ph), BSA_STATUS_BAD_BLOCK_ID);
                 const int64_t first = (int64_t)b * kPageSize;
 #pragma unroll
                 for (int pg = 0; pg < 8; ++pg)
@@ -244,7 +250,8 @@ __global__ void __launch_bounds__(kSegWarps * 32)
 sparse_table_seg64_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, int64_t H,
                           int32_t K, const int32_t* __restrict__ block_table,
                           int64_t max_blocks, const int32_t* __restrict__ seq_lens, int32_t dql,
-                          int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx) {
+                          int32_t* __restrict__ sparse_bt, int32_t* __restrict__ sparse_ctx,
+                        uint32_t* status) {
     constexpr int32_t kNone = 0x7FFFFFFF;      // sorts after every (id << 6 | e)
     __shared__ int32_t s_in[kSegWarps][64];    // gathered entry by element
     __shared__ int32_t s_blk[kSegWarps][64];   // kept ids, ascending
@@ -324,6 +331,7 @@ sparse_table_seg64_kernel(const int32_t* __restrict__ topk_idx, int64_t rows, in
             if (j < n) {
                 const int32_t b = s_blk[warp][j];
                 const int32_t ph = s_phys[warp][j];
+                report_status(status, bad_phys_block(ph), BSA_STATUS_BAD_BLOCK_ID);
                 const int64_t first = (int64_t)b * kPageSize;
 #pragma unroll
                 for (int pg = 0; pg < 8; ++pg)
@@ -381,6 +389,7 @@ cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, 
                                             int32_t* sparse_ctx, cudaStream_t stream) {
     const int64_t rows = T * H;
     if (rows == 0) return cudaSuccess;
+    uint32_t* status = current_status_word();
     if (K <= 32) {
         const bool vec = (reinterpret_cast<uintptr_t>(sparse_bt) & 31) == 0;
         const int per_block = kSegWarps * (K <= 16 ? 2 : 1);
@@ -391,7 +400,7 @@ cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, 
                             : (vec ? sparse_table_seg_kernel<32, true>
                                    : sparse_table_seg_kernel<32, false>);
         kern<<<grid, kSegWarps * 32, 0, stream>>>(topk_idx, rows, H, K, block_table, max_blocks,
-                                                  seq_lens, dql, sparse_bt, sparse_ctx);
+                                                  seq_lens, dql, sparse_bt, sparse_ctx, status);
         return cudaGetLastError();
     }
     if (K <= 64) {
@@ -400,7 +409,7 @@ cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, 
         const int grid = grid_for(rows, kSegWarps, 1 << 20);
         auto kern = vec ? sparse_table_seg64_kernel<true> : sparse_table_seg64_kernel<false>;
         kern<<<grid, kSegWarps * 32, 0, stream>>>(topk_idx, rows, H, K, block_table, max_blocks,
-                                                  seq_lens, dql, sparse_bt, sparse_ctx);
+                                                  seq_lens, dql, sparse_bt, sparse_ctx, status);
         return cudaGetLastError();
     }
     const size_t smem = (size_t)kTableWarps * 3 * K * sizeof(int32_t);
@@ -411,7 +420,7 @@ cudaError_t launch_build_sparse_block_table(const int32_t* topk_idx, int64_t T, 
         if (e != cudaSuccess) return e;
     }
     sparse_table_kernel<<<grid_for(rows, kTableWarps, 16), kTableWarps * 32, smem, stream>>>(
-        topk_idx, rows, H, K, block_table, max_blocks, seq_lens, dql, sparse_bt, sparse_ctx);
+        topk_idx, rows, H, K, block_table, max_blocks, seq_lens, dql, sparse_bt, sparse_ctx, status);
     return cudaGetLastError();
 }
 

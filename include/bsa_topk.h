@@ -297,6 +297,45 @@ int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_t T, int64_
 int bsa_select_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
                       bsa_launch_policy_t* policy);
 
+/* ---- device status word ------------------------------------------------ */
+/* A diagnostic aid of this library (the pages describe none; their kernels
+ * mask the cases below, [47984] 实现拆解 item 3).  Instead of trapping, the
+ * kernels set bits in a 32-bit device word that the caller registers when
+ * they meet input that the calls above handle without a fault but that is
+ * not valid:
+ *   BSA_STATUS_BAD_BLOCK_ID  the sparse-table expansion (bsa_build_sparse_block_table
+ *                            and the fused calls) met a block_table entry of a
+ *                            kept block that is negative or above
+ *                            BSA_MAX_PHYS_BLOCK (its page ids phys * 8 + p are
+ *                            still written as computed); or the index scoring
+ *                            met an entry of a causal block below max_blocks
+ *                            outside [0, num_phys_blocks) (scored -inf).
+ *   BSA_STATUS_BAD_PAGE      the sparse decode attention met a table entry of
+ *                            a context token outside [0, num_pages) (the token
+ *                            takes no part).
+ *   BSA_STATUS_BAD_CONTEXT   the sparse decode attention met a sparse_ctx
+ *                            entry below 0 or above K * 128 (clamped). */
+#define BSA_STATUS_BAD_BLOCK_ID 0x1u
+#define BSA_STATUS_BAD_PAGE 0x2u
+#define BSA_STATUS_BAD_CONTEXT 0x4u
+#define BSA_MAX_PHYS_BLOCK 0x0FFFFFFF  /* largest block id whose page ids fit int32 */
+
+/* Registers `word`, a DEVICE pointer to one uint32 on the current device
+ * (4-byte aligned, owned by the caller, zeroed by the caller), as that
+ * device's status word; NULL unregisters it.  Calls made afterwards on the
+ * device pass it to their kernels (a CUDA graph keeps the word registered
+ * when it was captured); with none registered the kernels skip the checks.
+ * Registration is not ordered against calls being made from other threads.
+ * Errors: BSA_ERR_ALIGN; BSA_ERR_SHAPE for a device ordinal >= 64; a
+ * positive cudaError_t when the current device cannot be read. */
+int bsa_set_status_word(uint32_t* word);
+
+/* Copies the current device's status word to *out (HOST) once the work
+ * queued on `stream` so far is done, and clears the word when `clear` is
+ * nonzero; synchronizes `stream`.  *out = 0 when no word is registered.
+ * Errors: BSA_ERR_NULL (out); a positive cudaError_t from the copy. */
+int bsa_read_status(uint32_t* out, int32_t clear, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,6 +31,9 @@ TOL = 1e-3
     (24, 2, 2, 3, 128, 96, 16),     # GQA group of 3, two index/KV heads
     (16, 1, 1, 8, 64, 200, 64),     # topk 64, group of 8
     (32, 4, 1, 1, 256, 40, 16),     # query length 4, one query head, wide heads
+    (20, 4, 1, 4, 64, 64, 16),      # the bench's shape: group of 4, D = 64
+    (16, 2, 2, 2, 128, 80, 32),     # group of 2, D = 128
+    (12, 1, 3, 1, 64, 50, 16),      # one query head, three KV heads
 ])
 def test_sparse_decode_attention(cuda_device, B, dql, H, G, D, MB, K):
     dev = cuda_device
@@ -69,11 +72,12 @@ def test_sparse_decode_attention(cuda_device, B, dql, H, G, D, MB, K):
     assert torch.equal(got2, got)
 
 
-def test_sparse_decode_attention_pages_out_of_range(cuda_device):
+@pytest.mark.parametrize("G", [2, 8])
+def test_sparse_decode_attention_pages_out_of_range(cuda_device, G):
     """Tokens on page ids outside the cache take no part, as in the oracle;
     a row whose every page is out of range yields zeros."""
     dev = cuda_device
-    T, H, G, D, K = 6, 1, 2, 64, 2
+    T, H, D, K = 6, 1, 64, 2
     num_pages = 5
     bt = np.zeros((T, H, K * 8), dtype=np.int32)
     bt[:, 0, :4] = [[1, 7, 2, -1], [0, 1, 2, 3], [9, 9, 9, 9], [4, 4, 5, 0],
