@@ -55,7 +55,8 @@ def parse():
     p.add_argument("--no-configs", action="store_true")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the topk-64, index-score and attention measurements")
-    p.add_argument("--extras-only", choices=["index_score", "attention"], default=None,
+    p.add_argument("--extras-only", choices=["index_score", "attention", "prefill_heavy"],
+                   default=None,
                    help="time only this call and print its record (for profiling)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
@@ -609,10 +610,11 @@ def run_e2e(args, w, table, device, stream, rows, expect=None):
             "steps": args.e2e_steps, "chunks": C, "kernel_launches_per_step": C}
 
 
-def config_latencies(device):
-    """Latency of one fused/select call on each workload as given: the call is
-    captured in a CUDA graph and each replay is timed with events (inputs
-    resident in HBM; L2 flushed before each replay by writing 256 MB)."""
+def config_latencies(device, only=None):
+    """Latency of one fused/select call on each workload as given (or on the
+    one named `only`): the call is captured in a CUDA graph and each replay
+    is timed with events (inputs resident in HBM; L2 flushed before each
+    replay by writing 256 MB)."""
     import synth
     import block_sparse_attention_topk_gb300 as bsa
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device=device)
@@ -633,6 +635,8 @@ def config_latencies(device):
             device=device, H=4, M=8192, K=16, dtype=torch.bfloat16,
             prefill_prefix=(0, 8192 * 128 - 8192), decode_max_prefix=8192 * 128 - 1),
     }
+    if only is not None:
+        cases = {only: cases[only]}
     for name, w in cases.items():
         if w.seq_lens is not None:
             nvp = bsa.bsa_num_valid_pages_decode(w.seq_lens, w.dql)
@@ -749,8 +753,12 @@ def run_extras_only(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     bsa.lib()
-    fn = index_score_step if args.extras_only == "index_score" else attention_step
-    print(json.dumps({args.extras_only: fn(device, args)}), flush=True)
+    if args.extras_only == "prefill_heavy":
+        res = config_latencies(device, only="prefill_heavy_8192")["prefill_heavy_8192"]
+    else:
+        fn = index_score_step if args.extras_only == "index_score" else attention_step
+        res = fn(device, args)
+    print(json.dumps({args.extras_only: res}), flush=True)
 
 
 if __name__ == "__main__":

@@ -426,6 +426,12 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs& a, int64_t row) {
     return row_info_from(a, row, row_meta(a, row));
 }
 
+// Ask L2 to fetch [addr, addr + bytes) (16-byte aligned, multiple of 16)
+// ahead of use; no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(uintptr_t addr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
+
 // One work item (row, chunk) processed by a whole warp: the warp path, and
 // the fallback of the group path for rows whose candidates overflow.  COH:
 // the scores were written earlier in the same kernel, so they are read
@@ -462,8 +468,21 @@ __device__ void warp_item(const KernelParams& P, int64_t row, int chunk, uint32_
         if (chunk >= nchunks) return;
         const int k_begin = chunk * P.vecs_per_chunk;
         const int k_end = min(nvec, k_begin + P.vecs_per_chunk);
+        if (!COH && k_end - k_begin > 32 * NV) {
+            // more than one pass: bring the warp's whole range towards L2 at
+            // once, 4 KB per lane, so that later passes do not wait on DRAM
+            uintptr_t plo = v0 + ((uintptr_t)k_begin << 4);
+            uintptr_t phi = v0 + ((uintptr_t)k_end << 4);
+            if (plo < P.buf_lo) plo = (P.buf_lo + 15) & ~(uintptr_t)15;
+            if (phi > P.buf_hi) phi = P.buf_hi & ~(uintptr_t)15;
+            const uintptr_t at = plo + ((uintptr_t)lane << 12);
+            if (at < phi) prefetch_l2(at, (uint32_t)min((uintptr_t)4096, phi - at));
+        }
 
         Buf b{s_keys, s_ids, 0, 0u, false};
+        // the largest theta of the earlier passes (raw, -1 = none): each is a
+        // lower bound of the row's kp-th largest key, so it filters later passes
+        int32_t th_run = -1;
 
         for (int pass = k_begin; pass < k_end && !b.closed; pass += 32 * NV) {
             // ---- load NV vectors per lane (masked outside [lo, hi)) ----
@@ -515,9 +534,14 @@ __device__ void warp_item(const KernelParams& P, int64_t row, int chunk, uint32_
                     rep[(2 * j + 1) % R] = max(rep[(2 * j + 1) % R], q1);
                 }
             }
+            // this pass's theta helps only if kp representatives lie above the
+            // bounds already known (the entry bound's raw value and th_run);
+            // otherwise the bit search is skipped and those bounds filter
+            const int32_t known =
+                max(b.kb >= E::kKeyOfPlusZero ? E::raw_of_nonneg_key(b.kb) : -1, th_run);
             int c0 = 0;
 #pragma unroll
-            for (int r = 0; r < R; ++r) c0 += rep[r] >= 0 ? 1 : 0;
+            for (int r = 0; r < R; ++r) c0 += rep[r] > known ? 1 : 0;
             c0 = __reduce_add_sync(kFull, c0);
             bool have_theta = c0 >= kp;
             int32_t theta = 0;
@@ -530,6 +554,13 @@ __device__ void warp_item(const KernelParams& P, int64_t row, int chunk, uint32_
                     c = __reduce_add_sync(kFull, c);
                     if (c >= kp) theta = tt;
                 }
+                // fp32 searches the top 16 bits only, so theta may fall below
+                // th_run
+                theta = max(theta, th_run);
+                th_run = theta;
+            } else if (th_run >= 0) {
+                have_theta = true;
+                theta = th_run;
             }
 
             // ---- filter + append, one 32-vector slot at a time ----
@@ -720,12 +751,6 @@ __device__ __forceinline__ uint4 group_load_edge(const KernelParams& P, int k, u
         }
     }
     return w;
-}
-
-// Ask L2 to fetch [addr, addr + bytes) (16-byte aligned, multiple of 16)
-// ahead of use; no completion to wait for.
-__device__ __forceinline__ void prefetch_l2(uintptr_t addr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
 }
 
 // Two partial maxima of a vector (bf16: the two halves of the packed max;
