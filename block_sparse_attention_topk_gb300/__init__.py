@@ -27,6 +27,7 @@ BSA_PATH_SPLIT = 1
 BSA_PATH_GROUP = 2
 BSA_PATH_PAIR = 3
 BSA_PATH_OCTET = 4
+BSA_PATH_WIDE = 5
 PAGE_SIZE = 128
 PAGES_PER_SPARSE_BLOCK = 8
 MAX_TOPK = 1024

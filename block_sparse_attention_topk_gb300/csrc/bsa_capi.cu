@@ -111,6 +111,7 @@ int forced_path() {
         if (strcmp(e, "group") == 0) return BSA_PATH_GROUP;
         if (strcmp(e, "pair") == 0) return BSA_PATH_PAIR;
         if (strcmp(e, "octet") == 0) return BSA_PATH_OCTET;
+        if (strcmp(e, "wide") == 0) return BSA_PATH_WIDE;
         return -1;
     }();
     return v;
@@ -150,6 +151,26 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
     const bool short_rows = M * elem <= kGroupMaxBytes;
     const bool pair_ok = K <= kGroupMaxK && short_rows;
     const bool oct_ok = K <= kOctMaxK && short_rows;
+    // Wide path (one warp per row) for bf16 buffers wider than 2 KB with
+    // topk <= 64 wherever the row path would not split rows (with fewer
+    // rows the split path spreads each long row over several warps); any
+    // bf16 buffer when forced.
+    const bool wide_ok = dtype == BSA_DTYPE_BF16 && K <= kOctMaxK && cap <= kWideMaxCap;
+    if (wide_ok && (forced == BSA_PATH_WIDE ||
+                    (!short_rows && chunks == 1 && forced != BSA_PATH_ROW))) {
+        int64_t grid = (rows + kWideWarps - 1) / kWideWarps;
+        if (grid > INT32_MAX) grid = INT32_MAX;
+        if (grid < 1) grid = 1;
+        p->path = BSA_PATH_WIDE;
+        p->vecs_per_lane = 4;
+        p->chunks_per_row = 1;
+        p->reps_per_lane = 16;
+        p->warps_per_cta = kWideWarps;
+        p->grid = (int32_t)grid;
+        p->cand_capacity = cap;
+        p->smem_bytes = kWideWarps * (int)sizeof(WideSmem);
+        return BSA_OK;
+    }
     // Octet path (8 lanes per row, 4 rows per warp) for 32 < topk <= 64, or
     // for any topk <= 64 when forced.
     if (oct_ok && (forced == BSA_PATH_OCTET || (!pair_ok && forced != BSA_PATH_ROW))) {

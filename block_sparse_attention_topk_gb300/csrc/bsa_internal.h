@@ -105,6 +105,24 @@ struct OctSmem {
     uint32_t scratch[32][8];            // one 32-byte chunk per lane while candidates are read out
 };
 
+// Wide path: one warp per row, for bf16 rows longer than 2 KB and topk <= 64
+// (see bsa_select.cu).
+constexpr int kWideCand = 256;       // candidate capacity per row (8 per lane)
+constexpr int kWideWarps = 4;        // warps per CTA, one row each
+constexpr int kWideMaxCap = 320;     // warp-path buffer entries an overflowing row needs (topk <= 64)
+
+struct WideSmem {
+    union {
+        struct {
+            int16_t ckey[kWideCand];      // candidate keys (signed order-preserving), id order
+            uint16_t cid[kWideCand];      // their block ids
+            int32_t sorted[kOctMaxK];     // selected non-forced ids, ascending
+        } c;
+        uint32_t fallback[2 * kWideMaxCap];  // the warp path's keys and ids
+    };
+    uint32_t scratch[32][8];              // one 32-byte chunk per lane while candidates are read out
+};
+
 // Everything one selector launch needs.  Pointers are device pointers.
 struct SelectArgs {
     const void* scores;

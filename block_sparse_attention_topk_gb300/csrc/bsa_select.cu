@@ -2440,6 +2440,268 @@ cudaError_t launch_octet(const KernelParams& P, const bsa_launch_policy_t& pol, 
     return cudaGetLastError();
 }
 
+// ===========================================================================
+// Wide path: one warp per row, for bf16 rows of a buffer wider than 2 KB
+// (capacities above 1024 tiles, up to the 8192-tile capture-time capacity)
+// and topk <= 64.  The octet path's steps with all 32 lanes on one row:
+//  1. the lanes stream the row's interior 32-byte chunks (chunk k to lane
+//     k mod 32, two loads in flight) and keep, per element position, the raw
+//     maximum and minimum: 16 representatives per lane, 512 per row, each
+//     the largest key of a distinct set of elements; the row is asked into
+//     L2 first, 4 KB per lane;
+//  2. theta: a binary search over the representatives' counts, stopped when
+//     the interval is 16 keys wide, gives a bound that at least K' of them,
+//     so at least K' elements, reach;
+//  3. the chunks are read again (L2 hits, the next chunk in flight) and the
+//     elements >= theta are appended to a 256-entry list in id order, placed
+//     by a warp-wide scan; rows of at most 256 non-forced blocks skip steps
+//     1-2 and take every element;
+//  4. kappa, the K'-th largest candidate, by a binary search over the
+//     candidates (8 per lane); those above it are kept, and of those equal
+//     to it the first in id order, as many as K' still needs; the kept ids,
+//     already in id order, go to the sorted list;
+//  5. the row path's outputs (ids, and in fused mode the table).
+// A row whose candidates overflow the list is redone by the warp on the row
+// path.
+// ===========================================================================
+
+// Per lane: how many of the 2 NW packed signed keys are >= t (t > -32768).
+template <int NW>
+__device__ __forceinline__ int count_ge16(const uint32_t (&w)[NW], int32_t t) {
+    const uint32_t t2 = ((uint32_t)(t - 1) & 0xFFFFu) * 0x10001u;
+    uint32_t acc = 0;
+#pragma unroll
+    for (int x = 0; x < NW; ++x) acc += min_u16x2(max_s16x2(w[x], t2) ^ t2, 0x00010001u);
+    return (int)((acc & 0xFFFFu) + (acc >> 16));
+}
+
+template <int NW>
+__device__ __forceinline__ int32_t max16(const uint32_t (&w)[NW]) {
+    uint32_t m = w[0];
+#pragma unroll
+    for (int x = 1; x < NW; ++x) m = max_s16x2(m, w[x]);
+    return max((int32_t)(int16_t)(uint16_t)m, (int32_t)(int16_t)(uint16_t)(m >> 16));
+}
+
+template <int FM>
+__global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const KernelParams P) {
+    constexpr int CE = 16;                 // bf16 elements per 32-byte chunk
+    constexpr int32_t kKeyMin = -32768;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    WideSmem& sm = *reinterpret_cast<WideSmem*>(smem_raw + (size_t)warp * sizeof(WideSmem));
+    const SelectArgs& a = P.a;
+    const int64_t stride = (int64_t)gridDim.x * kWideWarps;
+
+    for (int64_t row = (int64_t)blockIdx.x * kWideWarps + warp; row < P.rows; row += stride) {
+        const RowInfo r = row_info_from<FM>(a, row, row_meta<FM>(a, row));
+        if (!r.need) {
+            write_outputs(P, row, r.t, r.h, r.n, r.lo, r.hi, r.kp, r.all, sm.c.sorted,
+                          r.causal_len, r.req, lane);
+            __syncwarp();
+            continue;
+        }
+
+        // ---- geometry of the non-forced range [lo, hi), 32-byte chunks ----
+        const char* row_ptr = reinterpret_cast<const char*>(a.scores) +
+                              ((int64_t)r.t * a.token_stride + (int64_t)r.h * a.head_stride) * 2;
+        const uintptr_t a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * 2;
+        const uintptr_t a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * 2;
+        const uintptr_t c0 = a_lo & ~(uintptr_t)31;
+        const int nchunk = (int)((a_hi - c0 + 31) >> 5);
+        const int base_id = r.lo - (int)((a_lo - c0) / 2);
+        {
+            // the whole range towards L2, 4 KB per lane (a row is at most 128 KB)
+            uintptr_t plo = c0 < P.buf_lo ? (P.buf_lo + 15) & ~(uintptr_t)15 : c0;
+            uintptr_t phi = c0 + ((uintptr_t)nchunk << 5);
+            if (phi > P.buf_hi) phi = P.buf_hi & ~(uintptr_t)15;
+            const uintptr_t at = plo + ((uintptr_t)lane << 12);
+            if (at < phi) prefetch_l2(at, (uint32_t)min((uintptr_t)4096, phi - at));
+        }
+        const int kp = r.kp;
+
+        // ---- steps 1-2: representatives and theta ----
+        int32_t theta = kKeyMin;
+        if (r.hi - r.lo > kWideCand) {
+            uint32_t rmx[8], rmn[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                rmx[x] = 0x80008000u;
+                rmn[x] = 0x7FFF7FFFu;
+            }
+            auto fold = [&](const uint32_t (&w)[8]) {
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    rmx[x] = max_s16x2(rmx[x], w[x]);
+                    rmn[x] = min_s16x2(rmn[x], w[x]);
+                }
+            };
+            // interior chunks 1 .. nchunk - 2; the edge chunks are left out
+            const int klast = nchunk - 2;
+            int k = lane == 0 ? 32 : lane;
+            const bool any_interior = k <= klast;
+            for (; k + 32 <= klast; k += 64) {
+                uint32_t w0[8], w1[8];
+                ld32(c0 + ((uintptr_t)k << 5), w0);
+                ld32(c0 + ((uintptr_t)(k + 32) << 5), w1);
+                fold(w0);
+                fold(w1);
+            }
+            if (k <= klast) {
+                uint32_t w0[8];
+                ld32(c0 + ((uintptr_t)k << 5), w0);
+                fold(w0);
+            }
+            uint32_t rp[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                // a position's largest key: its raw maximum when that is
+                // non-negative, else the key of its raw minimum
+                const uint32_t mneg = sign_mask16(rmx[x]);
+                rp[x] = any_interior ? (rmx[x] & ~mneg) | ((rmn[x] ^ 0x7FFF7FFFu) & mneg)
+                                     : 0x80008000u;
+            }
+            // count(>= lo) >= kp throughout (every representative counts at
+            // the smallest key); stop at a 16-key interval
+            int32_t lo = kKeyMin, hi = __reduce_max_sync(kFull, max16(rp)) + 1;
+            while (hi - lo > 16) {
+                const int32_t mid = (lo + hi) >> 1;
+                if ((int)__reduce_add_sync(kFull, (unsigned)count_ge16(rp, mid)) >= kp) lo = mid;
+                else hi = mid;
+            }
+            theta = lo;
+        }
+
+        // ---- step 3: candidates >= theta, in id order ----
+        const bool raw_ok = theta >= 0;   // raw signed order is key order against it
+        const int steps = (nchunk + 31) >> 5;
+        int cbase = 0;
+        auto plain = [&](int k) {
+            const uintptr_t addr = c0 + ((uintptr_t)k << 5);
+            return (k != 0 && k != nchunk - 1) || (addr >= P.buf_lo && addr + 32 <= P.buf_hi);
+        };
+        uint32_t nx[8];
+        auto issue = [&](int st) {
+            const int k = lane + 32 * st;
+            if (k < nchunk && plain(k)) ld32(c0 + ((uintptr_t)k << 5), nx);
+        };
+        issue(0);
+        for (int st = 0; st < steps; ++st) {
+            const int k = lane + 32 * st;
+            const bool has = k < nchunk;
+            uint32_t w[8];
+            uint32_t m = 0;
+            if (has) {
+                if (!plain(k)) {
+                    // masked keys, which compare like raw bits against theta >= 0
+                    pair_load_edge<true>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) w[x] = nx[x];
+                    if (!raw_ok) chunk_to_keys<true>(w);
+                }
+            }
+            issue(st + 1);
+            if (has) {
+                m = theta == kKeyMin ? 0xFFFFu : ge_bits16<8>(w, theta);
+                if (k == 0 || k == nchunk - 1) {
+                    const int first_id = base_id + k * CE;
+                    const int lo_e = min(max(r.lo - first_id, 0), CE);
+                    const int hi_e = min(max(r.hi - first_id, 0), CE);
+                    m &= ((1u << hi_e) - 1u) & ~((1u << lo_e) - 1u);
+                }
+            }
+            int tot;
+            const int off = warp_excl_scan(__popc(m), lane, tot);
+            if (m) {
+                uint32_t* scr = sm.scratch[lane];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) scr[x] = w[x];
+                const int first_id = base_id + k * CE;
+                int pos = cbase + off;
+                while (m) {
+                    const int e = __ffs(m) - 1;
+                    m &= m - 1;
+                    if (pos < kWideCand) {
+                        sm.c.ckey[pos] = reinterpret_cast<const int16_t*>(scr)[e];
+                        sm.c.cid[pos] = (uint16_t)(first_id + e);
+                    }
+                    ++pos;
+                }
+            }
+            cbase += tot;
+        }
+        __syncwarp();
+        if (cbase > kWideCand) {
+            // overflow: the whole warp redoes the row on the row path
+            warp_item<true, 4, 2>(P, row, 0, sm.fallback,
+                                  reinterpret_cast<int32_t*>(sm.fallback + P.cap), lane);
+            __syncwarp();
+            continue;
+        }
+
+        // ---- step 4: kappa, the K'-th largest candidate key ----
+        // lane holds list positions 8 lane .. 8 lane + 7; padding holds the
+        // smallest key, which no searched threshold (> lo >= -32768) counts
+        const int nvalid = min(max(cbase - 8 * lane, 0), 8);
+        const uint32_t valid = (1u << nvalid) - 1u;
+        uint32_t kw[4];
+        {
+            const uint4 v = *reinterpret_cast<const uint4*>(&sm.c.ckey[8 * lane]);
+            kw[0] = v.x; kw[1] = v.y; kw[2] = v.z; kw[3] = v.w;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const uint32_t keep = ((valid >> (2 * x)) & 1u ? 0x0000FFFFu : 0u) |
+                                      ((valid >> (2 * x + 1)) & 1u ? 0xFFFF0000u : 0u);
+                kw[x] = (kw[x] & keep) | (0x80008000u & ~keep);
+            }
+        }
+        // count(>= lo) >= K' > count(>= hi) = cnt_hi throughout
+        int32_t lo = theta, hi = __reduce_max_sync(kFull, max16(kw)) + 1;
+        int cnt_hi = 0;
+        while (hi - lo > 1) {
+            const int32_t mid = (lo + hi) >> 1;
+            const int cnt = (int)__reduce_add_sync(kFull, (unsigned)count_ge16(kw, mid));
+            if (cnt >= kp) {
+                lo = mid;
+            } else {
+                hi = mid;
+                cnt_hi = cnt;
+            }
+        }
+        // kappa = lo: every candidate above it, and the first (K' - count
+        // above) of those equal to it, in id order
+        const uint32_t gtm = ge_bits16<4>(kw, lo + 1) & valid;
+        const uint32_t eqm = (lo == kKeyMin ? valid : ge_bits16<4>(kw, lo) & valid) & ~gtm;
+        int tall;
+        const int tb = warp_excl_scan(__popc(eqm), lane, tall);
+        const int allowed = min(max(kp - cnt_hi - tb, 0), __popc(eqm));
+        uint32_t rest = eqm;
+        for (int i = 0; i < allowed; ++i) rest &= rest - 1;
+        uint32_t selm = gtm | (eqm & ~rest);
+        int stot;
+        int o = warp_excl_scan(__popc(selm), lane, stot);
+        while (selm) {
+            const int e = __ffs(selm) - 1;
+            selm &= selm - 1;
+            sm.c.sorted[o++] = sm.c.cid[8 * lane + e];
+        }
+        __syncwarp();
+
+        // ---- step 5: outputs ----
+        write_outputs(P, row, r.t, r.h, r.n, r.lo, r.hi, kp, false, sm.c.sorted, r.causal_len,
+                      r.req, lane);
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_wide(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
+    auto kern = P.a.fused ? wide_select_kernel<kFusedYes> : wide_select_kernel<kFusedNo>;
+    kern<<<pol.grid, kWideWarps * 32, pol.smem_bytes, st>>>(P);
+    return cudaGetLastError();
+}
+
 template <bool BF16, int FM>
 cudaError_t launch_pair_fm(const KernelParams& P, const bsa_launch_policy_t& pol,
                            cudaStream_t st) {
@@ -2828,6 +3090,10 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
     if (pol.path == BSA_PATH_OCTET)
         return a.dtype == BSA_DTYPE_BF16 ? launch_octet<true>(P, pol, stream)
                                          : launch_octet<false>(P, pol, stream);
+    if (pol.path == BSA_PATH_WIDE) {
+        if (a.dtype != BSA_DTYPE_BF16 || pol.cand_capacity > kWideMaxCap) return cudaErrorInvalidValue;
+        return launch_wide(P, pol, stream);
+    }
     return a.dtype == BSA_DTYPE_BF16 ? launch_dt<true>(P, pol, stream)
                                      : launch_dt<false>(P, pol, stream);
 }

@@ -78,6 +78,7 @@ extern "C" {
 #define BSA_PATH_GROUP 2    /* 4 lanes per row, 8 rows per warp (K <= 32)   */
 #define BSA_PATH_PAIR 3     /* 2 lanes per row, 16 rows per warp (K <= 32)  */
 #define BSA_PATH_OCTET 4    /* 8 lanes per row, 4 rows per warp (K <= 64)   */
+#define BSA_PATH_WIDE 5     /* 32 lanes per row, bf16 rows > 2 KB (K <= 64) */
 
 typedef struct bsa_launch_policy {
     int32_t path;             /* BSA_PATH_*                                   */
@@ -288,11 +289,14 @@ int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_t T, int64_
  * 128 / 129 and other capacity boundaries can be tested without a GPU.
  * Paths: BSA_PATH_PAIR when K <= 32 and a row holds at most 2 KB (M * element
  * size <= 2048), BSA_PATH_OCTET when 32 < K <= 64 and a row holds at most
- * 2 KB; otherwise BSA_PATH_ROW, or BSA_PATH_SPLIT when a row needs more than
- * one pass and the rows alone cannot fill the GPU.  The environment variable
- * BSA_SELECT_PATH=row|group|pair|octet, read once per process, forces a path
- * among those that can serve the call, for testing (BSA_PATH_GROUP is
- * reachable only that way).
+ * 2 KB; BSA_PATH_SPLIT when a row needs more than one pass and the rows
+ * alone cannot fill the GPU (at most num_sms * 16 rows); otherwise
+ * BSA_PATH_WIDE for bf16 rows of more than 2 KB (M > 1024, up to the
+ * 8192-tile capture-time capacity and beyond) with K <= 64, and
+ * BSA_PATH_ROW for the rest.  The
+ * environment variable BSA_SELECT_PATH=row|group|pair|octet|wide, read once
+ * per process, forces a path among those that can serve the call, for
+ * testing (BSA_PATH_GROUP is reachable only that way).
  * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_TOPK, BSA_ERR_DTYPE. */
 int bsa_select_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
                       bsa_launch_policy_t* policy);

@@ -59,10 +59,13 @@ BF, FP = 0, 1
 @pytest.mark.parametrize("M,dtype,K,path", [
     # pair path: topk <= 32 and a row of at most 2 KB
     (16, FP, 4, 3), (74, BF, 16, 3), (128, BF, 16, 3), (129, BF, 16, 3), (1024, BF, 16, 3),
-    (1025, BF, 16, 0), (512, FP, 16, 3), (513, FP, 16, 0), (1024, BF, 32, 3),
+    (1025, BF, 16, 5), (512, FP, 16, 3), (513, FP, 16, 0), (1024, BF, 32, 3),
     # octet path: 32 < topk <= 64 and a row of at most 2 KB
     (1024, BF, 33, 4), (74, BF, 64, 4), (1024, BF, 64, 4), (512, FP, 64, 4), (513, FP, 64, 0),
-    (1025, BF, 64, 0), (1024, BF, 65, 0), (8192, BF, 16, 0)])
+    # wide path: bf16 rows of more than 2 KB, topk <= 64, many rows
+    (1025, BF, 64, 5), (8192, BF, 16, 5), (8192, BF, 1, 5), (65536, BF, 64, 5),
+    # row path: topk > 64, or fp32 rows of more than 2 KB
+    (1024, BF, 65, 0), (8192, FP, 16, 0), (8192, BF, 65, 0)])
 def test_policy_path(bsa, M, dtype, K, path):
     assert _policy(bsa, 10**6, M, K, dtype)["path"] == path
 
@@ -123,9 +126,27 @@ def test_policy_split_only_for_few_long_rows(bsa):
     assert _policy(bsa, 2432, 8192, 16, BF)["chunks_per_row"] == 2
 
 
+def test_policy_wide(bsa):
+    """Wide path: one row per warp, 4 warps per CTA, wherever rows are not
+    split (more than num_sms * 16 rows; fewer long rows are split over
+    several warps); the overflow fallback's buffer fits in a warp's shared
+    memory."""
+    for sms in (148, 152):
+        p = _policy(bsa, 32 * sms, 8192, 64, BF, sms)
+        assert p["path"] == bsa.BSA_PATH_WIDE and p["chunks_per_row"] == 1
+        assert p["grid"] == 32 * sms // 4 and p["warps_per_cta"] == 4
+        assert p["cand_capacity"] * 8 <= p["smem_bytes"] // p["warps_per_cta"]
+        assert _policy(bsa, 16 * sms + 1, 8192, 64, BF, sms)["path"] == bsa.BSA_PATH_WIDE
+        p = _policy(bsa, 16 * sms, 8192, 64, BF, sms)
+        assert p["path"] == bsa.BSA_PATH_SPLIT and p["chunks_per_row"] == 2
+    # a 2 KB capacity stays on the pair and octet paths
+    assert _policy(bsa, 10**6, 1024, 16, BF)["path"] == bsa.BSA_PATH_PAIR
+    assert _policy(bsa, 10**6, 1024, 64, BF)["path"] == bsa.BSA_PATH_OCTET
+
+
 def test_policy_capacity_and_grid(bsa):
-    p = _policy(bsa, 10**6, 1025, 64, BF)
-    assert p["cand_capacity"] >= 64 + 32 * 8 and p["cand_capacity"] % 32 == 0
+    p = _policy(bsa, 10**6, 1025, 65, BF)
+    assert p["cand_capacity"] >= 65 + 32 * 8 and p["cand_capacity"] % 32 == 0
     assert p["smem_bytes"] == p["warps_per_cta"] * p["cand_capacity"] * 8
     assert p["grid"] == (10**6 + 7) // 8          # one row per warp, 8 warps per CTA
     g = _policy(bsa, 10**6, 1024, 16, BF)

@@ -1,5 +1,6 @@
-"""The group path (4 lanes per row), the octet path (8 lanes per row) and
-the row path (one warp per row) for topk <= 32, forced with BSA_SELECT_PATH,
+"""The group path (4 lanes per row), the octet path (8 lanes per row), the
+wide path (one warp per row, bf16 calls) and the row path (one warp per row)
+for topk <= 32, forced with BSA_SELECT_PATH,
 against the oracle.  The library reads the variable once per process, so
 each path runs in a child process."""
 import os
@@ -58,7 +59,7 @@ print("ok")
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("path,code", [("group", 2), ("row", 0), ("octet", 4)])
+@pytest.mark.parametrize("path,code", [("group", 2), ("row", 0), ("octet", 4), ("wide", 5)])
 def test_forced_path_matches_oracle(cuda_device, path, code):
     env = dict(os.environ, BSA_SELECT_PATH=path)
     res = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT, code=code)], env=env,

@@ -120,6 +120,7 @@ def test_prefill_heavy_batch_at_full_capacity(cuda_device, dtype, K, L):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     pol = bsa.bsa_select_policy(T * H, M, K, dt, sms)
     assert pol["chunks_per_row"] == 1, "thousands of rows must not take the split path"
+    assert pol["path"] == (bsa.BSA_PATH_WIDE if dtype == torch.bfloat16 else bsa.BSA_PATH_ROW)
     out = bsa.bsa_topk_select(w.scores, nvp, K, 1, L)
     torch.cuda.synchronize()
     _props.check_selection(w.scores, nvp, out, K, 1, L)

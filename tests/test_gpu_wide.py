@@ -1,0 +1,88 @@
+"""The wide path (one warp per row) for bf16 buffers wider than 2 KB with
+topk <= 64, taken by the launch policy when there are at least num_sms * 32
+rows (needs a GB300).  Every row is compared with the oracle element by
+element: ids for the plain select, ids, table and context lengths for the
+fused call.  The rows cover the path's cases:
+  * rows of at most 256 non-forced blocks (every element is a candidate) and
+    longer rows (a threshold from the representatives first);
+  * capacity-wide views whose rows start off a 32-byte boundary (edge chunks
+    inside and at the ends of the buffer);
+  * NaN, +-Inf, +-0 and exact ties; rows of one repeated value, whose
+    candidates overflow the 256-entry list and are redone on the row path;
+  * topk 1, 16, 33 and 64.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_topk_gb300 as bsa
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows_for_wide(dev):
+    return 32 * torch.cuda.get_device_properties(dev).multi_processor_count
+
+
+def _scores(T, H, width, seed, dev):
+    """bf16 N(0, 1) [T, H, width] with specials and ties, and every 97th row
+    one repeated value (ties everywhere)."""
+    sc = synth.normal_scores((T, H, width), torch.bfloat16, seed, dev)
+    synth.inject_specials(sc, seed=seed + 1, frac_each=0.002, frac_ties=0.02)
+    flat = sc.view(T * H, width)
+    flat[::97] = 0.75
+    return sc
+
+
+@pytest.mark.parametrize("K,I,L", [(1, 0, 0), (16, 1, 2), (33, 1, 1), (64, 1, 2)])
+@pytest.mark.parametrize("M,pad", [(2048, 0), (8192, 8), (1500, 5)])
+def test_wide_select_matches_oracle(cuda_device, K, I, L, M, pad):
+    dev = cuda_device
+    H = 2
+    T = (_rows_for_wide(dev) + 255) // H
+    g = np.random.default_rng(M + K + pad)
+    # valid counts: short rows (every element a candidate), rows just past
+    # 256 non-forced blocks, and rows up to the capacity
+    nvp_host = g.integers(0, M + 1, T).astype(np.int32)
+    nvp_host[::5] = g.integers(0, 300, len(nvp_host[::5]))
+    nvp_host[1::11] = 256 + I + L + g.integers(0, 3, len(nvp_host[1::11]))
+    nvp_host[2::13] = M
+    big = _scores(T, H, M + pad, seed=M + K, dev=dev)
+    scores = big[:, :, :M]                       # rows start off 32-byte boundaries when pad > 0
+    nvp = torch.from_numpy(nvp_host).to(dev)
+    synth.fill_tail(scores, nvp, float("-inf"))
+    pol = bsa.bsa_select_policy(T * H, M, K, bsa.BSA_DTYPE_BF16,
+                                torch.cuda.get_device_properties(dev).multi_processor_count)
+    assert pol["path"] == bsa.BSA_PATH_WIDE
+    got = bsa.bsa_topk_select(scores, nvp, K, I, L)
+    torch.cuda.synchronize()
+    want = oracle.topk_select(scores.cpu(), nvp_host, K, I, L)
+    bad = np.nonzero((got.cpu().numpy() != want).any(axis=2))
+    assert bad[0].size == 0, f"{bad[0].size} rows differ, first (t, h) = {bad[0][0]}, {bad[1][0]}"
+
+
+@pytest.mark.parametrize("K", [16, 64])
+def test_wide_fused_table_matches_oracle(cuda_device, K):
+    """Decode rows of a 2048-tile buffer through the fused select + table."""
+    dev = cuda_device
+    dql, H, M = 2, 2, 2048
+    B = (_rows_for_wide(dev) + 255) // (dql * H)
+    g = torch.Generator().manual_seed(K)
+    seq = torch.randint(1, M * 128 + 1, (B,), generator=g, dtype=torch.int32)
+    seq[::9] = 0                                                # padded requests
+    seq[1::7] = torch.randint(1, 300 * 128, (len(seq[1::7]),), generator=g, dtype=torch.int32)
+    table = synth.paged_block_table(B, M, B * M, seed=K + 3)
+    T = B * dql
+    scores = _scores(T, H, M, seed=K + 5, dev=dev)
+    nvp = oracle.num_valid_pages_decode(seq.numpy(), dql)
+    synth.fill_tail(scores, torch.from_numpy(nvp).to(dev), float("-inf"))
+    idx, bt, ctx = bsa.bsa_topk_select_sparse_table(scores, seq.to(dev), dql, K, 1, 2,
+                                                    table.to(dev))
+    torch.cuda.synchronize()
+    want_idx, want_bt, want_ctx = oracle.topk_select_sparse_table(scores.cpu(), seq.numpy(), dql,
+                                                                  K, 1, 2, table.numpy())
+    assert np.array_equal(idx.cpu().numpy(), want_idx)
+    assert np.array_equal(bt.cpu().numpy(), want_bt)
+    assert np.array_equal(ctx.cpu().numpy(), want_ctx)
