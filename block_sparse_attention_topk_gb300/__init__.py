@@ -66,7 +66,8 @@ class LaunchPolicy(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("vecs_per_lane", ctypes.c_int32),
                 ("chunks_per_row", ctypes.c_int32), ("reps_per_lane", ctypes.c_int32),
                 ("warps_per_cta", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("cand_capacity", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
+                ("cand_capacity", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("long_rows", ctypes.c_int32), ("long_grid", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

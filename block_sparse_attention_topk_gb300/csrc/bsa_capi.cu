@@ -51,8 +51,16 @@ size_t split_workspace_bytes(int64_t rows, int32_t chunks, int32_t K) {
            align_up((size_t)rows * 4);
 }
 
+// The list of rows left to the wide path and its counter.
+size_t long_workspace_bytes(int64_t rows) { return align_up((size_t)rows * 4) + kAlign; }
+
+size_t select_workspace_bytes(int64_t rows, const bsa_launch_policy_t& pol, int32_t K) {
+    return pol.long_rows ? long_workspace_bytes(rows)
+                         : split_workspace_bytes(rows, pol.chunks_per_row, K);
+}
+
 SplitWorkspace carve_split_workspace(void* base, int64_t rows, int32_t chunks, int32_t K) {
-    SplitWorkspace ws{nullptr, nullptr, nullptr, nullptr};
+    SplitWorkspace ws{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     if (chunks <= 1 || base == nullptr) return ws;
     const size_t entries = (size_t)rows * chunks * K;
     char* p = static_cast<char*>(base);
@@ -120,6 +128,7 @@ int forced_path() {
 // The launch policy (see bsa_select_policy in the header).
 int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
                 bsa_launch_policy_t* p) {
+    memset(p, 0, sizeof(*p));
     const int vec = dtype == BSA_DTYPE_BF16 ? 8 : 4;
     // Vectors per lane per pass: smallest of 1, 2, 4 covering the capacity.
     int nv = 4;
@@ -149,15 +158,18 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
     const int elem = dtype == BSA_DTYPE_BF16 ? 2 : 4;
     const int forced = forced_path();
     const bool short_rows = M * elem <= kGroupMaxBytes;
-    const bool pair_ok = K <= kGroupMaxK && short_rows;
-    const bool oct_ok = K <= kOctMaxK && short_rows;
-    // Wide path (one warp per row) for bf16 buffers wider than 2 KB with
-    // topk <= 64 wherever the row path would not split rows (with fewer
-    // rows the split path spreads each long row over several warps); any
-    // bf16 buffer when forced.
+    // bf16 buffers wider than 2 KB whose rows are not split: the pair and
+    // octet paths take the rows whose range fits in 2 KB and list the others
+    // for a second, wide-path launch
+    const bool tail = !short_rows && dtype == BSA_DTYPE_BF16 && chunks == 1 &&
+                      cap <= kWideMaxCap;
+    const bool pair_ok = K <= kGroupMaxK && (short_rows || tail);
+    const bool oct_ok = K <= kOctMaxK && (short_rows || tail);
+    const int32_t long_grid = tail ? num_sms * kWideCtasPerSm : 0;
+    // Wide path alone (one warp per row, every row), for bf16 calls with
+    // topk <= 64, when forced.
     const bool wide_ok = dtype == BSA_DTYPE_BF16 && K <= kOctMaxK && cap <= kWideMaxCap;
-    if (wide_ok && (forced == BSA_PATH_WIDE ||
-                    (!short_rows && chunks == 1 && forced != BSA_PATH_ROW))) {
+    if (wide_ok && forced == BSA_PATH_WIDE) {
         int64_t grid = (rows + kWideWarps - 1) / kWideWarps;
         if (grid > INT32_MAX) grid = INT32_MAX;
         if (grid < 1) grid = 1;
@@ -186,6 +198,8 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
         p->grid = (int32_t)grid;
         p->cand_capacity = cap;
         p->smem_bytes = kOctWarps * (int)sizeof(OctSmem);
+        p->long_rows = tail ? 1 : 0;
+        p->long_grid = long_grid;
         return BSA_OK;
     }
     if (pair_ok && forced != BSA_PATH_ROW && forced != BSA_PATH_GROUP) {
@@ -208,6 +222,8 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
         p->grid = (int32_t)grid;
         p->cand_capacity = cap;
         p->smem_bytes = gsmem;
+        p->long_rows = tail ? 1 : 0;
+        p->long_grid = long_grid;
         return BSA_OK;
     }
     if (K <= kGroupMaxK && M * elem <= kGroupMaxBytes && forced != BSA_PATH_ROW) {
@@ -254,11 +270,22 @@ int run_select(SelectArgs& a, void* workspace, size_t workspace_bytes, cudaStrea
     const int64_t rows = a.T * a.H;
     if (rows > INT32_MAX) return BSA_ERR_SHAPE;
     make_policy(rows, a.M, a.K, a.dtype, device_sm_count(), &pol);
-    const size_t need = split_workspace_bytes(rows, pol.chunks_per_row, a.K);
+    const size_t need = select_workspace_bytes(rows, pol, a.K);
     if (need > 0) {
         if (workspace == nullptr || workspace_bytes < need ||
             (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
             return BSA_ERR_WORKSPACE;
+    }
+    if (pol.long_rows) {
+        SplitWorkspace ws{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+        ws.long_list = static_cast<int32_t*>(workspace);
+        ws.long_count = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
+                                                    align_up((size_t)rows * 4));
+        // the list starts empty and untaken on every call (one memset node
+        // in a graph)
+        cudaError_t e = cudaMemsetAsync(ws.long_count, 0, 2 * sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return (int)e;
+        return status_of(launch_select(a, pol, ws, stream));
     }
     SplitWorkspace ws = carve_split_workspace(workspace, rows, pol.chunks_per_row, a.K);
     if (need > 0) {
@@ -307,7 +334,7 @@ size_t bsa_topk_workspace_bytes(int64_t T, int64_t H, int64_t M, int32_t K, int3
     if (dtype != BSA_DTYPE_BF16 && dtype != BSA_DTYPE_FP32) return 0;
     bsa_launch_policy_t pol;
     make_policy(T * H, M, K, dtype, device_sm_count(), &pol);
-    return split_workspace_bytes(T * H, pol.chunks_per_row, K);
+    return select_workspace_bytes(T * H, pol, K);
 }
 
 int bsa_num_valid_pages_decode(const int32_t* seq_lens, int64_t num_reqs, int32_t dql,

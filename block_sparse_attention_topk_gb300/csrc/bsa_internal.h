@@ -110,6 +110,7 @@ struct OctSmem {
 constexpr int kWideCand = 256;       // candidate capacity per row (8 per lane)
 constexpr int kWideWarps = 4;        // warps per CTA, one row each
 constexpr int kWideMaxCap = 320;     // warp-path buffer entries an overflowing row needs (topk <= 64)
+constexpr int kWideCtasPerSm = 6;    // resident CTAs per SM (register bound), for persistent grids
 
 struct WideSmem {
     union {
@@ -180,6 +181,9 @@ struct SplitWorkspace {
     int32_t* ids;       // [rows, chunks, K]
     int32_t* counts;    // [rows, chunks]
     int32_t* tickets;   // [rows]
+    // pair / octet paths with long_rows: the rows left to the wide path
+    int32_t* long_list;     // [rows]
+    uint32_t* long_count;   // [0]: entries in long_list, [1]: entries past the first grid stride taken (zeroed per call)
 };
 
 size_t split_workspace_bytes(int64_t rows, int32_t chunks, int32_t K);

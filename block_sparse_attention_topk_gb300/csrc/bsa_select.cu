@@ -260,6 +260,8 @@ struct Split {
 struct KernelParams {
     SelectArgs a;
     Split ws;
+    int32_t* long_list;       // pair / octet paths: rows left to the wide path, or null
+    uint32_t* long_count;     // [0]: entries in long_list; [1]: entries past the first grid stride taken
     int32_t chunks_per_row;   // work items per row
     int32_t vecs_per_chunk;   // vectors (16 B) per work item
     int32_t cap;              // candidate buffer entries per warp
@@ -1584,7 +1586,12 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         r.all = true;
         if (active) r = row_info_from<FM>(a, row, meta);
         meta = nmeta;
-        const bool need = active && r.need;
+        // a row whose range exceeds 2 KB (a wider buffer) goes to the list of
+        // the second, wide-path launch
+        const bool longr = P.long_list != nullptr && active && r.need &&
+                           (int64_t)(r.hi - r.lo) * S > kGroupMaxBytes;
+        if (longr && s == 0) P.long_list[atomicAdd(P.long_count, 1u)] = (int32_t)row;
+        const bool need = active && r.need && !longr;
 
         // ---- geometry of the non-forced range [lo, hi), 32-byte chunks ----
         const char* row_ptr = nullptr;
@@ -1965,7 +1972,8 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         __syncwarp();
 
         // ---- outputs ----
-        group_write_outputs<2, FM>(P, row, r, r.all, sm.q.sorted[p], s, active && (!need || !ovf));
+        group_write_outputs<2, FM>(P, row, r, r.all, sm.q.sorted[p], s,
+                                   active && !longr && (!need || !ovf));
 
         // ---- rows whose candidates overflowed: the whole warp redoes them ----
         unsigned fb = __ballot_sync(kFull, s == 0 && need && ovf);
@@ -2077,7 +2085,9 @@ __device__ __forceinline__ int32_t oct_theta(uint32_t (&rp)[8], int q) {
     return m;
 }
 
-template <bool BF16, int FM>
+// TAIL: rows over 2 KB are listed for the wide path (buffers wider than
+// 2 KB); without it the kernel has none of that code.
+template <bool BF16, int FM, bool TAIL>
 __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const KernelParams P) {
     using E = Elem<BF16>;
     constexpr int S = E::kBytes;
@@ -2099,7 +2109,11 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
         RowInfo r{};
         r.all = true;
         if (active) r = row_info_from<FM>(a, row, row_meta<FM>(a, row));
-        const bool need = active && r.need;
+        // a row whose range exceeds 2 KB (a wider buffer) goes to the list of
+        // the second, wide-path launch
+        const bool longr = TAIL && active && r.need && (int64_t)(r.hi - r.lo) * S > kGroupMaxBytes;
+        if (longr && q == 0) P.long_list[atomicAdd(P.long_count, 1u)] = (int32_t)row;
+        const bool need = active && r.need && !longr;
 
         // ---- geometry of the non-forced range [lo, hi), 32-byte chunks ----
         const char* row_ptr = nullptr;
@@ -2410,7 +2424,7 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
 
         // ---- step 5: outputs ----
         group_write_outputs<kOctLanes, FM>(P, row, r, r.all, sm.sorted[g], q,
-                                           active && (!need || !ovf));
+                                           active && !longr && (!need || !ovf));
 
         // ---- rows whose candidates overflowed: the whole warp redoes them ----
         unsigned fb = __ballot_sync(kFull, q == 0 && need && ovf);
@@ -2430,7 +2444,13 @@ __global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const K
 
 template <bool BF16>
 cudaError_t launch_octet(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
-    auto kern = P.a.fused ? octet_select_kernel<BF16, kFusedYes> : octet_select_kernel<BF16, kFusedNo>;
+    auto kern = P.a.fused ? octet_select_kernel<BF16, kFusedYes, false>
+                          : octet_select_kernel<BF16, kFusedNo, false>;
+    if constexpr (BF16) {
+        if (P.long_list != nullptr)
+            kern = P.a.fused ? octet_select_kernel<BF16, kFusedYes, true>
+                             : octet_select_kernel<BF16, kFusedNo, true>;
+    }
     if (pol.smem_bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              pol.smem_bytes);
@@ -2483,7 +2503,9 @@ __device__ __forceinline__ int32_t max16(const uint32_t (&w)[NW]) {
     return max((int32_t)(int16_t)(uint16_t)m, (int32_t)(int16_t)(uint16_t)(m >> 16));
 }
 
-template <int FM>
+// LIST: the rows are the long_count entries of long_list (the pair or octet
+// path's long rows) and the grid is persistent; else rows 0 .. P.rows - 1.
+template <int FM, bool LIST>
 __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const KernelParams P) {
     constexpr int CE = 16;                 // bf16 elements per 32-byte chunk
     constexpr int32_t kKeyMin = -32768;
@@ -2493,8 +2515,24 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
     WideSmem& sm = *reinterpret_cast<WideSmem*>(smem_raw + (size_t)warp * sizeof(WideSmem));
     const SelectArgs& a = P.a;
     const int64_t stride = (int64_t)gridDim.x * kWideWarps;
+    const int64_t nrows = LIST ? (int64_t)P.long_count[0] : P.rows;
+    // LIST: after its first row (by position) each warp takes the next
+    // listed row from a second counter, so that rows of unequal length and
+    // late CTAs balance; a list no longer than the grid needs no counter
+    auto next_item = [&](int64_t i) -> int64_t {
+        if constexpr (LIST) {
+            if (nrows <= stride) return nrows;
+            uint32_t n = 0;
+            if (lane == 0) n = atomicAdd(P.long_count + 1, 1u);
+            return stride + (int64_t)__shfl_sync(kFull, n, 0);
+        } else {
+            return i;
+        }
+    };
 
-    for (int64_t row = (int64_t)blockIdx.x * kWideWarps + warp; row < P.rows; row += stride) {
+    for (int64_t i = (int64_t)blockIdx.x * kWideWarps + warp; i < nrows;
+         i = next_item(i + stride)) {
+        const int64_t row = LIST ? (int64_t)P.long_list[i] : i;
         const RowInfo r = row_info_from<FM>(a, row, row_meta<FM>(a, row));
         if (!r.need) {
             write_outputs(P, row, r.t, r.h, r.n, r.lo, r.hi, r.kp, r.all, sm.c.sorted,
@@ -2697,8 +2735,18 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
 }
 
 cudaError_t launch_wide(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
-    auto kern = P.a.fused ? wide_select_kernel<kFusedYes> : wide_select_kernel<kFusedNo>;
+    auto kern = P.a.fused ? wide_select_kernel<kFusedYes, false> : wide_select_kernel<kFusedNo, false>;
     kern<<<pol.grid, kWideWarps * 32, pol.smem_bytes, st>>>(P);
+    return cudaGetLastError();
+}
+
+// The second launch of a pair / octet call with long_rows: the listed rows.
+cudaError_t launch_wide_list(const KernelParams& P, const bsa_launch_policy_t& pol,
+                             cudaStream_t st) {
+    if (P.a.dtype != BSA_DTYPE_BF16 || P.cap > kWideMaxCap || pol.long_grid < 1)
+        return cudaErrorInvalidValue;
+    auto kern = P.a.fused ? wide_select_kernel<kFusedYes, true> : wide_select_kernel<kFusedNo, true>;
+    kern<<<pol.long_grid, kWideWarps * 32, kWideWarps * (int)sizeof(WideSmem), st>>>(P);
     return cudaGetLastError();
 }
 
@@ -3067,6 +3115,8 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
     div_magic((uint32_t)(a.H > 0 ? a.H : 1), &P.a.h_mul, &P.a.h_shift);
     div_magic((uint32_t)(a.dql > 0 ? a.dql : 1), &P.a.dql_mul, &P.a.dql_shift);
     P.ws = Split{ws.keys, ws.ids, ws.counts, ws.tickets};
+    P.long_list = nullptr;
+    P.long_count = nullptr;
     P.chunks_per_row = pol.chunks_per_row;
     P.cap = pol.cand_capacity;
     P.rows = a.T * a.H;
@@ -3084,6 +3134,18 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
     if (pol.path == BSA_PATH_GROUP)
         return a.dtype == BSA_DTYPE_BF16 ? launch_group<true>(P, pol, stream)
                                          : launch_group<false>(P, pol, stream);
+    if (pol.long_rows) {
+        // rows over 2 KB: listed by the pair / octet kernel, then the wide path
+        if (ws.long_list == nullptr || ws.long_count == nullptr || a.dtype != BSA_DTYPE_BF16 ||
+            (pol.path != BSA_PATH_PAIR && pol.path != BSA_PATH_OCTET))
+            return cudaErrorInvalidValue;
+        P.long_list = ws.long_list;
+        P.long_count = ws.long_count;
+        const cudaError_t e = pol.path == BSA_PATH_PAIR ? launch_pair<true>(P, pol, stream)
+                                                        : launch_octet<true>(P, pol, stream);
+        if (e != cudaSuccess) return e;
+        return launch_wide_list(P, pol, stream);
+    }
     if (pol.path == BSA_PATH_PAIR)
         return a.dtype == BSA_DTYPE_BF16 ? launch_pair<true>(P, pol, stream)
                                          : launch_pair<false>(P, pol, stream);
@@ -3107,6 +3169,8 @@ cudaError_t launch_index_score_select(const SelectArgs& a, const uint16_t* q, co
     div_magic((uint32_t)(a.H > 0 ? a.H : 1), &P.a.h_mul, &P.a.h_shift);
     div_magic((uint32_t)(a.dql > 0 ? a.dql : 1), &P.a.dql_mul, &P.a.dql_shift);
     P.ws = Split{nullptr, nullptr, nullptr, nullptr};
+    P.long_list = nullptr;
+    P.long_count = nullptr;
     P.chunks_per_row = 1;
     // the warp path with 4 fp32 vectors per lane per pass
     P.cap = (a.K + 32 * 4 + 31) / 32 * 32;

@@ -89,6 +89,9 @@ typedef struct bsa_launch_policy {
     int32_t grid;             /* CTAs launched                                */
     int32_t cand_capacity;    /* candidate buffer entries per warp            */
     int32_t smem_bytes;       /* dynamic shared memory per CTA                */
+    int32_t long_rows;        /* 1: rows whose range exceeds 2 KB are left to a
+                                 second, wide-path launch over a list of them */
+    int32_t long_grid;        /* CTAs of that launch (0 when long_rows is 0)  */
 } bsa_launch_policy_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -119,8 +122,10 @@ int bsa_num_valid_pages_varlen(const int32_t* cu_seqlens_q, const int32_t* prefi
 
 /* Bytes of device workspace bsa_topk_select / bsa_topk_select_sparse_table
  * need for these sizes on the current device (0 when the launch policy keeps
- * every row in one warp).  The workspace holds the per-chunk candidate lists
- * and the merge tickets of the split path.  Host-only; launches nothing. */
+ * every row in one warp and leaves none to a second launch).  The workspace
+ * holds the per-chunk candidate lists and the merge tickets of the split
+ * path, or the list of rows longer than 2 KB and its counter (long_rows in
+ * the policy).  Host-only; launches nothing. */
 size_t bsa_topk_workspace_bytes(int64_t T, int64_t H, int64_t M, int32_t K, int32_t dtype);
 
 /* Batched causal top-k over the unified token-major score buffer
@@ -290,13 +295,16 @@ int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_t T, int64_
  * Paths: BSA_PATH_PAIR when K <= 32 and a row holds at most 2 KB (M * element
  * size <= 2048), BSA_PATH_OCTET when 32 < K <= 64 and a row holds at most
  * 2 KB; BSA_PATH_SPLIT when a row needs more than one pass and the rows
- * alone cannot fill the GPU (at most num_sms * 16 rows); otherwise
- * BSA_PATH_WIDE for bf16 rows of more than 2 KB (M > 1024, up to the
- * 8192-tile capture-time capacity and beyond) with K <= 64, and
- * BSA_PATH_ROW for the rest.  The
+ * alone cannot fill the GPU (at most num_sms * 16 rows); otherwise, for bf16
+ * rows of more than 2 KB (M > 1024, up to the 8192-tile capture-time
+ * capacity and beyond) with K <= 64, BSA_PATH_PAIR or BSA_PATH_OCTET with
+ * long_rows = 1: those paths take every row whose non-forced range fits in
+ * 2 KB and list the others, which a second launch on the same stream takes
+ * with the wide path (one warp per row); BSA_PATH_ROW for the rest.  The
  * environment variable BSA_SELECT_PATH=row|group|pair|octet|wide, read once
  * per process, forces a path among those that can serve the call, for
- * testing (BSA_PATH_GROUP is reachable only that way).
+ * testing (BSA_PATH_GROUP is reachable only that way; BSA_PATH_WIDE alone
+ * takes every row with one warp).
  * Errors: BSA_ERR_NULL, BSA_ERR_SHAPE, BSA_ERR_TOPK, BSA_ERR_DTYPE. */
 int bsa_select_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_sms,
                       bsa_launch_policy_t* policy);

@@ -1,14 +1,17 @@
-"""The wide path (one warp per row) for bf16 buffers wider than 2 KB with
-topk <= 64, taken by the launch policy when there are at least num_sms * 32
-rows (needs a GB300).  Every row is compared with the oracle element by
-element: ids for the plain select, ids, table and context lengths for the
-fused call.  The rows cover the path's cases:
+"""bf16 buffers wider than 2 KB with topk <= 64 and more than num_sms * 16
+rows (needs a GB300): the launch policy sends them to the pair or octet path,
+which takes every row whose non-forced range fits in 2 KB and lists the
+others for a second launch, the wide path (one warp per row).  Every row is
+compared with the oracle element by element: ids for the plain select, ids,
+table and context lengths for the fused call; a graph replay and the
+allocation-free entry point run the same two launches.  The rows cover:
   * rows of at most 256 non-forced blocks (every element is a candidate) and
     longer rows (a threshold from the representatives first);
   * capacity-wide views whose rows start off a 32-byte boundary (edge chunks
     inside and at the ends of the buffer);
   * NaN, +-Inf, +-0 and exact ties; rows of one repeated value, whose
     candidates overflow the 256-entry list and are redone on the row path;
+  * rows that fit in 2 KB (pair / octet path) and longer ones (wide path);
   * topk 1, 16, 33 and 64.
 """
 import numpy as np
@@ -55,7 +58,7 @@ def test_wide_select_matches_oracle(cuda_device, K, I, L, M, pad):
     synth.fill_tail(scores, nvp, float("-inf"))
     pol = bsa.bsa_select_policy(T * H, M, K, bsa.BSA_DTYPE_BF16,
                                 torch.cuda.get_device_properties(dev).multi_processor_count)
-    assert pol["path"] == bsa.BSA_PATH_WIDE
+    assert pol["path"] in (bsa.BSA_PATH_PAIR, bsa.BSA_PATH_OCTET) and pol["long_rows"] == 1
     got = bsa.bsa_topk_select(scores, nvp, K, I, L)
     torch.cuda.synchronize()
     want = oracle.topk_select(scores.cpu(), nvp_host, K, I, L)
@@ -86,3 +89,41 @@ def test_wide_fused_table_matches_oracle(cuda_device, K):
     assert np.array_equal(idx.cpu().numpy(), want_idx)
     assert np.array_equal(bt.cpu().numpy(), want_bt)
     assert np.array_equal(ctx.cpu().numpy(), want_ctx)
+
+
+def test_long_rows_graph_replay_and_noalloc(cuda_device):
+    """The memset of the list counter and the two launches replay in a CUDA
+    graph (twice, with new scores in between), and the allocation-free entry
+    point takes the list from its scratch."""
+    dev = cuda_device
+    H, M, K = 2, 4096, 16
+    T = (_rows_for_wide(dev) + 511) // H
+    g = np.random.default_rng(5)
+    nvp_host = g.integers(0, M + 1, T).astype(np.int32)
+    nvp_host[::3] = g.integers(0, 1000, len(nvp_host[::3]))
+    nvp = torch.from_numpy(nvp_host).to(dev)
+    scores = _scores(T, H, M, seed=41, dev=dev)
+    synth.fill_tail(scores, nvp, float("-inf"))
+    out = torch.empty((T, H, K), dtype=torch.int32, device=dev)
+    ws = torch.empty(bsa.bsa_topk_workspace_bytes(T, H, M, K, bsa.BSA_DTYPE_BF16, dev),
+                     dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        bsa.bsa_topk_select(scores, nvp, K, 1, 2, out_idx=out, workspace=ws)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        bsa.bsa_topk_select(scores, nvp, K, 1, 2, out_idx=out, workspace=ws)
+    for seed in (42, 43):
+        scores.copy_(_scores(T, H, M, seed=seed, dev=dev))
+        synth.fill_tail(scores, nvp, float("-inf"))
+        out.fill_(-7)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        want = oracle.topk_select(scores.cpu(), nvp_host, K, 1, 2)
+        assert np.array_equal(out.cpu().numpy(), want), f"graph replay, scores seed {seed}"
+    got = bsa.bsa_topk_select_noalloc(scores, nvp, K, 1, 2)
+    torch.cuda.synchronize(dev)
+    assert np.array_equal(got.cpu().numpy(), want), "allocation-free entry point"
