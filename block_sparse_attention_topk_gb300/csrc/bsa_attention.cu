@@ -22,9 +22,11 @@
 // lane scores one token against every query head (reading the token's key
 // row as 16-byte vectors), the warp folds the tile into a running maximum
 // and sum per head (online softmax, Milakov and Gimelshein, "Online
-// normalizer calculation for softmax", 2018), and then the lanes, each
-// owning D / 32 output dimensions, accumulate the tile's value rows (one
-// coalesced row per token) weighted by the broadcast probabilities.  The
+// normalizer calculation for softmax", 2018), and then the lanes accumulate
+// the tile's value rows weighted by the broadcast probabilities: each lane
+// owns 4 (D = 64, 128) or D / 32 dimensions of one token of a warp-wide
+// load, so that a load covers two tokens' rows at D = 64 (8 bytes per lane)
+// and one row above; the tile's two page ids are read once.  The
 // warps' partial maxima, sums and outputs then merge in shared memory (each
 // rescaled by exp(its maximum - the overall maximum)).  Decode attention
 // moves each key and value once and does O(G) flops per element, so it is
@@ -98,10 +100,21 @@ __device__ __forceinline__ void load_dl(const uint16_t* p, float (&f)[DL]) {
 // GP >= G query heads (a power of two), DL = D / 32 dimensions per lane.
 // Shared memory: queries [GP][D], then per warp its partial maxima [GP],
 // sums [GP] and outputs [GP][D].
+// Resident CTAs per SM the register bound asks for: 4 where the lane's
+// accumulators are small (a decode batch is often a single wave of CTAs, so
+// occupancy decides), 2 for 8 query heads of wide dimensions.
+constexpr int attn_ctas(int gp, int dl) { return gp * (dl < 4 ? 4 : dl) <= 16 ? 4 : 2; }
+
 template <int GP, int DL>
-__global__ void __launch_bounds__(kAttnWarps * 32)
+__global__ void __launch_bounds__(kAttnWarps * 32, attn_ctas(GP, DL))
 sparse_decode_attention_kernel(const AttnParams A) {
     constexpr int D = 32 * DL;
+    // value phase: each lane owns VD dimensions of one token of a load; a
+    // load covers TPL tokens (D = 64: two tokens, 8 bytes per lane)
+    constexpr int VD = DL < 4 ? 4 : DL;
+    constexpr int LPT = D / VD;            // lanes per token
+    constexpr int TPL = 32 / LPT;          // tokens per warp-wide load
+    constexpr int VB = VD >= 8 ? 2 : 4;    // value loads in flight per lane
     extern __shared__ __align__(16) float smem[];
     float* qs = smem;
     float* pm = qs + GP * D;
@@ -109,8 +122,11 @@ sparse_decode_attention_kernel(const AttnParams A) {
     float* pacc = pl + kAttnWarps * GP;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int sub = lane / LPT;            // the lane's token within a load
+    const int d0 = (lane % LPT) * VD;      // its first value dimension
     const int G = A.G;
     const int cap = A.width * BSA_SUB_PAGE_SIZE;
+    const int64_t slot_stride = (int64_t)A.H * D;   // elements between slots of a page
     for (int64_t row = blockIdx.x; row < A.rows; row += gridDim.x) {
         const int h = (int)(row % A.H);
         const int32_t* bt = A.bt + row * A.width;
@@ -122,26 +138,32 @@ sparse_decode_attention_kernel(const AttnParams A) {
         for (int i = threadIdx.x; i < G * D; i += kAttnWarps * 32)
             qs[i] = __uint_as_float((uint32_t)__ldg(qrow + i) << 16);
         __syncthreads();
-        float m[GP], l[GP], acc[GP][DL];
+        float m[GP], l[GP], acc[GP][VD];
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
             m[g] = -INFINITY;
             l[g] = 0.f;
 #pragma unroll
-            for (int d = 0; d < DL; ++d) acc[g][d] = 0.f;
+            for (int d = 0; d < VD; ++d) acc[g][d] = 0.f;
         }
         for (int tile = 32 * warp; tile < ctx; tile += 32 * kAttnWarps) {
+            // the tile's two pages (tokens tile .. tile + 15 and tile + 16 .. tile + 31)
+            const int32_t pa = __ldg(bt + (tile >> 4));
+            const int32_t pb = tile + 16 < ctx ? __ldg(bt + (tile >> 4) + 1) : -1;
+            const bool oka = pa >= 0 && pa < A.num_pages;
+            const bool okb = pb >= 0 && pb < A.num_pages;
+            report_status(A.status, lane == 0 && (!oka || (tile + 16 < ctx && !okb)),
+                          BSA_STATUS_BAD_PAGE);
             // ---- scores: lane j of the tile takes token tile + j ----
             const int j = tile + lane;
-            const int32_t page = j < ctx ? __ldg(bt + (j >> 4)) : -1;
-            const bool ok = page >= 0 && page < A.num_pages;
-            report_status(A.status, j < ctx && !ok, BSA_STATUS_BAD_PAGE);
+            const int32_t page = lane < 16 ? pa : pb;
+            const bool ok = j < ctx && (lane < 16 ? oka : okb);
             float s[GP];
 #pragma unroll
             for (int g = 0; g < GP; ++g) s[g] = 0.f;
             if (ok) {
                 const uint4* kr = reinterpret_cast<const uint4*>(
-                    A.k + (((int64_t)page * BSA_SUB_PAGE_SIZE + (j & 15)) * A.H + h) * D);
+                    A.k + ((int64_t)page * BSA_SUB_PAGE_SIZE + (lane & 15)) * slot_stride + (int64_t)h * D);
 #pragma unroll 8
                 for (int c = 0; c < D / 8; ++c) {
                     const uint4 kv = __ldg(kr + c);
@@ -177,39 +199,48 @@ sparse_decode_attention_kernel(const AttnParams A) {
                 p[g] = ok ? expf(sg - mn) : 0.f;
                 l[g] = l[g] * corr + warp_sum(p[g]);
 #pragma unroll
-                for (int d = 0; d < DL; ++d) acc[g][d] *= corr;
+                for (int d = 0; d < VD; ++d) acc[g][d] *= corr;
                 m[g] = mn;
             }
-            // ---- values: the lane owns dimensions [lane * DL, lane * DL + DL);
-            // VB value rows are loaded before any of them is used ----
-            constexpr int VB = DL >= 8 ? 2 : 16 / DL;
-            const int nt = min(32, ctx - tile);
-            for (int j0 = 0; j0 < nt; j0 += VB) {
-                float vf[VB][DL];
+            // ---- values: lane (sub, d0) takes tokens sub, sub + TPL, ... of
+            // the tile, dimensions [d0, d0 + VD); VB rows are loaded before
+            // any of them is used ----
+            const uint16_t* va = A.v + (int64_t)pa * BSA_SUB_PAGE_SIZE * slot_stride + (int64_t)h * D + d0;
+            const uint16_t* vb = A.v + (int64_t)pb * BSA_SUB_PAGE_SIZE * slot_stride + (int64_t)h * D + d0;
 #pragma unroll
-                for (int u = 0; u < VB; ++u) {
-                    const int jt = tile + j0 + u;
-                    const int32_t pg = j0 + u < nt ? __ldg(bt + (jt >> 4)) : -1;
-                    if (pg >= 0 && pg < A.num_pages) {
-                        load_dl<DL>(A.v + (((int64_t)pg * BSA_SUB_PAGE_SIZE + (jt & 15)) * A.H + h) * D +
-                                        lane * DL,
-                                    vf[u]);
+            for (int i0 = 0; i0 < 32 / TPL; i0 += VB) {
+                float vf[VB][VD];
+#pragma unroll
+                for (int v = 0; v < VB; ++v) {
+                    const int u = sub + TPL * (i0 + v);
+                    const bool use = tile + u < ctx && (u < 16 ? oka : okb);
+                    if (use) {
+                        load_dl<VD>((u < 16 ? va : vb) + (int64_t)(u & 15) * slot_stride, vf[v]);
                     } else {
 #pragma unroll
-                        for (int d = 0; d < DL; ++d) vf[u][d] = 0.f;
+                        for (int d = 0; d < VD; ++d) vf[v][d] = 0.f;
                     }
                 }
                 // tokens past the context or on unusable pages have p = 0
 #pragma unroll
-                for (int u = 0; u < VB; ++u) {
+                for (int v = 0; v < VB; ++v) {
+                    const int u = sub + TPL * (i0 + v);
 #pragma unroll
                     for (int g = 0; g < GP; ++g) {
-                        const float pj = __shfl_sync(kFull, p[g], (j0 + u) & 31);
+                        const float pj = __shfl_sync(kFull, p[g], u);
 #pragma unroll
-                        for (int d = 0; d < DL; ++d) acc[g][d] = fmaf(pj, vf[u][d], acc[g][d]);
+                        for (int d = 0; d < VD; ++d) acc[g][d] = fmaf(pj, vf[v][d], acc[g][d]);
                     }
                 }
             }
+        }
+        // the lanes that share dimensions (one per token of a load) add up
+#pragma unroll
+        for (int t = LPT; t < 32; t <<= 1) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g)
+#pragma unroll
+                for (int d = 0; d < VD; ++d) acc[g][d] += __shfl_xor_sync(kFull, acc[g][d], t);
         }
         // ---- merge the warps' partial results ----
 #pragma unroll
@@ -218,8 +249,10 @@ sparse_decode_attention_kernel(const AttnParams A) {
                 pm[warp * GP + g] = m[g];
                 pl[warp * GP + g] = l[g];
             }
+            if (sub == 0) {
 #pragma unroll
-            for (int d = 0; d < DL; ++d) pacc[(warp * GP + g) * D + lane * DL + d] = acc[g][d];
+                for (int d = 0; d < VD; ++d) pacc[(warp * GP + g) * D + d0 + d] = acc[g][d];
+            }
         }
         __syncthreads();
         float* orow = A.out + row * (int64_t)G * D;
