@@ -177,3 +177,32 @@ def test_graph_keeps_the_word_registered_at_capture(cuda_device, word):
     g.replay()
     torch.cuda.synchronize(dev)
     assert int(word.item()) == bsa.BSA_STATUS_BAD_BLOCK_ID
+
+
+def test_long_rows_report_bad_block_ids(cuda_device, word):
+    """A 2048-tile buffer with enough rows for the pair path and its list of
+    long rows: a -1 entry for block 0 of requests whose rows exceed 2 KB is
+    reported by the wide path's table epilogue, and the outputs match the
+    oracle."""
+    dev = cuda_device
+    dql, H, M, K = 1, 2, 2048, 16
+    B = (32 * torch.cuda.get_device_properties(dev).multi_processor_count + 255) // H
+    g = torch.Generator().manual_seed(3)
+    seq = torch.randint(1, M * 128 + 1, (B,), generator=g, dtype=torch.int32)
+    table = synth.paged_block_table(B, M, B * M, seed=4)
+    long_req = torch.nonzero(seq > 1100 * 128).flatten()[:40]
+    table[long_req, 0] = -1
+    scores = synth.normal_scores((B * dql, H, M), torch.bfloat16, seed=5, device=dev)
+    nvp = oracle.num_valid_pages_decode(seq.numpy(), dql)
+    synth.fill_tail(scores, torch.from_numpy(nvp).to(dev), float("-inf"))
+    pol = bsa.bsa_select_policy(B * dql * H, M, K, bsa.BSA_DTYPE_BF16,
+                                torch.cuda.get_device_properties(dev).multi_processor_count)
+    assert pol["long_rows"] == 1
+    idx, bt, ctx = bsa.bsa_topk_select_sparse_table(scores, seq.to(dev), dql, K, 1, 2,
+                                                    table.to(dev))
+    assert bsa.bsa_read_status() == bsa.BSA_STATUS_BAD_BLOCK_ID
+    want_idx, want_bt, want_ctx = oracle.topk_select_sparse_table(scores.cpu(), seq.numpy(), dql,
+                                                                  K, 1, 2, table.numpy())
+    assert np.array_equal(idx.cpu().numpy(), want_idx)
+    assert np.array_equal(bt.cpu().numpy(), want_bt)
+    assert np.array_equal(ctx.cpu().numpy(), want_ctx)
