@@ -111,6 +111,7 @@ constexpr int kWideCand = 256;       // candidate capacity per row (8 per lane)
 constexpr int kWideWarps = 4;        // warps per CTA, one row each
 constexpr int kWideMaxCap = 320;     // warp-path buffer entries an overflowing row needs (topk <= 64)
 constexpr int kWideCtasPerSm = 6;    // resident CTAs per SM (register bound), for persistent grids
+constexpr int kWideHotChunks = 1024; // rows of up to 32 KB keep their chunk maxima for pass 2
 
 struct WideSmem {
     union {
@@ -122,6 +123,8 @@ struct WideSmem {
         uint32_t fallback[2 * kWideMaxCap];  // the warp path's keys and ids
     };
     uint32_t scratch[32][8];              // one 32-byte chunk per lane while candidates are read out
+    int16_t cmax[kWideHotChunks];         // raw maximum of each interior chunk (pass 1)
+    uint16_t hot[kWideHotChunks];         // the chunks pass 2 reads, ascending
 };
 
 // Everything one selector launch needs.  Pointers are device pointers.

@@ -2575,7 +2575,13 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
                     rmn[x] = min_s16x2(rmn[x], w[x]);
                 }
             };
-            // interior chunks 1 .. nchunk - 2; the edge chunks are left out
+            // interior chunks 1 .. nchunk - 2; the edge chunks are left out.
+            // Rows of up to kWideHotChunks chunks also keep each chunk's raw
+            // maximum, so that pass 2 reads only the chunks that reach theta.
+            const bool track = nchunk <= kWideHotChunks;
+            auto note = [&](int k, const uint32_t (&w)[8]) {
+                if (track) sm.cmax[k] = (int16_t)max16(w);
+            };
             const int klast = nchunk - 2;
             int k = lane == 0 ? 32 : lane;
             const bool any_interior = k <= klast;
@@ -2585,11 +2591,14 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
                 ld32(c0 + ((uintptr_t)(k + 32) << 5), w1);
                 fold(w0);
                 fold(w1);
+                note(k, w0);
+                note(k + 32, w1);
             }
             if (k <= klast) {
                 uint32_t w0[8];
                 ld32(c0 + ((uintptr_t)k << 5), w0);
                 fold(w0);
+                note(k, w0);
             }
             uint32_t rp[8];
 #pragma unroll
@@ -2613,7 +2622,25 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
 
         // ---- step 3: candidates >= theta, in id order ----
         const bool raw_ok = theta >= 0;   // raw signed order is key order against it
-        const int steps = (nchunk + 31) >> 5;
+        // the chunks to read: with theta >= 0 and the chunk maxima kept, the
+        // edge chunks and the interior chunks whose raw maximum reaches theta
+        // (raw order is key order against a non-negative theta), ascending
+        const bool use_hot = raw_ok && r.hi - r.lo > kWideCand && nchunk <= kWideHotChunks;
+        int nread = nchunk;
+        if (use_hot) {
+            int tot = 0;
+            for (int b0 = 0; b0 < nchunk; b0 += 32) {
+                const int k = b0 + lane;
+                const bool hot = k < nchunk && (k == 0 || k == nchunk - 1 || sm.cmax[k] >= theta);
+                const unsigned hb = __ballot_sync(kFull, hot);
+                if (hot) sm.hot[tot + __popc(hb & lanemask_lt())] = (uint16_t)k;
+                tot += __popc(hb);
+            }
+            nread = tot;
+            __syncwarp();
+        }
+        auto chunk_at = [&](int i) { return use_hot ? (int)sm.hot[i] : i; };
+        const int steps = (nread + 31) >> 5;
         int cbase = 0;
         auto plain = [&](int k) {
             const uintptr_t addr = c0 + ((uintptr_t)k << 5);
@@ -2621,13 +2648,16 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
         };
         uint32_t nx[8];
         auto issue = [&](int st) {
-            const int k = lane + 32 * st;
-            if (k < nchunk && plain(k)) ld32(c0 + ((uintptr_t)k << 5), nx);
+            const int i = lane + 32 * st;
+            if (i < nread) {
+                const int k = chunk_at(i);
+                if (plain(k)) ld32(c0 + ((uintptr_t)k << 5), nx);
+            }
         };
         issue(0);
         for (int st = 0; st < steps; ++st) {
-            const int k = lane + 32 * st;
-            const bool has = k < nchunk;
+            const bool has = lane + 32 * st < nread;
+            const int k = has ? chunk_at(lane + 32 * st) : 0;
             uint32_t w[8];
             uint32_t m = 0;
             if (has) {
