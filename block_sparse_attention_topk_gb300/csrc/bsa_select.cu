@@ -2469,9 +2469,10 @@ cudaError_t launch_octet(const KernelParams& P, const bsa_launch_policy_t& pol, 
 //     maximum and minimum: 16 representatives per lane, 512 per row, each
 //     the largest key of a distinct set of elements; the row is asked into
 //     L2 first, 4 KB per lane;
-//  2. theta: a binary search over the representatives' counts, stopped when
-//     the interval is 16 keys wide, gives a bound that at least K' of them,
-//     so at least K' elements, reach;
+//  2. theta: for K' <= 32 the K'-th largest of the lanes' largest
+//     representatives (a bitonic sort across the warp), else a binary
+//     search over the representatives' counts stopped at a 16-key interval:
+//     a bound that at least K' representatives, so K' elements, reach;
 //  3. the chunks are read again (L2 hits, the next chunk in flight) and the
 //     elements >= theta are appended to a 256-entry list in id order, placed
 //     by a warp-wide scan; rows of at most 256 non-forced blocks skip steps
@@ -2609,15 +2610,33 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
                 rp[x] = any_interior ? (rmx[x] & ~mneg) | ((rmn[x] ^ 0x7FFF7FFFu) & mneg)
                                      : 0x80008000u;
             }
-            // count(>= lo) >= kp throughout (every representative counts at
-            // the smallest key); stop at a 16-key interval
-            int32_t lo = kKeyMin, hi = __reduce_max_sync(kFull, max16(rp)) + 1;
-            while (hi - lo > 16) {
-                const int32_t mid = (lo + hi) >> 1;
-                if ((int)__reduce_add_sync(kFull, (unsigned)count_ge16(rp, mid)) >= kp) lo = mid;
-                else hi = mid;
+            if (kp <= 32) {
+                // the kp-th largest of the lanes' largest representatives
+                // (a bitonic sort across the warp, descending): kp lanes each
+                // hold a representative at or above it
+                int32_t v = max16(rp);
+#pragma unroll
+                for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+                    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+                        const int32_t o = __shfl_xor_sync(kFull, v, jj);
+                        const bool desc = (lane & kk) == 0;
+                        const bool lower = (lane & jj) == 0;
+                        v = (lower == desc) ? max(v, o) : min(v, o);
+                    }
+                }
+                theta = __shfl_sync(kFull, v, kp - 1);
+            } else {
+                // count(>= lo) >= kp throughout (every representative counts
+                // at the smallest key); stop at a 16-key interval
+                int32_t lo = kKeyMin, hi = __reduce_max_sync(kFull, max16(rp)) + 1;
+                while (hi - lo > 16) {
+                    const int32_t mid = (lo + hi) >> 1;
+                    if ((int)__reduce_add_sync(kFull, (unsigned)count_ge16(rp, mid)) >= kp) lo = mid;
+                    else hi = mid;
+                }
+                theta = lo;
             }
-            theta = lo;
         }
 
         // ---- step 3: candidates >= theta, in id order ----
