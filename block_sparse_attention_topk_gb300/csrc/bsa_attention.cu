@@ -152,6 +152,13 @@ sparse_decode_attention_kernel(const AttnParams A) {
             const int32_t pb = tile + 16 < ctx ? __ldg(bt + (tile >> 4) + 1) : -1;
             const bool oka = pa >= 0 && pa < A.num_pages;
             const bool okb = pb >= 0 && pb < A.num_pages;
+            // the tile's value pages towards L2 while the scores are formed
+            if (lane < 2 && (lane == 0 ? oka : okb)) {
+                const int64_t pg = lane == 0 ? pa : pb;
+                const uint16_t* vp = A.v + pg * BSA_SUB_PAGE_SIZE * slot_stride;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vp),
+                             "r"((uint32_t)(BSA_SUB_PAGE_SIZE * slot_stride * 2)) : "memory");
+            }
             report_status(A.status, lane == 0 && (!oka || (tile + 16 < ctx && !okb)),
                           BSA_STATUS_BAD_PAGE);
             // ---- scores: lane j of the tile takes token tile + j ----
