@@ -14,8 +14,8 @@
 // ("Support speculative decode with AITER sparse PA", 实现拆解 items 1 and 3)
 // and of the EMIT_SPARSE_TABLE flag in PR #55235.
 //
-// How (a design for this GPU, not the pages' Triton/ROCm kernels).  Three
-// kernels share one method:
+// How (a design for this GPU, not the pages' Triton/ROCm kernels).  The
+// selector kernels share one method:
 //  * Threshold.  Representatives (maxima of disjoint element subsets) give a
 //    lower bound theta on the K'-th best non-forced score: K' distinct
 //    elements reach the K'-th largest representative.  Only elements >= theta
@@ -32,8 +32,17 @@
 //    chunk maxima select the hot chunks, which are reloaded (L2 hits) and
 //    filtered; bitonic networks across the lane pair sort representatives and
 //    candidates.  Rows whose candidates overflow are redone by the warp path.
-//  * group_select_kernel: the same with 4 lanes per row, 8 rows per warp
-//    (selectable for testing).
+//  * octet_select_kernel (default for 32 < topk <= 64 and rows <= 2 KB): 8
+//    lanes per row, 4 rows per warp; position maxima as representatives,
+//    packed sorting networks for theta, an id-ordered candidate list and an
+//    exact kappa search.
+//  * wide_select_kernel (bf16 rows over 2 KB, topk <= 64): the octet method
+//    with all 32 lanes on one row, and a list of the chunks that reach
+//    theta.  On a buffer wider than 2 KB (the 8192-tile capture-time
+//    capacity) the pair and octet kernels take every row whose range fits in
+//    2 KB and list the others, which a second launch takes with this kernel.
+//  * group_select_kernel: the pair method with 4 lanes per row, 8 rows per
+//    warp (selectable for testing).
 //  * select_kernel (warp path): one warp per row, or per chunk of a long row
 //    when there are too few rows to fill the GPU (split path).  Candidates
 //    are appended in id order to a per-warp shared buffer compacted by an
@@ -45,6 +54,8 @@
 //    warp.
 //  * The fused variant of every kernel gathers block_table[req, b] for the
 //    selected blocks and writes their page-16 entries and ctx in the same pass.
+//  * index_score_select_kernel (further down) computes decode index scores
+//    into the unified buffer and selects from them in the same launch.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
