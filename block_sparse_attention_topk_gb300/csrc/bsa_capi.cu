@@ -158,17 +158,16 @@ int make_policy(int64_t rows, int64_t M, int32_t K, int32_t dtype, int32_t num_s
     const int elem = dtype == BSA_DTYPE_BF16 ? 2 : 4;
     const int forced = forced_path();
     const bool short_rows = M * elem <= kGroupMaxBytes;
-    // bf16 buffers wider than 2 KB whose rows are not split: the pair and
-    // octet paths take the rows whose range fits in 2 KB and list the others
-    // for a second, wide-path launch
-    const bool tail = !short_rows && dtype == BSA_DTYPE_BF16 && chunks == 1 &&
-                      cap <= kWideMaxCap;
+    // buffers wider than 2 KB whose rows are not split: the pair and octet
+    // paths take the rows whose range fits in 2 KB and list the others for a
+    // second, wide-path launch
+    const bool tail = !short_rows && chunks == 1 && cap <= kWideMaxCap;
     const bool pair_ok = K <= kGroupMaxK && (short_rows || tail);
     const bool oct_ok = K <= kOctMaxK && (short_rows || tail);
     const int32_t long_grid = tail ? num_sms * kWideCtasPerSm : 0;
-    // Wide path alone (one warp per row, every row), for bf16 calls with
-    // topk <= 64, when forced.
-    const bool wide_ok = dtype == BSA_DTYPE_BF16 && K <= kOctMaxK && cap <= kWideMaxCap;
+    // Wide path alone (one warp per row, every row), for calls with topk <=
+    // 64, when forced.
+    const bool wide_ok = K <= kOctMaxK && cap <= kWideMaxCap;
     if (wide_ok && forced == BSA_PATH_WIDE) {
         int64_t grid = (rows + kWideWarps - 1) / kWideWarps;
         if (grid > INT32_MAX) grid = INT32_MAX;

@@ -105,8 +105,8 @@ struct OctSmem {
     uint32_t scratch[32][8];            // one 32-byte chunk per lane while candidates are read out
 };
 
-// Wide path: one warp per row, for bf16 rows longer than 2 KB and topk <= 64
-// (see bsa_select.cu).
+// Wide path: one warp per row, for rows longer than 2 KB and topk <= 64 (see
+// bsa_select.cu).
 constexpr int kWideCand = 256;       // candidate capacity per row (8 per lane)
 constexpr int kWideWarps = 4;        // warps per CTA, one row each
 constexpr int kWideMaxCap = 320;     // warp-path buffer entries an overflowing row needs (topk <= 64)
@@ -116,14 +116,17 @@ constexpr int kWideHotChunks = 1024; // rows of up to 32 KB keep their chunk max
 struct WideSmem {
     union {
         struct {
-            int16_t ckey[kWideCand];      // candidate keys (signed order-preserving), id order
+            union {
+                int16_t ckey[kWideCand];    // candidate keys (signed order-preserving), id order: bf16
+                int32_t ckey32[kWideCand];  // the same for fp32
+            };
             uint16_t cid[kWideCand];      // their block ids
             int32_t sorted[kOctMaxK];     // selected non-forced ids, ascending
         } c;
         uint32_t fallback[2 * kWideMaxCap];  // the warp path's keys and ids
     };
     uint32_t scratch[32][8];              // one 32-byte chunk per lane while candidates are read out
-    int16_t cmax[kWideHotChunks];         // raw maximum of each interior chunk (pass 1)
+    int16_t cmax[kWideHotChunks];         // each interior chunk's maximum (pass 1): bf16 raw, fp32 key's top 16 bits
     uint16_t hot[kWideHotChunks];         // the chunks pass 2 reads, ascending
 };
 

@@ -36,7 +36,7 @@
 //    lanes per row, 4 rows per warp; position maxima as representatives,
 //    packed sorting networks for theta, an id-ordered candidate list and an
 //    exact kappa search.
-//  * wide_select_kernel (bf16 rows over 2 KB, topk <= 64): the octet method
+//  * wide_select_kernel (rows over 2 KB, topk <= 64): the octet method
 //    with all 32 lanes on one row, and a list of the chunks that reach
 //    theta.  On a buffer wider than 2 KB (the 8192-tile capture-time
 //    capacity) the pair and octet kernels take every row whose range fits in
@@ -2457,11 +2457,9 @@ template <bool BF16>
 cudaError_t launch_octet(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
     auto kern = P.a.fused ? octet_select_kernel<BF16, kFusedYes, false>
                           : octet_select_kernel<BF16, kFusedNo, false>;
-    if constexpr (BF16) {
-        if (P.long_list != nullptr)
-            kern = P.a.fused ? octet_select_kernel<BF16, kFusedYes, true>
-                             : octet_select_kernel<BF16, kFusedNo, true>;
-    }
+    if (P.long_list != nullptr)
+        kern = P.a.fused ? octet_select_kernel<BF16, kFusedYes, true>
+                         : octet_select_kernel<BF16, kFusedNo, true>;
     if (pol.smem_bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              pol.smem_bytes);
@@ -2472,9 +2470,11 @@ cudaError_t launch_octet(const KernelParams& P, const bsa_launch_policy_t& pol, 
 }
 
 // ===========================================================================
-// Wide path: one warp per row, for bf16 rows of a buffer wider than 2 KB
-// (capacities above 1024 tiles, up to the 8192-tile capture-time capacity)
-// and topk <= 64.  The octet path's steps with all 32 lanes on one row:
+// Wide path: one warp per row, for rows of a buffer wider than 2 KB (bf16
+// capacities above 1024 tiles, fp32 above 512, up to the 8192-tile
+// capture-time capacity) and topk <= 64.  The octet path's steps with all 32
+// lanes on one row (fp32 as on the octet path: representatives and chunk
+// maxima are the top 16 bits of keys, and kappa searches 32-bit keys):
 //  1. the lanes stream the row's interior 32-byte chunks (chunk k to lane
 //     k mod 32, two loads in flight) and keep, per element position, the raw
 //     maximum and minimum: 16 representatives per lane, 512 per row, each
@@ -2517,10 +2517,11 @@ __device__ __forceinline__ int32_t max16(const uint32_t (&w)[NW]) {
 
 // LIST: the rows are the long_count entries of long_list (the pair or octet
 // path's long rows) and the grid is persistent; else rows 0 .. P.rows - 1.
-template <int FM, bool LIST>
+template <int FM, bool LIST, bool BF16>
 __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const KernelParams P) {
-    constexpr int CE = 16;                 // bf16 elements per 32-byte chunk
-    constexpr int32_t kKeyMin = -32768;
+    constexpr int S = BF16 ? 2 : 4;        // element bytes
+    constexpr int CE = 32 / S;             // elements per 32-byte chunk
+    constexpr int32_t kKeyMin = BF16 ? -32768 : INT32_MIN;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -2555,12 +2556,12 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
 
         // ---- geometry of the non-forced range [lo, hi), 32-byte chunks ----
         const char* row_ptr = reinterpret_cast<const char*>(a.scores) +
-                              ((int64_t)r.t * a.token_stride + (int64_t)r.h * a.head_stride) * 2;
-        const uintptr_t a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * 2;
-        const uintptr_t a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * 2;
+                              ((int64_t)r.t * a.token_stride + (int64_t)r.h * a.head_stride) * S;
+        const uintptr_t a_lo = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.lo * S;
+        const uintptr_t a_hi = reinterpret_cast<uintptr_t>(row_ptr) + (uintptr_t)r.hi * S;
         const uintptr_t c0 = a_lo & ~(uintptr_t)31;
         const int nchunk = (int)((a_hi - c0 + 31) >> 5);
-        const int base_id = r.lo - (int)((a_lo - c0) / 2);
+        const int base_id = r.lo - (int)((a_lo - c0) / S);
         {
             // the whole range towards L2, 4 KB per lane (a row is at most 128 KB)
             uintptr_t plo = c0 < P.buf_lo ? (P.buf_lo + 15) & ~(uintptr_t)15 : c0;
@@ -2574,25 +2575,41 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
         // ---- steps 1-2: representatives and theta ----
         int32_t theta = kKeyMin;
         if (r.hi - r.lo > kWideCand) {
+            // bf16: a raw maximum and minimum per element position (16 per
+            // lane); fp32: the key maximum per position in two sets by the
+            // chunk's parity (16 per lane), packed as the top 16 bits below
             uint32_t rmx[8], rmn[8];
+            int32_t ra[8], rb[8];
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
                 rmx[x] = 0x80008000u;
                 rmn[x] = 0x7FFF7FFFu;
+                ra[x] = rb[x] = INT32_MIN;
             }
-            auto fold = [&](const uint32_t (&w)[8]) {
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    rmx[x] = max_s16x2(rmx[x], w[x]);
-                    rmn[x] = min_s16x2(rmn[x], w[x]);
-                }
-            };
             // interior chunks 1 .. nchunk - 2; the edge chunks are left out.
-            // Rows of up to kWideHotChunks chunks also keep each chunk's raw
-            // maximum, so that pass 2 reads only the chunks that reach theta.
+            // Rows of up to kWideHotChunks chunks also keep each chunk's
+            // maximum (bf16: raw; fp32: the top 16 bits of its key maximum),
+            // so that pass 2 reads only the chunks that reach theta.
             const bool track = nchunk <= kWideHotChunks;
-            auto note = [&](int k, const uint32_t (&w)[8]) {
-                if (track) sm.cmax[k] = (int16_t)max16(w);
+            auto fold = [&](uint32_t (&w)[8], int k, bool second) {
+                if constexpr (BF16) {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        rmx[x] = max_s16x2(rmx[x], w[x]);
+                        rmn[x] = min_s16x2(rmn[x], w[x]);
+                    }
+                    if (track) sm.cmax[k] = (int16_t)max16(w);
+                } else {
+                    chunk_to_keys<false>(w);
+                    int32_t km = INT32_MIN;
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        if (second) rb[x] = max(rb[x], (int32_t)w[x]);
+                        else ra[x] = max(ra[x], (int32_t)w[x]);
+                        km = max(km, (int32_t)w[x]);
+                    }
+                    if (track) sm.cmax[k] = (int16_t)(km >> 16);
+                }
             };
             const int klast = nchunk - 2;
             int k = lane == 0 ? 32 : lane;
@@ -2601,25 +2618,29 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
                 uint32_t w0[8], w1[8];
                 ld32(c0 + ((uintptr_t)k << 5), w0);
                 ld32(c0 + ((uintptr_t)(k + 32) << 5), w1);
-                fold(w0);
-                fold(w1);
-                note(k, w0);
-                note(k + 32, w1);
+                fold(w0, k, false);
+                fold(w1, k + 32, true);
             }
             if (k <= klast) {
                 uint32_t w0[8];
                 ld32(c0 + ((uintptr_t)k << 5), w0);
-                fold(w0);
-                note(k, w0);
+                fold(w0, k, false);
             }
-            uint32_t rp[8];
+            uint32_t rp[8];   // 16 packed 16-bit representatives
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
-                // a position's largest key: its raw maximum when that is
-                // non-negative, else the key of its raw minimum
-                const uint32_t mneg = sign_mask16(rmx[x]);
-                rp[x] = any_interior ? (rmx[x] & ~mneg) | ((rmn[x] ^ 0x7FFF7FFFu) & mneg)
-                                     : 0x80008000u;
+                if constexpr (BF16) {
+                    // a position's largest key: its raw maximum when that is
+                    // non-negative, else the key of its raw minimum
+                    const uint32_t mneg = sign_mask16(rmx[x]);
+                    rp[x] = any_interior ? (rmx[x] & ~mneg) | ((rmn[x] ^ 0x7FFF7FFFu) & mneg)
+                                         : 0x80008000u;
+                } else {
+                    // the top 16 bits of the key maxima (a lower bound of each)
+                    const int32_t* src = x < 4 ? ra : rb;
+                    const int y = 2 * (x & 3);
+                    rp[x] = ((uint32_t)src[y] >> 16) | ((uint32_t)src[y + 1] & 0xFFFF0000u);
+                }
             }
             if (kp <= 32) {
                 // the kp-th largest of the lanes' largest representatives
@@ -2637,6 +2658,7 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
                     }
                 }
                 theta = __shfl_sync(kFull, v, kp - 1);
+                if constexpr (!BF16) theta = (int32_t)((uint32_t)theta << 16);
             } else {
                 // count(>= lo) >= kp throughout (every representative counts
                 // at the smallest key); stop at a 16-key interval
@@ -2646,7 +2668,7 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
                     if ((int)__reduce_add_sync(kFull, (unsigned)count_ge16(rp, mid)) >= kp) lo = mid;
                     else hi = mid;
                 }
-                theta = lo;
+                theta = BF16 ? lo : (int32_t)((uint32_t)lo << 16);
             }
         }
 
@@ -2661,7 +2683,8 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
             int tot = 0;
             for (int b0 = 0; b0 < nchunk; b0 += 32) {
                 const int k = b0 + lane;
-                const bool hot = k < nchunk && (k == 0 || k == nchunk - 1 || sm.cmax[k] >= theta);
+                const bool hot = k < nchunk && (k == 0 || k == nchunk - 1 ||
+                                                (int32_t)sm.cmax[k] >= (BF16 ? theta : theta >> 16));
                 const unsigned hb = __ballot_sync(kFull, hot);
                 if (hot) sm.hot[tot + __popc(hb & lanemask_lt())] = (uint16_t)k;
                 tot += __popc(hb);
@@ -2693,16 +2716,23 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
             if (has) {
                 if (!plain(k)) {
                     // masked keys, which compare like raw bits against theta >= 0
-                    pair_load_edge<true>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
+                    pair_load_edge<BF16>(P, k, c0, base_id, r.lo, r.hi, row_ptr, w);
                 } else {
 #pragma unroll
                     for (int x = 0; x < 8; ++x) w[x] = nx[x];
-                    if (!raw_ok) chunk_to_keys<true>(w);
+                    if (!raw_ok) chunk_to_keys<BF16>(w);
                 }
             }
             issue(st + 1);
             if (has) {
-                m = theta == kKeyMin ? 0xFFFFu : ge_bits16<8>(w, theta);
+                if (theta == kKeyMin) {
+                    m = (1u << CE) - 1u;
+                } else if constexpr (BF16) {
+                    m = ge_bits16<8>(w, theta);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) m |= ((int32_t)w[x] >= theta ? 1u : 0u) << x;
+                }
                 if (k == 0 || k == nchunk - 1) {
                     const int first_id = base_id + k * CE;
                     const int lo_e = min(max(r.lo - first_id, 0), CE);
@@ -2722,7 +2752,8 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
                     const int e = __ffs(m) - 1;
                     m &= m - 1;
                     if (pos < kWideCand) {
-                        sm.c.ckey[pos] = reinterpret_cast<const int16_t*>(scr)[e];
+                        if constexpr (BF16) sm.c.ckey[pos] = reinterpret_cast<const int16_t*>(scr)[e];
+                        else sm.c.ckey32[pos] = (int32_t)scr[e];
                         sm.c.cid[pos] = (uint16_t)(first_id + e);
                     }
                     ++pos;
@@ -2733,7 +2764,7 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
         __syncwarp();
         if (cbase > kWideCand) {
             // overflow: the whole warp redoes the row on the row path
-            warp_item<true, 4, 2>(P, row, 0, sm.fallback,
+            warp_item<BF16, 4, 2>(P, row, 0, sm.fallback,
                                   reinterpret_cast<int32_t*>(sm.fallback + P.cap), lane);
             __syncwarp();
             continue;
@@ -2741,37 +2772,76 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
 
         // ---- step 4: kappa, the K'-th largest candidate key ----
         // lane holds list positions 8 lane .. 8 lane + 7; padding holds the
-        // smallest key, which no searched threshold (> lo >= -32768) counts
+        // smallest key, which no searched threshold (> lo >= the smallest
+        // key) counts.  count(>= lo) >= K' > count(>= hi) = cnt_hi throughout.
         const int nvalid = min(max(cbase - 8 * lane, 0), 8);
         const uint32_t valid = (1u << nvalid) - 1u;
-        uint32_t kw[4];
-        {
-            const uint4 v = *reinterpret_cast<const uint4*>(&sm.c.ckey[8 * lane]);
-            kw[0] = v.x; kw[1] = v.y; kw[2] = v.z; kw[3] = v.w;
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const uint32_t keep = ((valid >> (2 * x)) & 1u ? 0x0000FFFFu : 0u) |
-                                      ((valid >> (2 * x + 1)) & 1u ? 0xFFFF0000u : 0u);
-                kw[x] = (kw[x] & keep) | (0x80008000u & ~keep);
-            }
-        }
-        // count(>= lo) >= K' > count(>= hi) = cnt_hi throughout
-        int32_t lo = theta, hi = __reduce_max_sync(kFull, max16(kw)) + 1;
+        uint32_t gtm = 0, eqm = 0;
         int cnt_hi = 0;
-        while (hi - lo > 1) {
-            const int32_t mid = (lo + hi) >> 1;
-            const int cnt = (int)__reduce_add_sync(kFull, (unsigned)count_ge16(kw, mid));
-            if (cnt >= kp) {
-                lo = mid;
-            } else {
-                hi = mid;
-                cnt_hi = cnt;
+        if constexpr (BF16) {
+            uint32_t kw[4];
+            {
+                const uint4 v = *reinterpret_cast<const uint4*>(&sm.c.ckey[8 * lane]);
+                kw[0] = v.x; kw[1] = v.y; kw[2] = v.z; kw[3] = v.w;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const uint32_t keep = ((valid >> (2 * x)) & 1u ? 0x0000FFFFu : 0u) |
+                                          ((valid >> (2 * x + 1)) & 1u ? 0xFFFF0000u : 0u);
+                    kw[x] = (kw[x] & keep) | (0x80008000u & ~keep);
+                }
+            }
+            int32_t lo = theta, hi = __reduce_max_sync(kFull, max16(kw)) + 1;
+            while (hi - lo > 1) {
+                const int32_t mid = (lo + hi) >> 1;
+                const int cnt = (int)__reduce_add_sync(kFull, (unsigned)count_ge16(kw, mid));
+                if (cnt >= kp) {
+                    lo = mid;
+                } else {
+                    hi = mid;
+                    cnt_hi = cnt;
+                }
+            }
+            // kappa = lo: every candidate above it, and the first (K' - count
+            // above) of those equal to it, in id order
+            gtm = ge_bits16<4>(kw, lo + 1) & valid;
+            eqm = (lo == kKeyMin ? valid : ge_bits16<4>(kw, lo) & valid) & ~gtm;
+        } else {
+            int32_t kk[8];
+            {
+                const int4* src = reinterpret_cast<const int4*>(&sm.c.ckey32[8 * lane]);
+                const int4 u0 = src[0], u1 = src[1];
+                kk[0] = u0.x; kk[1] = u0.y; kk[2] = u0.z; kk[3] = u0.w;
+                kk[4] = u1.x; kk[5] = u1.y; kk[6] = u1.z; kk[7] = u1.w;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (!((valid >> e) & 1u)) kk[e] = INT32_MIN;
+            }
+            int32_t mx = kk[0];
+#pragma unroll
+            for (int e = 1; e < 8; ++e) mx = max(mx, kk[e]);
+            int64_t lo = theta, hi = (int64_t)__reduce_max_sync(kFull, mx) + 1;
+            while (hi - lo > 1) {
+                const int64_t mid = lo + ((hi - lo) >> 1);
+                const int32_t t = (int32_t)mid;
+                int c = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) c += kk[e] >= t ? 1 : 0;
+                const int cnt = (int)__reduce_add_sync(kFull, (unsigned)c);
+                if (cnt >= kp) {
+                    lo = mid;
+                } else {
+                    hi = mid;
+                    cnt_hi = cnt;
+                }
+            }
+            const int32_t kappa = (int32_t)lo;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const bool vd = (valid >> e) & 1u;
+                if (vd && kk[e] > kappa) gtm |= 1u << e;
+                if (vd && kk[e] == kappa) eqm |= 1u << e;
             }
         }
-        // kappa = lo: every candidate above it, and the first (K' - count
-        // above) of those equal to it, in id order
-        const uint32_t gtm = ge_bits16<4>(kw, lo + 1) & valid;
-        const uint32_t eqm = (lo == kKeyMin ? valid : ge_bits16<4>(kw, lo) & valid) & ~gtm;
         int tall;
         const int tb = warp_excl_scan(__popc(eqm), lane, tall);
         const int allowed = min(max(kp - cnt_hi - tb, 0), __popc(eqm));
@@ -2794,8 +2864,10 @@ __global__ void __launch_bounds__(kWideWarps * 32) wide_select_kernel(const Kern
     }
 }
 
+template <bool BF16>
 cudaError_t launch_wide(const KernelParams& P, const bsa_launch_policy_t& pol, cudaStream_t st) {
-    auto kern = P.a.fused ? wide_select_kernel<kFusedYes, false> : wide_select_kernel<kFusedNo, false>;
+    auto kern = P.a.fused ? wide_select_kernel<kFusedYes, false, BF16>
+                          : wide_select_kernel<kFusedNo, false, BF16>;
     kern<<<pol.grid, kWideWarps * 32, pol.smem_bytes, st>>>(P);
     return cudaGetLastError();
 }
@@ -2803,9 +2875,12 @@ cudaError_t launch_wide(const KernelParams& P, const bsa_launch_policy_t& pol, c
 // The second launch of a pair / octet call with long_rows: the listed rows.
 cudaError_t launch_wide_list(const KernelParams& P, const bsa_launch_policy_t& pol,
                              cudaStream_t st) {
-    if (P.a.dtype != BSA_DTYPE_BF16 || P.cap > kWideMaxCap || pol.long_grid < 1)
-        return cudaErrorInvalidValue;
-    auto kern = P.a.fused ? wide_select_kernel<kFusedYes, true> : wide_select_kernel<kFusedNo, true>;
+    if (P.cap > kWideMaxCap || pol.long_grid < 1) return cudaErrorInvalidValue;
+    const bool bf16 = P.a.dtype == BSA_DTYPE_BF16;
+    auto kern = P.a.fused ? (bf16 ? wide_select_kernel<kFusedYes, true, true>
+                                  : wide_select_kernel<kFusedYes, true, false>)
+                          : (bf16 ? wide_select_kernel<kFusedNo, true, true>
+                                  : wide_select_kernel<kFusedNo, true, false>);
     kern<<<pol.long_grid, kWideWarps * 32, kWideWarps * (int)sizeof(WideSmem), st>>>(P);
     return cudaGetLastError();
 }
@@ -3196,13 +3271,16 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
                                          : launch_group<false>(P, pol, stream);
     if (pol.long_rows) {
         // rows over 2 KB: listed by the pair / octet kernel, then the wide path
-        if (ws.long_list == nullptr || ws.long_count == nullptr || a.dtype != BSA_DTYPE_BF16 ||
+        if (ws.long_list == nullptr || ws.long_count == nullptr ||
             (pol.path != BSA_PATH_PAIR && pol.path != BSA_PATH_OCTET))
             return cudaErrorInvalidValue;
         P.long_list = ws.long_list;
         P.long_count = ws.long_count;
-        const cudaError_t e = pol.path == BSA_PATH_PAIR ? launch_pair<true>(P, pol, stream)
-                                                        : launch_octet<true>(P, pol, stream);
+        const bool bf16 = a.dtype == BSA_DTYPE_BF16;
+        const cudaError_t e =
+            pol.path == BSA_PATH_PAIR
+                ? (bf16 ? launch_pair<true>(P, pol, stream) : launch_pair<false>(P, pol, stream))
+                : (bf16 ? launch_octet<true>(P, pol, stream) : launch_octet<false>(P, pol, stream));
         if (e != cudaSuccess) return e;
         return launch_wide_list(P, pol, stream);
     }
@@ -3213,8 +3291,9 @@ cudaError_t launch_select(const SelectArgs& a, const bsa_launch_policy_t& pol,
         return a.dtype == BSA_DTYPE_BF16 ? launch_octet<true>(P, pol, stream)
                                          : launch_octet<false>(P, pol, stream);
     if (pol.path == BSA_PATH_WIDE) {
-        if (a.dtype != BSA_DTYPE_BF16 || pol.cand_capacity > kWideMaxCap) return cudaErrorInvalidValue;
-        return launch_wide(P, pol, stream);
+        if (pol.cand_capacity > kWideMaxCap) return cudaErrorInvalidValue;
+        return a.dtype == BSA_DTYPE_BF16 ? launch_wide<true>(P, pol, stream)
+                                         : launch_wide<false>(P, pol, stream);
     }
     return a.dtype == BSA_DTYPE_BF16 ? launch_dt<true>(P, pol, stream)
                                      : launch_dt<false>(P, pol, stream);

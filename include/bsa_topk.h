@@ -295,9 +295,9 @@ int bsa_topk_select_noalloc(const void* scores, int32_t dtype, int64_t T, int64_
  * Paths: BSA_PATH_PAIR when K <= 32 and a row holds at most 2 KB (M * element
  * size <= 2048), BSA_PATH_OCTET when 32 < K <= 64 and a row holds at most
  * 2 KB; BSA_PATH_SPLIT when a row needs more than one pass and the rows
- * alone cannot fill the GPU (at most num_sms * 16 rows); otherwise, for bf16
- * rows of more than 2 KB (M > 1024, up to the 8192-tile capture-time
- * capacity and beyond) with K <= 64, BSA_PATH_PAIR or BSA_PATH_OCTET with
+ * alone cannot fill the GPU (at most num_sms * 16 rows); otherwise, for rows
+ * of more than 2 KB (bf16 M > 1024, fp32 M > 512, up to the 8192-tile
+ * capture-time capacity and beyond) with K <= 64, BSA_PATH_PAIR or BSA_PATH_OCTET with
  * long_rows = 1: those paths take every row whose non-forced range fits in
  * 2 KB and list the others, which a second launch on the same stream takes
  * with the wide path (one warp per row); BSA_PATH_ROW for the rest.  The

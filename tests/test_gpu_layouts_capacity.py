@@ -120,12 +120,9 @@ def test_prefill_heavy_batch_at_full_capacity(cuda_device, dtype, K, L):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     pol = bsa.bsa_select_policy(T * H, M, K, dt, sms)
     assert pol["chunks_per_row"] == 1, "thousands of rows must not take the split path"
-    if dtype == torch.bfloat16:
-        # rows within 2 KB on the pair / octet path, the rest on the wide path
-        assert pol["path"] == (bsa.BSA_PATH_PAIR if K <= 32 else bsa.BSA_PATH_OCTET)
-        assert pol["long_rows"] == 1
-    else:
-        assert pol["path"] == bsa.BSA_PATH_ROW and pol["long_rows"] == 0
+    # rows within 2 KB on the pair / octet path, the rest on the wide path
+    assert pol["path"] == (bsa.BSA_PATH_PAIR if K <= 32 else bsa.BSA_PATH_OCTET)
+    assert pol["long_rows"] == 1
     out = bsa.bsa_topk_select(w.scores, nvp, K, 1, L)
     torch.cuda.synchronize()
     _props.check_selection(w.scores, nvp, out, K, 1, L)

@@ -1,4 +1,4 @@
-"""bf16 buffers wider than 2 KB with topk <= 64 and more than num_sms * 16
+"""bf16 and fp32 buffers wider than 2 KB with topk <= 64 and more than num_sms * 16
 rows (needs a GB300): the launch policy sends them to the pair or octet path,
 which takes every row whose non-forced range fits in 2 KB and lists the
 others for a second launch, the wide path (one warp per row).  Every row is
@@ -29,19 +29,20 @@ def _rows_for_wide(dev):
     return 32 * torch.cuda.get_device_properties(dev).multi_processor_count
 
 
-def _scores(T, H, width, seed, dev):
-    """bf16 N(0, 1) [T, H, width] with specials and ties, and every 97th row
-    one repeated value (ties everywhere)."""
-    sc = synth.normal_scores((T, H, width), torch.bfloat16, seed, dev)
+def _scores(T, H, width, seed, dev, dtype=torch.bfloat16):
+    """N(0, 1) [T, H, width] with specials and ties, and every 97th row one
+    repeated value (ties everywhere)."""
+    sc = synth.normal_scores((T, H, width), dtype, seed, dev)
     synth.inject_specials(sc, seed=seed + 1, frac_each=0.002, frac_ties=0.02)
     flat = sc.view(T * H, width)
     flat[::97] = 0.75
     return sc
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("K,I,L", [(1, 0, 0), (16, 1, 2), (33, 1, 1), (64, 1, 2)])
 @pytest.mark.parametrize("M,pad", [(2048, 0), (8192, 8), (1500, 5)])
-def test_wide_select_matches_oracle(cuda_device, K, I, L, M, pad):
+def test_wide_select_matches_oracle(cuda_device, K, I, L, M, pad, dtype):
     dev = cuda_device
     H = 2
     T = (_rows_for_wide(dev) + 255) // H
@@ -52,11 +53,12 @@ def test_wide_select_matches_oracle(cuda_device, K, I, L, M, pad):
     nvp_host[::5] = g.integers(0, 300, len(nvp_host[::5]))
     nvp_host[1::11] = 256 + I + L + g.integers(0, 3, len(nvp_host[1::11]))
     nvp_host[2::13] = M
-    big = _scores(T, H, M + pad, seed=M + K, dev=dev)
+    big = _scores(T, H, M + pad, seed=M + K, dev=dev, dtype=dtype)
     scores = big[:, :, :M]                       # rows start off 32-byte boundaries when pad > 0
     nvp = torch.from_numpy(nvp_host).to(dev)
     synth.fill_tail(scores, nvp, float("-inf"))
-    pol = bsa.bsa_select_policy(T * H, M, K, bsa.BSA_DTYPE_BF16,
+    dt = bsa.BSA_DTYPE_BF16 if dtype == torch.bfloat16 else bsa.BSA_DTYPE_FP32
+    pol = bsa.bsa_select_policy(T * H, M, K, dt,
                                 torch.cuda.get_device_properties(dev).multi_processor_count)
     assert pol["path"] in (bsa.BSA_PATH_PAIR, bsa.BSA_PATH_OCTET) and pol["long_rows"] == 1
     got = bsa.bsa_topk_select(scores, nvp, K, I, L)
@@ -66,8 +68,9 @@ def test_wide_select_matches_oracle(cuda_device, K, I, L, M, pad):
     assert bad[0].size == 0, f"{bad[0].size} rows differ, first (t, h) = {bad[0][0]}, {bad[1][0]}"
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("K", [16, 64])
-def test_wide_fused_table_matches_oracle(cuda_device, K):
+def test_wide_fused_table_matches_oracle(cuda_device, K, dtype):
     """Decode rows of a 2048-tile buffer through the fused select + table."""
     dev = cuda_device
     dql, H, M = 2, 2, 2048
@@ -78,7 +81,7 @@ def test_wide_fused_table_matches_oracle(cuda_device, K):
     seq[1::7] = torch.randint(1, 300 * 128, (len(seq[1::7]),), generator=g, dtype=torch.int32)
     table = synth.paged_block_table(B, M, B * M, seed=K + 3)
     T = B * dql
-    scores = _scores(T, H, M, seed=K + 5, dev=dev)
+    scores = _scores(T, H, M, seed=K + 5, dev=dev, dtype=dtype)
     nvp = oracle.num_valid_pages_decode(seq.numpy(), dql)
     synth.fill_tail(scores, torch.from_numpy(nvp).to(dev), float("-inf"))
     idx, bt, ctx = bsa.bsa_topk_select_sparse_table(scores, seq.to(dev), dql, K, 1, 2,
