@@ -56,7 +56,8 @@ constexpr int kPairMaxChunks = 66;   // 32-byte chunks per row (2 KB + alignment
 constexpr int kPairStepsPad = 40;    // >= ceil(kPairMaxChunks / 2), multiple of 8
 constexpr int kPairCand = 32;        // candidate capacity per row (one 2-lane sort)
 constexpr int kPairWarps = 4;        // warps per CTA
-constexpr int kPairCtas = 5;         // CTAs per SM the kernel's register bound allows
+constexpr int kPairCtas = 5;         // CTAs per SM the fused kernel's register bound allows
+constexpr int kPairCtasSelect = 6;   // the same for the plain bf16 select (no table epilogue)
 
 struct PairRowDesc {
     unsigned long long c0;       // first 32-byte chunk of the non-forced range
@@ -94,6 +95,8 @@ constexpr int kOctRows = 4;          // rows per warp
 constexpr int kOctCand = 128;        // candidate capacity per row (16 per lane)
 constexpr int kOctMaxK = 64;         // largest topk the octet path serves
 constexpr int kOctWarps = 4;         // warps per CTA
+constexpr int kOctCtas = 6;          // CTAs per SM of the fused kernel (register bound)
+constexpr int kOctCtasSelect = 7;    // the same for the plain bf16 select
 
 struct OctSmem {
     union {

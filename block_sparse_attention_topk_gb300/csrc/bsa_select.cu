@@ -1565,7 +1565,11 @@ __device__ __forceinline__ void pair_top16_desc(T (&x)[16]) {
 }
 
 template <bool BF16, bool SMALLK, int FM>
-__global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel(const KernelParams P) {
+// The plain bf16 select needs fewer registers than the fused kernel, whose
+// table epilogue holds 8 gathers in flight: more of its CTAs fit on an SM.
+__global__ void __launch_bounds__(kPairWarps * 32,
+                                  FM == kFusedNo && BF16 ? kPairCtasSelect : kPairCtas)
+    pair_select_kernel(const KernelParams P) {
     using E = Elem<BF16>;
     using CK = typename std::conditional<BF16, uint32_t, unsigned long long>::type;
     using G = PairSmem<CK>;
@@ -1581,21 +1585,23 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
     const int s = lane & 1;    // lane within the row's pair
     G& sm = *reinterpret_cast<G*>(smem_raw + (size_t)warp * sizeof(G));
     const SelectArgs& a = P.a;
-    const int64_t nitems = (P.rows + kPairRows - 1) / kPairRows;
-    const int64_t stride = (int64_t)gridDim.x * kPairWarps;
+    // rows < 2^31 (checked on the host), so items and the policy's grid fit int
+    const int nitems = (int)((P.rows + kPairRows - 1) / kPairRows);
+    const int stride = (int)gridDim.x * kPairWarps;
 
-    int64_t it = (int64_t)blockIdx.x * kPairWarps + warp;
+    int it = (int)blockIdx.x * kPairWarps + warp;
     int32_t meta = 0;
-    if (it < nitems && it * kPairRows + p < P.rows) meta = row_meta<FM>(a, it * kPairRows + p);
+    if (it < nitems && (int64_t)it * kPairRows + p < P.rows) meta = row_meta<FM>(a, (int64_t)it * kPairRows + p);
     for (; it < nitems; it += stride) {
-        const int64_t row = it * kPairRows + p;
+        const int64_t row = (int64_t)it * kPairRows + p;
         const bool active = row < P.rows;
-        const int64_t nrow = (it + stride) * kPairRows + p;
-        const bool nactive = it + stride < nitems && nrow < P.rows;
+        const int64_t nrow = ((int64_t)it + stride) * kPairRows + p;
+        const bool nactive = (int64_t)it + stride < nitems && nrow < P.rows;
         const int32_t nmeta = nactive ? row_meta<FM>(a, nrow) : 0;
         RowInfo r{};
         r.all = true;
         if (active) r = row_info_from<FM>(a, row, meta);
+        const int32_t cur_meta = meta;
         meta = nmeta;
         // a row whose range exceeds 2 KB (a wider buffer) goes to the list of
         // the second, wide-path launch
@@ -1917,6 +1923,17 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         }
         __syncwarp();
 
+        {
+            // the row's geometry again from its page count (passed through an
+            // opaque move, so that the compiler recomputes it rather than
+            // holding it in registers through the candidate phase)
+            int32_t m2;
+            asm volatile("mov.b32 %0, %1;" : "=r"(m2) : "r"(cur_meta));
+            RowInfo r2{};
+            r2.all = true;
+            if (active) r2 = row_info_from<FM>(a, row, m2);
+            r = r2;
+        }
         // ---- exact select: sort the row's candidates, keep the first K' ----
         const bool ovf = sm.ovf[p] != 0;
         const int cn = min(sm.ccount[p], kPairCand);
@@ -1992,7 +2009,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, kPairCtas) pair_select_kernel
         while (fb) {
             const int bit = __ffs(fb) - 1;
             fb &= fb - 1;
-            const int64_t frow = it * kPairRows + (bit >> 1);
+            const int64_t frow = (int64_t)it * kPairRows + (bit >> 1);
             uint32_t* s_keys = reinterpret_cast<uint32_t*>(&sm);
             warp_item<BF16, 4, 2>(P, frow, 0, s_keys, reinterpret_cast<int32_t*>(s_keys + P.cap),
                                   lane);
@@ -2099,7 +2116,9 @@ __device__ __forceinline__ int32_t oct_theta(uint32_t (&rp)[8], int q) {
 // TAIL: rows over 2 KB are listed for the wide path (buffers wider than
 // 2 KB); without it the kernel has none of that code.
 template <bool BF16, int FM, bool TAIL>
-__global__ void __launch_bounds__(kOctWarps * 32, 6) octet_select_kernel(const KernelParams P) {
+__global__ void __launch_bounds__(kOctWarps * 32,
+                                  FM == kFusedNo && BF16 ? kOctCtasSelect : kOctCtas)
+    octet_select_kernel(const KernelParams P) {
     using E = Elem<BF16>;
     constexpr int S = E::kBytes;
     constexpr int CE = 32 / S;                      // elements per 32-byte chunk
